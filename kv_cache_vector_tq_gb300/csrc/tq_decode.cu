@@ -1,0 +1,545 @@
+// Split-sequence decode attention over a TurboQuant_MSE KV cache (d = 128).
+//
+// "TurboQuant 详解", section decode 阶段到底怎么“用”这些压缩后的 KV (second
+// route): the kernel unpacks, looks up, scales and consumes the codes inside
+// attention, never materialising fp16 K/V.  "sub-byte-kv-cache-quantization-
+// turboquant", section 工程实现的关键路径: the query is rotated once and every
+// query head reads kv_head = q_head / (Hq / Hkv).
+//
+// Per (batch, kv head) the token range is cut into work items; a persistent
+// CTA takes an item, pulls its K codes, V pair blocks and norms into shared
+// memory with bulk asynchronous copies completing on one mbarrier, and its 8
+// warps process 16-token tiles:
+//   K side  S[t][n] = Σ_κ K̂[t][κ]·Q[κ][n]      (mma.m16n8k16, A built from a
+//           shared-memory pair table, B = pre-rotated queries, hi/lo columns)
+//   softmax online per head, base-2 logits with the scale folded into Q
+//   V side  O[μ][n] += Σ_t V̂[μ][t]·W[t][n]     (A from V pair blocks, which
+//           hold the codes of two consecutive tokens side by side; B = p·s_v)
+// O stays in the rotated domain: Σ_t p_t s_t Πᵀŷ_t = Πᵀ Σ_t p_t s_t ŷ_t, so the
+// merge kernel applies Πᵀ once per head after combining the splits with the
+// usual log-sum-exp rule.
+#include <algorithm>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+constexpr int kTileTok = 16;
+constexpr int kMaxTilesPerItem = 32;
+constexpr int kDecWarps = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazy = 8.f;          // rescale only when the max grows by > 2^8
+constexpr uint32_t kSpinLimit = 1u << 22;  // bounded mbarrier wait (~0.1-1 s)
+
+struct DecPlan {
+  int S;           // splits (work items) per (batch, kv head)
+  int tiles;       // tiles per (batch, kv head)
+  int per_item;    // tiles per item (last one may have fewer)
+  int NT;          // 8-column n-tiles (2·G columns)
+};
+
+static DecPlan make_plan(int B, int Hq, int Hkv, int64_t seq, int tmax = 8) {
+  DecPlan pl;
+  pl.tiles = (int)((seq + kTileTok - 1) / kTileTok);
+  const int groups = std::max(1, B * Hkv);
+  const int target = 2 * num_sms();
+  int S = std::max((pl.tiles + tmax - 1) / tmax, (target + groups - 1) / groups);
+  S = std::max(1, std::min(S, pl.tiles));
+  pl.per_item = (pl.tiles + S - 1) / S;
+  pl.S = (pl.tiles + pl.per_item - 1) / pl.per_item;
+  const int G = Hkv > 0 ? Hq / Hkv : 1;
+  pl.NT = (2 * G + 7) / 8;
+  return pl;
+}
+
+size_t decode_ws_bytes(int d, int B, int Hq, int Hkv, int64_t seq) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || seq <= 0) return 256;
+  DecPlan pl = make_plan(B, Hq, Hkv, seq, 8);  // tmax 8 gives the most splits: an upper bound
+  size_t frag = (size_t)B * Hkv * 8 * pl.NT * 32 * sizeof(uint2);
+  size_t part = (size_t)B * Hq * pl.S * (2 + 128) * sizeof(float);
+  return (frag + 255) / 256 * 256 + part + 256;
+}
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------------ query prep
+// One block per (batch, kv head): q̂_h = Π·q_h for the G query heads of the
+// group, folded with scale·log2(e)/(√d·α_K), split into fp16 hi (column 2h) and
+// lo (column 2h+1) B fragments:  b0 = (K index 16s+2t.., col g),
+// b1 = (16s+8+2t.., col g), K index 16s+8h+2t+e <-> coordinate 32t+4s+2h+e.
+__global__ void decode_qprep_kernel(const DevCtx kc, const void* __restrict__ q, int q_f16, int Hq,
+                                    int G, int NT, float fold, uint2* __restrict__ frag) {
+  __shared__ float qs[8][128];
+  __shared__ float qr[8][128];
+  const int bk = blockIdx.x;  // b * Hkv + kvh
+  const int i = threadIdx.x;  // 128 threads
+  const int Hkv = Hq / G;
+  const int b = bk / Hkv, kvh = bk % Hkv;
+  for (int h = 0; h < G; ++h) {
+    const int64_t off = ((int64_t)b * Hq + kvh * G + h) * 128 + i;
+    qs[h][i] = q_f16 ? __half2float(static_cast<const __half*>(q)[off]) : static_cast<const float*>(q)[off];
+  }
+  __syncthreads();
+  for (int h = 0; h < G; ++h) {
+    float a = 0.f;
+    for (int k = 0; k < 128; ++k) a = fmaf(kc.pi[i * 128 + k], qs[h][k], a);
+    qr[h][i] = a * fold;
+  }
+  __syncthreads();
+  // entries: s (8) x nt (NT) x lane (32)
+  for (int e = i; e < 8 * NT * 32; e += blockDim.x) {
+    const int lane = e & 31, nt = (e >> 5) % NT, s = e / (32 * NT);
+    const int g = lane >> 2, t = lane & 3;
+    const int n = nt * 8 + g, h = n >> 1, lo = n & 1;
+    uint2 f = make_uint2(0u, 0u);
+    if (h < G) {
+      const int c0 = 32 * t + 4 * s;
+      float v[4];
+      for (int u = 0; u < 4; ++u) {
+        const float x = qr[h][c0 + u];
+        const float hi = __half2float(__float2half_rn(x));
+        v[u] = lo ? (x - hi) : hi;
+      }
+      f.x = pack_f16x2(v[0], v[1]);
+      f.y = pack_f16x2(v[2], v[3]);
+    }
+    frag[((size_t)bk * 8 + s) * NT * 32 + nt * 32 + lane] = f;
+  }
+}
+
+// Shared-memory layout of the split kernel (byte offsets, host-computed).
+struct DecSmem {
+  int off_vlut, off_kc, off_vc, off_kn, off_vn, off_bar, bytes;
+  int tmax;  // tiles per work item at most
+};
+
+static DecSmem dec_smem(int bk, int bv, int G, bool same_lut) {
+  DecSmem m;
+  const int lutk = (1 << (2 * bk)) * 32 * 4, lutv = same_lut ? 0 : (1 << (2 * bv)) * 32 * 4;
+  const int comb = kDecWarps * G * 130 * 4;
+  const int per_tile = kTileTok * (4 * bk + 4 * bv) * 4 + 2 * kTileTok * 4;
+  const int budget = 110 * 1024 - lutk - lutv - 64;
+  int tmax = budget / per_tile;
+  tmax = std::max(8, std::min(kMaxTilesPerItem, tmax / 8 * 8));
+  m.tmax = tmax;
+  m.off_vlut = lutk;
+  m.off_kc = lutk + lutv;
+  m.off_vc = m.off_kc + tmax * kTileTok * 4 * bk * 4;
+  m.off_kn = m.off_vc + tmax * kTileTok * 4 * bv * 4;
+  m.off_vn = m.off_kn + tmax * kTileTok * 4;
+  int end_stage = m.off_vn + tmax * kTileTok * 4;
+  int end_comb = m.off_kc + comb;  // the warp-combine scratch reuses the staging area
+  m.off_bar = (std::max(end_stage, end_comb) + 15) / 16 * 16;
+  m.bytes = m.off_bar + 64;
+  return m;
+}
+
+// ------------------------------------------------------------------ split kernel
+struct DecParams {
+  const uint32_t* klut;  // global tables (copied to shared memory)
+  const uint32_t* vlut;
+  float v_fold;          // 1 / (α_V √d)
+  const uint32_t* kcodes;
+  const float* knorm;
+  const uint32_t* vcodes;
+  const float* vnorm;
+  int64_t seq, cap;
+  int B, Hq, Hkv, G;
+  DecPlan pl;
+  const uint2* qfrag;
+  float* part;           // [B*Hq][S][130]: m, l, acc[128]
+  int* status;
+  DecSmem sm;
+  int same_lut;
+};
+
+template <int BK, int BV, int G>
+__global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p) {
+  constexpr int NT = (2 * G + 7) / 8;
+  constexpr int WK = 4 * BK, WV = 4 * BV;  // words per vector (d = 128)
+  constexpr int EK = 1 << (2 * BK), EV = 1 << (2 * BV);
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint32_t* klut = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* vlut = p.same_lut ? klut : reinterpret_cast<uint32_t*>(smem + p.sm.off_vlut);
+  uint32_t* skc = reinterpret_cast<uint32_t*>(smem + p.sm.off_kc);
+  uint32_t* svc = reinterpret_cast<uint32_t*>(smem + p.sm.off_vc);
+  float* skn = reinterpret_cast<float*>(smem + p.sm.off_kn);
+  float* svn = reinterpret_cast<float*>(smem + p.sm.off_vn);
+  float* comb = reinterpret_cast<float*>(smem + p.sm.off_kc);  // reused after the tile loop
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + p.sm.off_bar);
+  volatile int& s_abort = *reinterpret_cast<int*>(smem + p.sm.off_bar + 16);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  for (int i = tid; i < EK * 32; i += blockDim.x) klut[i] = p.klut[i >> 5];
+  if (!p.same_lut)
+    for (int i = tid; i < EV * 32; i += blockDim.x) vlut[i] = p.vlut[i >> 5];
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  __syncthreads();
+
+  const int groups = p.B * p.Hkv;
+  const int n_items = groups * p.pl.S;
+  uint32_t phase = 0;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int bk = item / p.pl.S, sp = item % p.pl.S;
+    const int tile0 = sp * p.pl.per_item;
+    const int ntl = min(p.pl.per_item, p.pl.tiles - tile0);
+    const int64_t tok0 = (int64_t)tile0 * kTileTok;
+    const int ntok = ntl * kTileTok;  // staged tokens (whole tiles, inside cap)
+    const int64_t vbase = (int64_t)bk * p.cap + tok0;  // vector index of the first token
+    if (tid == 0) {
+      const uint32_t kb = (uint32_t)ntok * WK * 4, vb = (uint32_t)ntok * WV * 4,
+                     nb = (uint32_t)ntok * 4;
+      fence_proxy_async();
+      mbar_arrive_expect_tx(bar, kb + vb + 2 * nb);
+      bulk_g2s(skc, p.kcodes + vbase * WK, kb, bar);
+      bulk_g2s(svc, p.vcodes + vbase * WV, vb, bar);  // vbase even: pair blocks align
+      bulk_g2s(skn, p.knorm + vbase, nb, bar);
+      bulk_g2s(svn, p.vnorm + vbase, nb, bar);
+    }
+    // ---- bounded wait for the item's bytes
+    {
+      uint32_t spins = 0;
+      bool ok = false;
+      while (!(ok = mbar_try_wait(bar, phase)) && ++spins < kSpinLimit) {
+      }
+      if (!ok) {
+        atomicExch(p.status, 1);
+        s_abort = 1;
+      }
+    }
+    phase ^= 1u;
+    __syncthreads();
+    if (s_abort) {
+      if (tid == 0) {  // let the copies in flight land before leaving (bounded)
+        uint32_t spins = 0;
+        while (!mbar_try_wait(bar, phase ^ 1u) && ++spins < kSpinLimit) {
+        }
+      }
+      return;
+    }
+
+    // ---- per-warp state
+    uint2 qf[8][NT];
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) qf[s][nt] = p.qfrag[((size_t)bk * 8 + s) * NT * 32 + nt * 32 + lane];
+    float m_run[NT], l_run[NT];
+    float o[8][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m_run[nt] = -INFINITY;
+      l_run[nt] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+    }
+    const uint32_t* mykl = klut + lane;
+    const uint32_t* myvl = vlut + lane;
+
+    for (int tl = warp; tl < ntl; tl += kDecWarps) {
+      const int lt0 = tl * kTileTok;  // local token index of the tile
+      // ---------------- K side
+      uint32_t kw0[BK], kw1[BK];
+#pragma unroll
+      for (int w = 0; w < BK; ++w) {
+        kw0[w] = skc[(lt0 + g) * WK + t * BK + w];
+        kw1[w] = skc[(lt0 + g + 8) * WK + t * BK + w];
+      }
+      float sa[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) sa[nt][0] = sa[nt][1] = sa[nt][2] = sa[nt][3] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t a0 = mykl[get_bits<2 * BK>(kw0, 4 * s * BK) << 5];
+        const uint32_t a1 = mykl[get_bits<2 * BK>(kw1, 4 * s * BK) << 5];
+        const uint32_t a2 = mykl[get_bits<2 * BK>(kw0, (4 * s + 2) * BK) << 5];
+        const uint32_t a3 = mykl[get_bits<2 * BK>(kw1, (4 * s + 2) * BK) << 5];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(sa[nt], a0, a1, a2, a3, qf[s][nt].x, qf[s][nt].y);
+      }
+      const float sk0 = skn[lt0 + g], sk1 = skn[lt0 + g + 8];
+      const bool v0 = tok0 + lt0 + g < p.seq, v1 = tok0 + lt0 + g + 8 < p.seq;
+      const float sv0 = svn[lt0 + g], sv1 = svn[lt0 + g + 8];
+      // ---------------- online softmax per head h = 4nt + t (lanes of equal t)
+      float w0[NT], w1[NT];  // p·s_v·fold for tokens g, g+8 of head 4nt+t
+      bool need = false;
+      float zz0[NT], zz1[NT], mx[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        zz0[nt] = v0 ? (sa[nt][0] + sa[nt][1]) * sk0 : -INFINITY;
+        zz1[nt] = v1 ? (sa[nt][2] + sa[nt][3]) * sk1 : -INFINITY;
+        float m = fmaxf(zz0[nt], zz1[nt]);
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 16));
+        mx[nt] = m;
+        need |= m > m_run[nt] + kLazy;
+      }
+      if (__any_sync(kFull, need)) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          if (mx[nt] > m_run[nt] + kLazy) {
+            const float f = (m_run[nt] == -INFINITY) ? 0.f : ex2(m_run[nt] - mx[nt]);
+            m_run[nt] = mx[nt];
+            l_run[nt] *= f;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) o[mt][nt][e] *= f;
+          }
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float p0 = (m_run[nt] == -INFINITY) ? 0.f : ex2(zz0[nt] - m_run[nt]);
+        const float p1 = (m_run[nt] == -INFINITY) ? 0.f : ex2(zz1[nt] - m_run[nt]);
+        l_run[nt] += p0 + p1;
+        w0[nt] = p0 * sv0 * p.v_fold;
+        w1[nt] = p1 * sv1 * p.v_fold;
+      }
+      // ---------------- V side: B[k = token][n = col g] for tokens 2t,2t+1,2t+8,2t+9
+      uint32_t bw[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int h4 = (g >> 1);  // head within this n-tile (col g = 2·h4 + lo)
+        const int src0 = 4 * (2 * t) + h4, src1 = 4 * (2 * t + 1) + h4;
+        const float x0 = __shfl_sync(kFull, w0[nt], src0);  // token 2t
+        const float x1 = __shfl_sync(kFull, w0[nt], src1);  // token 2t+1
+        const float x2 = __shfl_sync(kFull, w1[nt], src0);  // token 2t+8
+        const float x3 = __shfl_sync(kFull, w1[nt], src1);  // token 2t+9
+        const bool lo = g & 1;
+        const bool head_ok = 4 * nt + h4 < G;
+        float y0 = x0, y1 = x1, y2 = x2, y3 = x3;
+        const float hi0 = __half2float(__float2half_rn(x0)), hi1 = __half2float(__float2half_rn(x1));
+        const float hi2 = __half2float(__float2half_rn(x2)), hi3 = __half2float(__float2half_rn(x3));
+        if (lo) {
+          y0 = x0 - hi0; y1 = x1 - hi1; y2 = x2 - hi2; y3 = x3 - hi3;
+        }
+        bw[nt][0] = head_ok ? pack_f16x2(y0, y1) : 0u;
+        bw[nt][1] = head_ok ? pack_f16x2(y2, y3) : 0u;
+      }
+      // V pair blocks t and t+4 of the tile; this lane's BV words at g·BV
+      uint32_t vw0[BV], vw1[BV];
+      const int pb0 = (lt0 >> 1) + t, pb1 = pb0 + 4;
+#pragma unroll
+      for (int w = 0; w < BV; ++w) {
+        vw0[w] = svc[pb0 * (2 * WV) + g * BV + w];
+        vw1[w] = svc[pb1 * (2 * WV) + g * BV + w];
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        // rows g / g+8 <-> coordinates 16g + 2mt / 16g + 2mt + 1
+        const uint32_t a0 = myvl[get_bits<2 * BV>(vw0, (2 * mt) * 2 * BV) << 5];
+        const uint32_t a1 = myvl[get_bits<2 * BV>(vw0, (2 * mt + 1) * 2 * BV) << 5];
+        const uint32_t a2 = myvl[get_bits<2 * BV>(vw1, (2 * mt) * 2 * BV) << 5];
+        const uint32_t a3 = myvl[get_bits<2 * BV>(vw1, (2 * mt + 1) * 2 * BV) << 5];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(o[mt][nt], a0, a1, a2, a3, bw[nt][0], bw[nt][1]);
+      }
+    }
+
+    // ---------------- combine the 8 warps of the CTA, write the item's partials
+    __syncthreads();  // every warp is done with the staged codes (comb aliases them)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float l = l_run[nt];
+      l += __shfl_xor_sync(kFull, l, 4);
+      l += __shfl_xor_sync(kFull, l, 8);
+      l += __shfl_xor_sync(kFull, l, 16);
+      const int h = 4 * nt + t;
+      if (g == 0 && h < G) {
+        comb[(warp * G + h) * 130 + 0] = m_run[nt];
+        comb[(warp * G + h) * 130 + 1] = l;
+      }
+      if (h < G) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          comb[(warp * G + h) * 130 + 2 + 16 * g + 2 * mt] = o[mt][nt][0] + o[mt][nt][1];
+          comb[(warp * G + h) * 130 + 2 + 16 * g + 2 * mt + 1] = o[mt][nt][2] + o[mt][nt][3];
+        }
+      }
+    }
+    __syncthreads();
+    for (int e = tid; e < G * 128; e += blockDim.x) {
+      const int h = e / 128, dim = e % 128;
+      float M = -INFINITY;
+      for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, comb[(w * G + h) * 130]);
+      float L = 0.f, A = 0.f;
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float mw = comb[(w * G + h) * 130];
+        const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+        L += f * comb[(w * G + h) * 130 + 1];
+        A += f * comb[(w * G + h) * 130 + 2 + dim];
+      }
+      const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+      float* dst = p.part + (((size_t)b * p.Hq + kvh * G + h) * p.pl.S + sp) * 130;
+      if (dim == 0) {
+        dst[0] = M;
+        dst[1] = L;
+      }
+      dst[2 + dim] = A;
+    }
+    __syncthreads();  // staging and comb are reused by the next item
+  }
+}
+
+// ------------------------------------------------------------------ merge
+// One block (128 threads) per (batch, q head): log-sum-exp combine of the
+// splits in the rotated domain, then out = Πᵀ·acc / L.
+__global__ void decode_merge_kernel(const float* __restrict__ pi, const float* __restrict__ part,
+                                    int S, float* __restrict__ out) {
+  __shared__ float acc[128];
+  __shared__ float red[2];
+  const int bh = blockIdx.x, i = threadIdx.x;
+  const float* P = part + (size_t)bh * S * 130;
+  float M = -INFINITY;
+  for (int s = 0; s < S; ++s) M = fmaxf(M, P[s * 130]);
+  float L = 0.f, A = 0.f;
+  for (int s = 0; s < S; ++s) {
+    const float ms = P[s * 130];
+    const float f = (ms == -INFINITY) ? 0.f : ex2(ms - M);
+    L += f * P[s * 130 + 1];
+    A += f * P[s * 130 + 2 + i];
+  }
+  acc[i] = A;
+  if (i == 0) red[0] = L;
+  __syncthreads();
+  const float invL = 1.f / red[0];
+  float o = 0.f;
+  for (int k = 0; k < 128; ++k) o = fmaf(pi[k * 128 + i], acc[k], o);  // (Πᵀ acc)_i
+  out[(size_t)bh * 128 + i] = o * invL;
+}
+
+template <int BK, int BV, int G>
+static cudaError_t run_split(const DecParams& p, cudaStream_t st) {
+  auto k = decode_split_kernel<BK, BV, G>;
+  static int attr_done = 0;  // the layout never exceeds 112 KB; set once, outside capture
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 112 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_done = 1;
+  }
+  const int items = p.B * p.Hkv * p.pl.S;
+  const int grid = std::max(1, std::min(items, 2 * num_sms()));
+  k<<<grid, 256, p.sm.bytes, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int BK, int BV>
+static cudaError_t run_split_g(const DecParams& p, cudaStream_t st) {
+  switch (p.G) {
+    case 1: return run_split<BK, BV, 1>(p, st);
+    case 2: return run_split<BK, BV, 2>(p, st);
+    case 4: return run_split<BK, BV, 4>(p, st);
+    case 8: return run_split<BK, BV, 8>(p, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int BK>
+static cudaError_t run_split_v(const DecParams& p, int bv, cudaStream_t st) {
+  switch (bv) {
+    case 1: return run_split_g<BK, 1>(p, st);
+    case 2: return run_split_g<BK, 2>(p, st);
+    case 3: return run_split_g<BK, 3>(p, st);
+    case 4: return run_split_g<BK, 4>(p, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+tq_status launch_decode(const DevCtx& kc, const DevCtx& vc, const void* q, int q_dtype,
+                        const tq_codes* K, const tq_codes* V, int B, int Hq, int Hkv, int64_t seq,
+                        int64_t cap, float scale, float* out, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+  if (cap % 16 != 0) return TQ_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  bool same_lut = kc.b_mse == vc.b_mse && kc.alpha == vc.alpha;
+  for (int k = 0; same_lut && k < (1 << kc.b_mse); ++k) same_lut = kc.cen[k] == vc.cen[k];
+  const DecSmem sm = dec_smem(kc.b_mse, vc.b_mse, G, same_lut);
+  const DecPlan pl = make_plan(B, Hq, Hkv, seq, sm.tmax);
+  uint2* frag = static_cast<uint2*>(ws);
+  size_t frag_bytes = (size_t)B * Hkv * 8 * pl.NT * 32 * sizeof(uint2);
+  float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + (frag_bytes + 255) / 256 * 256);
+  const float fold = scale * kLog2e / (kc.sqrt_d * kc.alpha);
+  decode_qprep_kernel<<<B * Hkv, 128, 0, stream>>>(kc, q, q_dtype == TQ_F16, Hq, G, pl.NT, fold, frag);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_cuda_error(e);
+  DecParams p;
+  p.klut = kc.lut;
+  p.vlut = vc.lut;
+  p.v_fold = 1.f / (vc.alpha * vc.sqrt_d);
+  p.kcodes = K->d_codes;
+  p.knorm = K->d_norm;
+  p.vcodes = V->d_codes;
+  p.vnorm = V->d_norm;
+  p.seq = seq;
+  p.cap = cap;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.pl = pl;
+  p.qfrag = frag;
+  p.part = part;
+  p.status = kc.status;
+  p.sm = sm;
+  p.same_lut = same_lut ? 1 : 0;
+  switch (kc.b_mse) {
+    case 1: e = run_split_v<1>(p, vc.b_mse, stream); break;
+    case 2: e = run_split_v<2>(p, vc.b_mse, stream); break;
+    case 3: e = run_split_v<3>(p, vc.b_mse, stream); break;
+    case 4: e = run_split_v<4>(p, vc.b_mse, stream); break;
+    default: return TQ_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return set_cuda_error(e);
+  decode_merge_kernel<<<B * Hq, 128, 0, stream>>>(vc.pi, part, pl.S, out);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? TQ_OK : set_cuda_error(e);
+}
+
+}  // namespace tq

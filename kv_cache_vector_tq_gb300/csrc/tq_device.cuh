@@ -1,0 +1,65 @@
+// Device helpers shared by the libtq kernels.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace tq {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// D += A·B with mma.m16n8k16, fp16 operands, fp32 accumulators.
+// Fragment ownership (lane = 4g + t):
+//   A (16x16, row): a0 = (g, 2t..2t+1), a1 = (g+8, 2t..), a2 = (g, 2t+8..), a3 = (g+8, 2t+8..)
+//   B (16x8, col) : b0 = (k 2t..2t+1, n g), b1 = (k 2t+8..2t+9, n g)
+//   D (16x8)      : d0 = (g, 2t), d1 = (g, 2t+1), d2 = (g+8, 2t), d3 = (g+8, 2t+1)
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// fp16 hi/lo split of two fp32 values: x ≈ hi + lo with |x - hi - lo| <= 2^-22 |x|
+// when hi and lo are normal numbers.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  __half2 h = __floats2half2_rn(x0, x1);
+  __half2 l = __floats2half2_rn(x0 - __low2float(h), x1 - __high2float(h));
+  hi = h2_bits(h);
+  lo = h2_bits(l);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float x0, float x1) {
+  return h2_bits(__floats2half2_rn(x0, x1));
+}
+
+// Extract `bits` bits at bit offset `off` of a little-endian word array (off
+// and bits compile-time after unrolling; codes may straddle two words).
+template <int BITS>
+__device__ __forceinline__ uint32_t get_bits(const uint32_t* w, int off) {
+  const int wi = off >> 5, sh = off & 31;
+  uint32_t v = w[wi] >> sh;
+  if (sh + BITS > 32) v |= w[wi + 1] << (32 - sh);
+  return v & ((1u << BITS) - 1u);
+}
+
+template <int BITS>
+__device__ __forceinline__ void put_bits(uint32_t* w, int off, uint32_t v) {
+  const int wi = off >> 5, sh = off & 31;
+  w[wi] |= v << sh;
+  if (sh + BITS > 32) w[wi + 1] |= v >> (32 - sh);
+}
+
+// Power-of-two scale 2^e such that s·2^e lies in [16, 32) (1 for s == 0).
+__device__ __forceinline__ float pow2_scale_16_32(float s) {
+  if (!(s > 0.f)) return 1.f;
+  int e;
+  frexpf(s, &e);  // s = m·2^e, m in [0.5, 1)
+  return ldexpf(1.f, 5 - e);
+}
+
+}  // namespace tq

@@ -1,0 +1,66 @@
+// Internal declarations shared by the host code and the kernels of libtq.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tq.h"
+
+namespace tq {
+
+// ------------------------------------------------------------------ limits
+constexpr int kMaxD = 3072;
+constexpr int kChunk = 128;       // output coordinates per encoder chunk
+constexpr int kWarpRows = 16;     // rows (vectors) per warp tile of the encoder
+constexpr int kEncWarps = 8;      // warps per encoder CTA
+
+// Device-side view of a context, passed by value to kernels.
+struct DevCtx {
+  int d, b, b_mse, mode, rot;
+  int words_per_vec, qjl_words_per_vec;
+  float sqrt_d;
+  float pi_scale;        // encoder B operand = pi_scale * Π (power of two)
+  float m_scale;         // QJL B operand = m_scale * S·Πᵀ (power of two)
+  float alpha;           // LUT values are fp16(alpha * centroid)
+  float thr[15];         // thresholds, unit-variance units (fp32)
+  float cen[16];         // centroids, unit-variance units (fp32)
+  const uint2* enc_pi;   // encoder B fragments of Π (hi/lo)
+  const uint2* enc_m;    // encoder B fragments of S·Πᵀ (hi/lo), Prod only
+  const float* pi;       // Π, d×d row-major fp32
+  const float* s_mat;    // S, d×d row-major fp32, Prod only
+  const uint32_t* lut;   // pair table: 2^(2 b_mse) fp16x2 entries (alpha-scaled)
+  int* status;           // device status word
+};
+
+struct Ctx {
+  DevCtx dev;
+  tq_codebook cb;
+  double* h_pi = nullptr;   // d×d fp64
+  double* h_s = nullptr;    // d×d fp64 (Prod)
+  void* d_alloc = nullptr;  // single device allocation holding every table
+  size_t d_bytes = 0;
+};
+
+tq_status set_cuda_error(cudaError_t e);
+
+inline int words_per_vector(int d, int bits) {
+  int w = (bits * d + 31) / 32;
+  return (w + 3) / 4 * 4;
+}
+
+// kernel launchers (defined in the .cu files)
+tq_status launch_encode(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
+                        int64_t offset, int64_t group_rows, int64_t group_stride,
+                        cudaStream_t stream);
+tq_status launch_scores(const DevCtx& c, const float* q, int M, const tq_codes* keys, int64_t first,
+                        int64_t N, float* scores, void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t scores_ws_bytes(const DevCtx& c, int M);
+tq_status launch_decode(const DevCtx& kc, const DevCtx& vc, const void* q, int q_dtype,
+                        const tq_codes* K, const tq_codes* V, int B, int Hq, int Hkv, int64_t seq,
+                        int64_t cap, float scale, float* out, void* ws, size_t ws_bytes,
+                        cudaStream_t stream);
+size_t decode_ws_bytes(int d, int B, int Hq, int Hkv, int64_t seq);
+int num_sms();
+
+}  // namespace tq

@@ -1,0 +1,291 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bars (from the benchmark spec of the method's build):
+  * packed indices bit-exact except coordinates within 1e-6 (relative) of a
+    decision threshold; that fraction is reported and must be <= 1e-5;
+  * QJL bits bit-exact except |(S r)_j| <= 1e-6·‖S_j‖·γ, for vectors whose MSE
+    indices match;
+  * norms within 1e-6 relative; scores within 1e-4·‖q‖‖x‖; attention outputs
+    within 2e-3·‖out‖ per head.
+Scores and attention are evaluated by the oracle on the GPU's own codes, so
+encode parity and read-path parity are checked separately.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import kv_cache_vector_tq_gb300 as tq  # noqa: E402
+from kv_cache_vector_tq_gb300 import synth  # noqa: E402
+from oracle import attention as oatt  # noqa: E402
+from oracle import codebook as ocb  # noqa: E402
+from oracle import quantizer as oq  # noqa: E402
+from oracle import rotation as orot  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+BAND_FRAC_MAX = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tq.lib()
+
+
+_cb_cache = {}
+
+
+def oracle_codebook(d, b):
+    if (d, b) not in _cb_cache:
+        _cb_cache[(d, b)] = ocb.build_codebook(d, b)
+    return _cb_cache[(d, b)]
+
+
+def make_pair(seed, d, b, mode=tq.TQ_MSE):
+    """Product context and the oracle's own rotation/QJL matrices for one seed."""
+    G = synth.gaussian_matrix(seed, d)
+    S = synth.qjl_matrix(seed, d) if mode == tq.TQ_PROD else None
+    ctx = tq.Context(d, b, mode, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(G), S)
+    return ctx, orot.haar_rotation(G), S
+
+
+def gpu_encode(ctx, x_np, layout=tq.TQ_LAYOUT_TOKEN, n=None):
+    x = torch.from_numpy(np.ascontiguousarray(x_np)).cuda()
+    cs = tq.CodeSet(ctx, n or x_np.shape[0], layout)
+    tq.tq_encode(ctx, x, cs)
+    torch.cuda.synchronize()
+    assert ctx.poll() == tq.TQ_OK
+    return cs
+
+
+def check_mse_encode(ctx, Pi, X, b, cs=None, first=0):
+    d = X.shape[1]
+    cb = oracle_codebook(d, b)
+    idx_ref, s_ref, v = oq.mse_quantize(X.astype(np.float64), Pi, cb["centroids"], math.sqrt(d))
+    band = oq.near_threshold(v, cb["centroids"])
+    idx = tq.tq_unpack_indices(cs, first, X.shape[0]).astype(np.int64)
+    mism = (idx != idx_ref) & ~band
+    assert not mism.any(), f"{mism.sum()} index mismatches outside the band, rows {np.nonzero(mism.any(1))[0][:10]}"
+    frac = band.mean()
+    assert frac <= BAND_FRAC_MAX or band.sum() <= 2, f"near-threshold fraction {frac}"
+    norm = cs.norm[first:first + X.shape[0]].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(norm, s_ref, rtol=1e-6, atol=0)
+    return idx_ref, band, frac
+
+
+# ------------------------------------------------------------------ encode
+@pytest.mark.parametrize("b", [1, 2, 3, 4])
+def test_encode_mse_fp32_config1(b):
+    """TurboQuant_MSE, d=128, N=4096 fp32 N(0,1) keys with channels 0-3 x20
+    (the first workload; b=3 is its own bit width, the others widen it)."""
+    ctx, Pi, _ = make_pair(0, 128, b)
+    X = synth.gaussian_rows(0, 4096, 128, outlier_cols=4, outlier_scale=20.0)
+    cs = gpu_encode(ctx, X)
+    idx_ref, band, frac = check_mse_encode(ctx, Pi, X, b, cs)
+    # raw words equal the canonical packing wherever no coordinate is in the band
+    words = cs.codes.view(torch.int32).cpu().numpy().view(np.uint32).reshape(4096, -1)
+    ok = ~band.any(axis=1)
+    np.testing.assert_array_equal(words[ok], oq.pack_codes(idx_ref[ok], b))
+
+
+@pytest.mark.parametrize("d", [32, 64, 96])
+@pytest.mark.parametrize("b", [1, 3, 4])
+def test_encode_small_dims(d, b):
+    ctx, Pi, _ = make_pair(3, d, b)
+    X = synth.gaussian_rows(3, 333, d, outlier_cols=2, outlier_scale=5.0)
+    cs = gpu_encode(ctx, X)
+    idx_ref, band, _ = check_mse_encode(ctx, Pi, X, b, cs)
+    words = cs.codes.view(torch.int32).cpu().numpy().view(np.uint32).reshape(333, -1)
+    ok = ~band.any(axis=1)
+    np.testing.assert_array_equal(words[ok], oq.pack_codes(idx_ref[ok], b))
+
+
+@pytest.mark.parametrize("N", [1, 31, 33, 129, 1000])
+def test_encode_ragged_and_zero_rows(N):
+    ctx, Pi, _ = make_pair(5, 128, 3)
+    X = synth.gaussian_rows(5, N, 128)
+    X[N // 2] = 0.0  # zero vector: s = 0, all codes 0
+    cs = gpu_encode(ctx, X)
+    check_mse_encode(ctx, Pi, X, 3, cs)
+    idx = tq.tq_unpack_indices(cs, N // 2, 1)
+    assert not idx.any() and cs.norm[N // 2].item() == 0.0
+
+
+@pytest.mark.parametrize("b", [2, 3, 4])
+def test_encode_fp16_kv_token_and_pair_layouts(b):
+    """fp16 K/V with 4 outlier channels x10 (the KV workloads), both layouts."""
+    ctx, Pi, _ = make_pair(0, 128, b)
+    K, V = synth.kv_layer(0, 0, 1, 2, 1000, 128)
+    for arr, layout in ((K, tq.TQ_LAYOUT_TOKEN), (V, tq.TQ_LAYOUT_PAIR)):
+        X = arr.reshape(-1, 128)
+        cs = gpu_encode(ctx, X, layout)
+        idx_ref, band, _ = check_mse_encode(ctx, Pi, X.astype(np.float32), b, cs)
+        if layout == tq.TQ_LAYOUT_PAIR:
+            # pair block i: coordinate j of vector 2i+q at bits (2j+q)·b of the block
+            words = cs.codes.view(torch.int32).cpu().numpy().view(np.uint32).reshape(-1, 2 * cs.words_per_vec)
+            inter = np.zeros((idx_ref.shape[0] // 2, 2 * 128), dtype=np.int64)
+            inter[:, 0::2] = idx_ref[0::2]
+            inter[:, 1::2] = idx_ref[1::2]
+            ok = ~(band[0::2].any(1) | band[1::2].any(1))
+            np.testing.assert_array_equal(words[ok], oq.pack_codes(inter[ok], b))
+
+
+def test_encode_append_mapping_pair_layout():
+    """Cache append: one token per (batch, head) block at position t (odd and
+    even), written next to tokens encoded earlier into the same pair blocks."""
+    b, cap, blocks = 3, 64, 6
+    ctx, Pi, _ = make_pair(2, 128, b)
+    X = synth.gaussian_rows(2, blocks * 40, 128).reshape(blocks, 40, 128)
+    cs = tq.CodeSet(ctx, blocks * cap, tq.TQ_LAYOUT_PAIR)
+    # prefill 37 tokens per block (odd count: the last pair is half written)
+    pre = torch.from_numpy(np.ascontiguousarray(X[:, :37].reshape(-1, 128))).cuda()
+    tq.tq_encode(ctx, pre, cs, offset=0, group_rows=37, group_stride=cap)
+    for t in (37, 38, 39):
+        new = torch.from_numpy(np.ascontiguousarray(X[:, t])).cuda()
+        tq.tq_encode(ctx, new, cs, offset=t, group_rows=1, group_stride=cap)
+    torch.cuda.synchronize()
+    cb = oracle_codebook(128, b)
+    idx_ref, s_ref, v = oq.mse_quantize(X.reshape(-1, 128).astype(np.float64), Pi, cb["centroids"], math.sqrt(128))
+    band = oq.near_threshold(v, cb["centroids"])
+    for blk in range(blocks):
+        got = tq.tq_unpack_indices(cs, blk * cap, 40).astype(np.int64)
+        ref = idx_ref[blk * 40:(blk + 1) * 40]
+        bb = band[blk * 40:(blk + 1) * 40]
+        assert not ((got != ref) & ~bb).any()
+        np.testing.assert_allclose(cs.norm[blk * cap: blk * cap + 40].cpu().numpy(), s_ref[blk * 40:(blk + 1) * 40], rtol=1e-6)
+
+
+def test_encode_prod_config3_sample():
+    """TurboQuant_Prod b=3 (2-bit MSE + 1-bit QJL), unit-norm Gaussian keys."""
+    d, b, N = 128, 3, 20000
+    ctx, Pi, S = make_pair(0, d, b, tq.TQ_PROD)
+    X = synth.unit_rows(0, N, d)
+    cs = gpu_encode(ctx, X)
+    cb = oracle_codebook(d, b - 1)
+    e = oq.prod_quantize(X.astype(np.float64), Pi, S, cb["centroids"], math.sqrt(d))
+    band = oq.near_threshold(e["v"], cb["centroids"])
+    idx, bits = tq.tq_unpack_indices(cs, 0, N, with_bits=True)
+    mism = (idx.astype(np.int64) != e["idx"]) & ~band
+    assert not mism.any()
+    assert band.mean() <= BAND_FRAC_MAX
+    rows_ok = (idx.astype(np.int64) == e["idx"]).all(axis=1)
+    qband = oq.qjl_near_zero(e["p"], e["gamma"], S)
+    bmism = (bits.astype(np.int64) != e["bits"]) & ~qband & rows_ok[:, None]
+    assert not bmism.any(), f"{bmism.sum()} QJL bit mismatches"
+    assert qband.mean() <= BAND_FRAC_MAX
+    g = cs.rnorm[:N].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(g[rows_ok], e["gamma"][rows_ok], rtol=1e-5, atol=1e-7)
+
+
+# ------------------------------------------------------------------ scores
+def _scores_check(ctx, Pi, S, X, Q, b_mse, prod):
+    d = X.shape[1]
+    N, M = X.shape[0], Q.shape[0]
+    cs = gpu_encode(ctx, X)
+    q = torch.from_numpy(np.ascontiguousarray(Q)).cuda()
+    out = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(tq.tq_scores_workspace_size(ctx, M) // 4 + 4, dtype=torch.float32, device="cuda")
+    tq.tq_scores(ctx, q, cs, out, ws)
+    torch.cuda.synchronize()
+    cb = oracle_codebook(d, b_mse)
+    s = cs.norm[:N].cpu().numpy().astype(np.float64)
+    if prod:
+        idx, bits = tq.tq_unpack_indices(cs, 0, N, with_bits=True)
+        gam = cs.rnorm[:N].cpu().numpy().astype(np.float64)
+        ref = oatt.prod_scores(Q.astype(np.float64), idx, s, bits, gam, Pi, S, cb["centroids"], math.sqrt(d))
+    else:
+        idx = tq.tq_unpack_indices(cs, 0, N)
+        ref = oatt.mse_scores(Q.astype(np.float64), idx, s, Pi, cb["centroids"], math.sqrt(d))
+    got = out.cpu().numpy().astype(np.float64)
+    bound = 1e-4 * np.linalg.norm(Q, axis=1)[:, None] * np.linalg.norm(X.astype(np.float64), axis=1)[None, :]
+    err = np.abs(got - ref)
+    assert (err <= bound).all(), f"max err/bound {np.max(err / np.maximum(bound, 1e-30))}"
+    return np.max(err / np.maximum(bound, 1e-30))
+
+
+def test_scores_mse_config1():
+    ctx, Pi, _ = make_pair(0, 128, 3)
+    X = synth.gaussian_rows(0, 4096, 128, outlier_cols=4, outlier_scale=20.0)
+    Q = synth.queries(0, 1, 128)
+    _scores_check(ctx, Pi, None, X, Q, 3, False)
+
+
+@pytest.mark.parametrize("b", [1, 2, 4])
+def test_scores_mse_bits_and_ragged(b):
+    ctx, Pi, _ = make_pair(7, 128, b)
+    X = synth.gaussian_rows(7, 1237, 128, outlier_cols=4, outlier_scale=20.0)
+    Q = synth.queries(7, 70, 128)  # more than one 64-query launch, ragged
+    _scores_check(ctx, Pi, None, X, Q, b, False)
+
+
+def test_scores_prod_config3_sample():
+    ctx, Pi, S = make_pair(0, 128, 3, tq.TQ_PROD)
+    X = synth.unit_rows(0, 8192, 128)
+    Q = synth.queries(0, 64, 128)
+    _scores_check(ctx, Pi, S, X, Q, 2, True)
+
+
+# ------------------------------------------------------------------ decode
+def run_decode(b_k, b_v, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float16):
+    d = 128
+    cap = cap or (seq + 15) // 16 * 16
+    kctx, Pi_k, _ = make_pair(seed, d, b_k)
+    if b_v == b_k:
+        vctx, Pi_v = kctx, Pi_k
+    else:
+        vctx, Pi_v, _ = make_pair(seed, d, b_v)
+    Kh, Vh = synth.kv_layer(seed, 0, B, Hkv, seq, d)
+    Kc = tq.CodeSet(kctx, B * Hkv * cap, tq.TQ_LAYOUT_TOKEN)
+    Vc = tq.CodeSet(vctx, B * Hkv * cap, tq.TQ_LAYOUT_PAIR)
+    kx = torch.from_numpy(np.ascontiguousarray(Kh.reshape(-1, d))).cuda()
+    vx = torch.from_numpy(np.ascontiguousarray(Vh.reshape(-1, d))).cuda()
+    tq.tq_encode(kctx, kx, Kc, offset=0, group_rows=seq, group_stride=cap)
+    tq.tq_encode(vctx, vx, Vc, offset=0, group_rows=seq, group_stride=cap)
+    q_np = synth.queries(seed, B * Hq, d).reshape(B, Hq, d)
+    q = torch.from_numpy(q_np).cuda().to(q_dtype)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(tq.tq_decode_workspace_size(kctx, B, Hq, Hkv, seq) // 4 + 4, dtype=torch.float32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    tq.tq_decode_attention(kctx, vctx, q, Kc, Vc, B, Hq, Hkv, seq, cap, scale, out, ws)
+    torch.cuda.synchronize()
+    assert kctx.poll() == tq.TQ_OK
+    # oracle on the GPU's own codes
+    kidx = np.concatenate([tq.tq_unpack_indices(Kc, blk * cap, seq) for blk in range(B * Hkv)])
+    vidx = np.concatenate([tq.tq_unpack_indices(Vc, blk * cap, seq) for blk in range(B * Hkv)])
+    kn = Kc.norm.cpu().numpy().reshape(B * Hkv, cap)[:, :seq].reshape(-1).astype(np.float64)
+    vn = Vc.norm.cpu().numpy().reshape(B * Hkv, cap)[:, :seq].reshape(-1).astype(np.float64)
+    cbk, cbv = oracle_codebook(d, b_k), oracle_codebook(d, b_v)
+    Khat = oatt.dequantize_cache(kidx, kn, Pi_k, cbk["centroids"], math.sqrt(d), B, Hkv, seq)
+    Vhat = oatt.dequantize_cache(vidx, vn, Pi_v, cbv["centroids"], math.sqrt(d), B, Hkv, seq)
+    qref = q.float().cpu().numpy().astype(np.float64)
+    ref = oatt.decode_attention(qref, Khat, Vhat, scale)
+    got = out.cpu().numpy().astype(np.float64)
+    rel = np.linalg.norm(got - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
+    assert rel.max() <= 2e-3, f"max per-head relative error {rel.max()}"
+    return rel.max()
+
+
+@pytest.mark.parametrize("b", [2, 4])
+def test_decode_config2(b):
+    """One layer, B=1, 32 query / 8 KV heads, d=128, seq 16384, fp16 K/V with
+    4 outlier channels x10, K and V TurboQuant_MSE at b."""
+    run_decode(b, b, 1, 32, 8, 16384)
+
+
+@pytest.mark.parametrize("seq", [1, 15, 17, 33, 1000])
+def test_decode_ragged_seq(seq):
+    run_decode(3, 3, 2, 8, 2, seq, cap=((seq + 15) // 16 + 1) * 16)
+
+
+@pytest.mark.parametrize("gqa", [1, 2, 8])
+def test_decode_gqa_variants(gqa):
+    run_decode(3, 3, 1, 4 * gqa, 4, 777, q_dtype=torch.float32)
+
+
+def test_decode_asymmetric_bits():
+    run_decode(4, 2, 1, 16, 4, 2048)
