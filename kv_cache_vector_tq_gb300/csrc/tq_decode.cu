@@ -19,6 +19,7 @@
 // merge kernel applies Πᵀ once per head after combining the splits with the
 // usual log-sum-exp rule.
 #include <algorithm>
+#include <utility>
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
@@ -28,6 +29,7 @@ namespace tq {
 constexpr int kTileTok = 16;
 constexpr int kMaxTilesPerItem = 32;
 constexpr int kDecWarps = 8;
+constexpr int kMaxRounds = kMaxTilesPerItem / kDecWarps;  // tile rounds staged per item
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.f;          // rescale only when the max grows by > 2^8
 constexpr uint32_t kSpinLimit = 1u << 22;  // bounded mbarrier wait (~0.1-1 s)
@@ -96,6 +98,11 @@ __device__ __forceinline__ void fence_proxy_async() {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
+// programmatic dependent launch: wait for the preceding grid / let the next one start
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
@@ -103,38 +110,57 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // ------------------------------------------------------------------ query prep
-// One block per (batch, kv head): q̂_h = Π·q_h for the G query heads of the
-// group, folded with scale·log2(e)/(√d·α_K), split into fp16 hi (column 2h) and
-// lo (column 2h+1) B fragments:  b0 = (K index 16s+2t.., col g),
+// One block (8 warps) per (batch, kv head): q̂_h = Π·q_h for the G query heads
+// of the group, folded with scale·log2(e)/(√d·α_K) and split into fp16 hi
+// (column 2h) and lo (column 2h+1) B fragments: b0 = (K index 16s+2t.., col g),
 // b1 = (16s+8+2t.., col g), K index 16s+8h+2t+e <-> coordinate 32t+4s+2h+e.
-__global__ void decode_qprep_kernel(const DevCtx kc, const void* __restrict__ q, int q_f16, int Hq,
-                                    int G, int NT, float fold, uint2* __restrict__ frag) {
+// Warp w computes rows 16w..16w+15 of Π·q with coalesced float4 loads of Π.
+__global__ void __launch_bounds__(256) decode_qprep_kernel(const float* __restrict__ pi,
+                                                           const void* __restrict__ q, int q_f16,
+                                                           int Hq, int G, int NT, float fold,
+                                                           uint2* __restrict__ frag) {
   __shared__ float qs[8][128];
   __shared__ float qr[8][128];
   const int bk = blockIdx.x;  // b * Hkv + kvh
-  const int i = threadIdx.x;  // 128 threads
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hkv = Hq / G;
   const int b = bk / Hkv, kvh = bk % Hkv;
-  for (int h = 0; h < G; ++h) {
+  float4 pv[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r)
+    pv[r] = __ldg(reinterpret_cast<const float4*>(pi + (size_t)(16 * warp + r) * 128) + lane);
+  griddep_wait();  // q and the workspace may be produced / still read by earlier grids
+  for (int e = tid; e < G * 128; e += blockDim.x) {
+    const int h = e >> 7, i = e & 127;
     const int64_t off = ((int64_t)b * Hq + kvh * G + h) * 128 + i;
     qs[h][i] = q_f16 ? __half2float(static_cast<const __half*>(q)[off]) : static_cast<const float*>(q)[off];
   }
   __syncthreads();
   for (int h = 0; h < G; ++h) {
-    float a = 0.f;
-    for (int k = 0; k < 128; ++k) a = fmaf(kc.pi[i * 128 + k], qs[h][k], a);
-    qr[h][i] = a * fold;
+    const float4 qq = *reinterpret_cast<const float4*>(&qs[h][4 * lane]);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float x = pv[r].x * qq.x + pv[r].y * qq.y + pv[r].z * qq.z + pv[r].w * qq.w;
+      x += __shfl_xor_sync(kFull, x, 16);
+      x += __shfl_xor_sync(kFull, x, 8);
+      x += __shfl_xor_sync(kFull, x, 4);
+      x += __shfl_xor_sync(kFull, x, 2);
+      x += __shfl_xor_sync(kFull, x, 1);
+      if (lane == 0) qr[h][16 * warp + r] = x * fold;
+    }
   }
   __syncthreads();
+  griddep_launch();
   // entries: s (8) x nt (NT) x lane (32)
-  for (int e = i; e < 8 * NT * 32; e += blockDim.x) {
-    const int lane = e & 31, nt = (e >> 5) % NT, s = e / (32 * NT);
-    const int g = lane >> 2, t = lane & 3;
+  for (int e = tid; e < 8 * NT * 32; e += blockDim.x) {
+    const int ln = e & 31, nt = (e >> 5) % NT, s = e / (32 * NT);
+    const int g = ln >> 2, t = ln & 3;
     const int n = nt * 8 + g, h = n >> 1, lo = n & 1;
     uint2 f = make_uint2(0u, 0u);
     if (h < G) {
       const int c0 = 32 * t + 4 * s;
       float v[4];
+#pragma unroll
       for (int u = 0; u < 4; ++u) {
         const float x = qr[h][c0 + u];
         const float hi = __half2float(__float2half_rn(x));
@@ -143,7 +169,7 @@ __global__ void decode_qprep_kernel(const DevCtx kc, const void* __restrict__ q,
       f.x = pack_f16x2(v[0], v[1]);
       f.y = pack_f16x2(v[2], v[3]);
     }
-    frag[((size_t)bk * 8 + s) * NT * 32 + nt * 32 + lane] = f;
+    frag[((size_t)bk * 8 + s) * NT * 32 + nt * 32 + ln] = f;
   }
 }
 
@@ -207,7 +233,7 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
   float* svn = reinterpret_cast<float*>(smem + p.sm.off_vn);
   float* comb = reinterpret_cast<float*>(smem + p.sm.off_kc);  // reused after the tile loop
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + p.sm.off_bar);
-  volatile int& s_abort = *reinterpret_cast<int*>(smem + p.sm.off_bar + 16);
+  volatile int& s_abort = *reinterpret_cast<int*>(smem + p.sm.off_bar + 8 * kMaxRounds);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -215,15 +241,17 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
   if (!p.same_lut)
     for (int i = tid; i < EV * 32; i += blockDim.x) vlut[i] = p.vlut[i >> 5];
   if (tid == 0) {
-    mbar_init(bar, 1);
+    for (int r = 0; r < kMaxRounds; ++r) mbar_init(bar + r, 1);
     fence_mbar_init();
     s_abort = 0;
   }
   __syncthreads();
+  griddep_wait();    // codes (appends), query fragments and partials of earlier grids
+  griddep_launch();  // the merge grid may start staging its tables
 
   const int groups = p.B * p.Hkv;
   const int n_items = groups * p.pl.S;
-  uint32_t phase = 0;
+  uint32_t phases = 0;  // parity bit per round barrier (flipped only when the round was armed)
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int bk = item / p.pl.S, sp = item % p.pl.S;
     const int tile0 = sp * p.pl.per_item;
@@ -231,36 +259,20 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
     const int64_t tok0 = (int64_t)tile0 * kTileTok;
     const int ntok = ntl * kTileTok;  // staged tokens (whole tiles, inside cap)
     const int64_t vbase = (int64_t)bk * p.cap + tok0;  // vector index of the first token
+    const int nrounds = (ntl + kDecWarps - 1) / kDecWarps;
     if (tid == 0) {
-      const uint32_t kb = (uint32_t)ntok * WK * 4, vb = (uint32_t)ntok * WV * 4,
-                     nb = (uint32_t)ntok * 4;
       fence_proxy_async();
-      mbar_arrive_expect_tx(bar, kb + vb + 2 * nb);
-      bulk_g2s(skc, p.kcodes + vbase * WK, kb, bar);
-      bulk_g2s(svc, p.vcodes + vbase * WV, vb, bar);  // vbase even: pair blocks align
-      bulk_g2s(skn, p.knorm + vbase, nb, bar);
-      bulk_g2s(svn, p.vnorm + vbase, nb, bar);
-    }
-    // ---- bounded wait for the item's bytes
-    {
-      uint32_t spins = 0;
-      bool ok = false;
-      while (!(ok = mbar_try_wait(bar, phase)) && ++spins < kSpinLimit) {
+      for (int r = 0; r < nrounds; ++r) {
+        const int rt0 = r * kDecWarps * kTileTok;  // first local token of the round
+        const int rtok = min(kDecWarps, ntl - r * kDecWarps) * kTileTok;
+        const uint32_t kb = (uint32_t)rtok * WK * 4, vb = (uint32_t)rtok * WV * 4,
+                       nb = (uint32_t)rtok * 4;
+        mbar_arrive_expect_tx(bar + r, kb + vb + 2 * nb);
+        bulk_g2s(skc + rt0 * WK, p.kcodes + (vbase + rt0) * WK, kb, bar + r);
+        bulk_g2s(svc + rt0 * WV, p.vcodes + (vbase + rt0) * WV, vb, bar + r);  // even: pairs align
+        bulk_g2s(skn + rt0, p.knorm + vbase + rt0, nb, bar + r);
+        bulk_g2s(svn + rt0, p.vnorm + vbase + rt0, nb, bar + r);
       }
-      if (!ok) {
-        atomicExch(p.status, 1);
-        s_abort = 1;
-      }
-    }
-    phase ^= 1u;
-    __syncthreads();
-    if (s_abort) {
-      if (tid == 0) {  // let the copies in flight land before leaving (bounded)
-        uint32_t spins = 0;
-        while (!mbar_try_wait(bar, phase ^ 1u) && ++spins < kSpinLimit) {
-        }
-      }
-      return;
     }
 
     // ---- per-warp state
@@ -282,6 +294,18 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
     const uint32_t* myvl = vlut + lane;
 
     for (int tl = warp; tl < ntl; tl += kDecWarps) {
+      {  // bounded wait for this round's bytes
+        uint32_t spins = 0;
+        bool ok = false;
+        while (!(ok = mbar_try_wait(bar + tl / kDecWarps, (phases >> (tl / kDecWarps)) & 1u)) &&
+               ++spins < kSpinLimit) {
+        }
+        if (!ok) {
+          atomicExch(p.status, 1);
+          s_abort = 1;
+          break;
+        }
+      }
       const int lt0 = tl * kTileTok;  // local token index of the tile
       // ---------------- K side
       uint32_t kw0[BK], kw1[BK];
@@ -290,9 +314,11 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
         kw0[w] = skc[(lt0 + g) * WK + t * BK + w];
         kw1[w] = skc[(lt0 + g + 8) * WK + t * BK + w];
       }
-      float sa[NT][4];
+      float sa[NT][4], sb[NT][4];  // even / odd k-steps: two independent MMA chains
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) sa[nt][0] = sa[nt][1] = sa[nt][2] = sa[nt][3] = 0.f;
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const uint32_t a0 = mykl[get_bits<2 * BK>(kw0, 4 * s * BK) << 5];
@@ -300,8 +326,17 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
         const uint32_t a2 = mykl[get_bits<2 * BK>(kw0, (4 * s + 2) * BK) << 5];
         const uint32_t a3 = mykl[get_bits<2 * BK>(kw1, (4 * s + 2) * BK) << 5];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(sa[nt], a0, a1, a2, a3, qf[s][nt].x, qf[s][nt].y);
+        for (int nt = 0; nt < NT; ++nt) {
+          if (s & 1)
+            mma16816(sb[nt], a0, a1, a2, a3, qf[s][nt].x, qf[s][nt].y);
+          else
+            mma16816(sa[nt], a0, a1, a2, a3, qf[s][nt].x, qf[s][nt].y);
+        }
       }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sa[nt][e] += sb[nt][e];
       const float sk0 = skn[lt0 + g], sk1 = skn[lt0 + g + 8];
       const bool v0 = tok0 + lt0 + g < p.seq, v1 = tok0 + lt0 + g + 8 < p.seq;
       const float sv0 = svn[lt0 + g], sv1 = svn[lt0 + g + 8];
@@ -385,6 +420,16 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
 
     // ---------------- combine the 8 warps of the CTA, write the item's partials
     __syncthreads();  // every warp is done with the staged codes (comb aliases them)
+    if (s_abort) {
+      if (tid == 0) {  // let the copies in flight land before leaving (bounded waits)
+        for (int r = 0; r < nrounds; ++r) {
+          uint32_t spins = 0;
+          while (!mbar_try_wait(bar + r, (phases >> r) & 1u) && ++spins < kSpinLimit) {
+          }
+        }
+      }
+      return;
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float l = l_run[nt];
@@ -425,34 +470,102 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
       dst[2 + dim] = A;
     }
     __syncthreads();  // staging and comb are reused by the next item
+    phases ^= (1u << nrounds) - 1u;
   }
 }
 
 // ------------------------------------------------------------------ merge
-// One block (128 threads) per (batch, q head): log-sum-exp combine of the
-// splits in the rotated domain, then out = Πᵀ·acc / L.
-__global__ void decode_merge_kernel(const float* __restrict__ pi, const float* __restrict__ part,
-                                    int S, float* __restrict__ out) {
-  __shared__ float acc[128];
-  __shared__ float red[2];
-  const int bh = blockIdx.x, i = threadIdx.x;
-  const float* P = part + (size_t)bh * S * 130;
-  float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, P[s * 130]);
-  float L = 0.f, A = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float ms = P[s * 130];
-    const float f = (ms == -INFINITY) ? 0.f : ex2(ms - M);
-    L += f * P[s * 130 + 1];
-    A += f * P[s * 130 + 2 + i];
+// One block (256 threads) per (batch, q head): log-sum-exp combine of the
+// splits in the rotated domain, then out = Πᵀ·acc / L.  Π is staged in shared
+// memory before the block waits for the split grid (programmatic launch), and
+// the split loads are spread over the threads so they are in flight together.
+__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float u = __shfl_xor_sync(kFull, v, o);
+    v = is_max ? fmaxf(v, u) : v + u;
   }
-  acc[i] = A;
-  if (i == 0) red[0] = L;
+  if (lane == 0) red[warp] = v;
   __syncthreads();
-  const float invL = 1.f / red[0];
+  float r = red[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(256) decode_merge_kernel(const float* __restrict__ pi,
+                                                           const float* __restrict__ part, int S,
+                                                           float* __restrict__ out) {
+  extern __shared__ __align__(16) float msm[];
+  float* spi = msm;               // Π, 128 x 128
+  float* acc = spi + 128 * 128;   // [2][128]
+  float* red = acc + 256;         // [8]
+  float* w = red + 8;             // [S]
+  const int tid = threadIdx.x, bh = blockIdx.x;
+  {
+    const float4* src = reinterpret_cast<const float4*>(pi);
+    float4* dst = reinterpret_cast<float4*>(spi);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) dst[tid + 256 * k] = __ldg(src + tid + 256 * k);
+  }
+  griddep_wait();  // partials of the split grid
+  const float* P = part + (size_t)bh * S * 130;
+  float mloc = -INFINITY;
+  for (int s = tid; s < S; s += blockDim.x) {
+    const float m = P[(size_t)s * 130];
+    w[s] = m;
+    mloc = fmaxf(mloc, m);
+  }
+  const float M = block_reduce(mloc, red, true);
+  float lloc = 0.f;
+  for (int s = tid; s < S; s += blockDim.x) {
+    const float f = (w[s] == -INFINITY) ? 0.f : ex2(w[s] - M);
+    lloc += f * P[(size_t)s * 130 + 1];
+    w[s] = f;
+  }
+  const float L = block_reduce(lloc, red, false);  // its barriers also publish w[]
+  const int i = tid & 127, hf = tid >> 7;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int s = hf;
+  for (; s + 6 < S; s += 8) {
+    a0 += w[s] * P[(size_t)s * 130 + 2 + i];
+    a1 += w[s + 2] * P[(size_t)(s + 2) * 130 + 2 + i];
+    a2 += w[s + 4] * P[(size_t)(s + 4) * 130 + 2 + i];
+    a3 += w[s + 6] * P[(size_t)(s + 6) * 130 + 2 + i];
+  }
+  for (; s < S; s += 2) a0 += w[s] * P[(size_t)s * 130 + 2 + i];
+  acc[hf * 128 + i] = (a0 + a1) + (a2 + a3);
+  __syncthreads();
+  if (tid < 128) acc[i] += acc[128 + i];
+  __syncthreads();
+  // out_i = Σ_k Π[k][i] acc[k]: two halves of k, combined through shared memory
   float o = 0.f;
-  for (int k = 0; k < 128; ++k) o = fmaf(pi[k * 128 + i], acc[k], o);  // (Πᵀ acc)_i
-  out[(size_t)bh * 128 + i] = o * invL;
+  const int k0 = hf * 64;
+#pragma unroll 8
+  for (int k = k0; k < k0 + 64; ++k) o = fmaf(spi[k * 128 + i], acc[k], o);
+  if (hf == 1) acc[128 + i] = o;  // the loop above reads acc[0..127] only
+  __syncthreads();
+  if (hf == 0) out[(size_t)bh * 128 + i] = (o + acc[128 + i]) / L;
+}
+
+// cudaLaunchKernelEx with programmatic stream serialization: the grid may start
+// while the previous grid in the stream finishes; it calls griddepcontrol.wait
+// before touching anything that grid produces.
+template <typename... Exp, typename... Act>
+static cudaError_t launch_pdl(void (*kern)(Exp...), int grid, int block, size_t smem, cudaStream_t st,
+                              Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Act>(args)...);
 }
 
 template <int BK, int BV, int G>
@@ -466,8 +579,7 @@ static cudaError_t run_split(const DecParams& p, cudaStream_t st) {
   }
   const int items = p.B * p.Hkv * p.pl.S;
   const int grid = std::max(1, std::min(items, 2 * num_sms()));
-  k<<<grid, 256, p.sm.bytes, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k, grid, 256, (size_t)p.sm.bytes, st, p);
 }
 
 template <int BK, int BV>
@@ -506,8 +618,8 @@ tq_status launch_decode(const DevCtx& kc, const DevCtx& vc, const void* q, int q
   size_t frag_bytes = (size_t)B * Hkv * 8 * pl.NT * 32 * sizeof(uint2);
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + (frag_bytes + 255) / 256 * 256);
   const float fold = scale * kLog2e / (kc.sqrt_d * kc.alpha);
-  decode_qprep_kernel<<<B * Hkv, 128, 0, stream>>>(kc, q, q_dtype == TQ_F16, Hq, G, pl.NT, fold, frag);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(decode_qprep_kernel, B * Hkv, 256, 0, stream, (const float*)kc.pi, q,
+                             (int)(q_dtype == TQ_F16), Hq, G, pl.NT, fold, frag);
   if (e != cudaSuccess) return set_cuda_error(e);
   DecParams p;
   p.klut = kc.lut;
@@ -537,8 +649,15 @@ tq_status launch_decode(const DevCtx& kc, const DevCtx& vc, const void* q, int q
     default: return TQ_ERR_UNSUPPORTED;
   }
   if (e != cudaSuccess) return set_cuda_error(e);
-  decode_merge_kernel<<<B * Hq, 128, 0, stream>>>(vc.pi, part, pl.S, out);
-  e = cudaGetLastError();
+  const size_t msmem = (size_t)(128 * 128 + 256 + 8 + pl.S) * sizeof(float);
+  static size_t merge_attr = 0;  // raised only when a larger split count needs it
+  if (msmem > merge_attr) {
+    e = cudaFuncSetAttribute(decode_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)std::max<size_t>(msmem, 80 * 1024));
+    if (e != cudaSuccess) return set_cuda_error(e);
+    merge_attr = std::max<size_t>(msmem, 80 * 1024);
+  }
+  e = launch_pdl(decode_merge_kernel, B * Hq, 256, msmem, stream, (const float*)vc.pi, (const float*)part,
+                 pl.S, out);
   return e == cudaSuccess ? TQ_OK : set_cuda_error(e);
 }
 

@@ -23,43 +23,62 @@ namespace tq {
 
 constexpr int kQTile = 64;  // queries per launch of the scan kernel
 
-// B fragments of one query tile (8 queries) for one kstep: uint2 per lane.
-// ws layout: [mse | qjl] x [qtile][kstep][lane] uint2
-__global__ void scores_qprep_kernel(const DevCtx c, const float* __restrict__ q, int M,
-                                    uint2* __restrict__ frag_mse, uint2* __restrict__ frag_qjl) {
-  const int m = blockIdx.x;  // one query per block, 128 threads = one coordinate each
-  const int d = c.d;
-  __shared__ float qs[kMaxD > 128 ? 128 : 128];
-  __shared__ float qr[128], sq[128];
-  const int i = threadIdx.x;
-  qs[i] = (m < M && i < d) ? q[(int64_t)m * d + i] : 0.f;
+// Query preparation, one block (8 warps) per query: q̂ = Π·q / α and, for
+// Prod, S·q, computed with coalesced float4 row loads (warp w: rows
+// 16w..16w+15), then written as B fragments (uint2 per lane):
+//   b0 = (K index 16s+2t.., col g), b1 = (16s+8+2t.., col g),
+//   K index 16s+8h+2t+e <-> coordinate 32t+4s+2h+e, query = 8·tile + g.
+// ws layout: [mse | qjl] x [qtile][kstep][lane] uint2.
+__device__ __forceinline__ float warp_dot4(float4 a, float4 b) {
+  float x = a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+  return x;
+}
+
+__global__ void __launch_bounds__(256) scores_qprep_kernel(const DevCtx c, const float* __restrict__ q, int M,
+                                                           uint2* __restrict__ frag_mse,
+                                                           uint2* __restrict__ frag_qjl) {
+  const int m = blockIdx.x;
+  __shared__ float qs[128], qr[128], sq[128];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < 128) qs[tid] = (m < M) ? q[(int64_t)m * 128 + tid] : 0.f;
   __syncthreads();
-  float acc = 0.f, acc2 = 0.f;
-  for (int k = 0; k < d; ++k) acc = fmaf(c.pi[i * d + k], qs[k], acc);
-  qr[i] = acc / c.alpha;
-  if (c.mode == TQ_PROD) {
-    for (int k = 0; k < d; ++k) acc2 = fmaf(c.s_mat[i * d + k], qs[k], acc2);
-    sq[i] = acc2;
+  const float4 qq = *reinterpret_cast<const float4*>(&qs[4 * lane]);
+  const bool prod = c.mode == TQ_PROD;
+  float4 pv[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r)
+    pv[r] = __ldg(reinterpret_cast<const float4*>(c.pi + (size_t)(16 * warp + r) * 128) + lane);
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const float x = warp_dot4(pv[r], qq);
+    if (lane == 0) qr[16 * warp + r] = x / c.alpha;
+  }
+  if (prod) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      pv[r] = __ldg(reinterpret_cast<const float4*>(c.s_mat + (size_t)(16 * warp + r) * 128) + lane);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const float x = warp_dot4(pv[r], qq);
+      if (lane == 0) sq[16 * warp + r] = x;
+    }
   }
   __syncthreads();
-  // write the fragments of query m: lane (g = m % 8, t), kstep s
-  if (i < 32) {
-    const int g = m & 7, nt = m >> 3;
-    for (int s = 0; s < 8; ++s)
-      for (int t = 0; t < 4; ++t) {
-        if (i != s * 4 + t) continue;
-        const int lane = 4 * g + t;
-        const int c0 = 32 * t + 4 * s, c1 = c0 + 2;
-        uint2 f;
-        f.x = pack_f16x2(qr[c0], qr[c0 + 1]);
-        f.y = pack_f16x2(qr[c1], qr[c1 + 1]);
-        frag_mse[((size_t)nt * 8 + s) * 32 + lane] = f;
-        if (c.mode == TQ_PROD) {
-          f.x = pack_f16x2(sq[c0], sq[c0 + 1]);
-          f.y = pack_f16x2(sq[c1], sq[c1 + 1]);
-          frag_qjl[((size_t)nt * 8 + s) * 32 + lane] = f;
-        }
-      }
+  if (tid < 32) {
+    const int s = tid >> 2, t = tid & 3, g = m & 7, nt = m >> 3;
+    const int ln = 4 * g + t;
+    const int c0 = 32 * t + 4 * s, c1 = c0 + 2;
+    uint2 f;
+    f.x = pack_f16x2(qr[c0], qr[c0 + 1]);
+    f.y = pack_f16x2(qr[c1], qr[c1 + 1]);
+    frag_mse[((size_t)nt * 8 + s) * 32 + ln] = f;
+    if (prod) {
+      f.x = pack_f16x2(sq[c0], sq[c0 + 1]);
+      f.y = pack_f16x2(sq[c1], sq[c1 + 1]);
+      frag_qjl[((size_t)nt * 8 + s) * 32 + ln] = f;
+    }
   }
 }
 
@@ -196,7 +215,7 @@ tq_status launch_scores(const DevCtx& c, const float* q, int M, const tq_codes* 
   const size_t tiles = (size_t)(M + 7) / 8;
   uint2* fm = static_cast<uint2*>(ws);
   uint2* fq = fm + tiles * 8 * 32;
-  scores_qprep_kernel<<<(int)(tiles * 8), 128, 0, stream>>>(c, q, M, fm, fq);
+  scores_qprep_kernel<<<(int)(tiles * 8), 256, 0, stream>>>(c, q, M, fm, fq);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e);
   ScoreParams p;
