@@ -27,12 +27,11 @@
 namespace tq {
 
 constexpr int kTileTok = 16;
-constexpr int kMaxTilesPerItem = 32;
 constexpr int kDecWarps = 8;
-constexpr int kMaxRounds = kMaxTilesPerItem / kDecWarps;  // tile rounds staged per item
+// resident split CTAs per SM (register budget: 2 for up to 4 heads per KV head, 1 for 8)
+static int ctas_per_sm(int G) { return G >= 8 ? 1 : 2; }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.f;          // rescale only when the max grows by > 2^8
-constexpr uint32_t kSpinLimit = 1u << 22;  // bounded mbarrier wait (~0.1-1 s)
 
 struct DecPlan {
   int S;           // splits (work items) per (batch, kv head)
@@ -41,72 +40,26 @@ struct DecPlan {
   int NT;          // 8-column n-tiles (2·G columns)
 };
 
-static DecPlan make_plan(int B, int Hq, int Hkv, int64_t seq, int tmax = 8) {
+static DecPlan make_plan(int B, int Hq, int Hkv, int64_t seq) {
   DecPlan pl;
   pl.tiles = (int)((seq + kTileTok - 1) / kTileTok);
   const int groups = std::max(1, B * Hkv);
-  const int target = 2 * num_sms();
-  int S = std::max((pl.tiles + tmax - 1) / tmax, (target + groups - 1) / groups);
-  S = std::max(1, std::min(S, pl.tiles));
+  const int G = Hkv > 0 ? Hq / Hkv : 1;
+  const int ctas = ctas_per_sm(G) * num_sms();
+  int S = std::max(1, (ctas + groups - 1) / groups);
+  S = std::min(S, pl.tiles);
   pl.per_item = (pl.tiles + S - 1) / S;
   pl.S = (pl.tiles + pl.per_item - 1) / pl.per_item;
-  const int G = Hkv > 0 ? Hq / Hkv : 1;
   pl.NT = (2 * G + 7) / 8;
   return pl;
 }
 
 size_t decode_ws_bytes(int d, int B, int Hq, int Hkv, int64_t seq) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || seq <= 0) return 256;
-  DecPlan pl = make_plan(B, Hq, Hkv, seq, 8);  // tmax 8 gives the most splits: an upper bound
+  DecPlan pl = make_plan(B, Hq, Hkv, seq);
   size_t frag = (size_t)B * Hkv * 8 * pl.NT * 32 * sizeof(uint2);
   size_t part = (size_t)B * Hq * pl.S * (2 + 128) * sizeof(float);
   return (frag + 255) / 256 * 256 + part + 256;
-}
-
-// ------------------------------------------------------------------ PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-}
-// programmatic dependent launch: wait for the preceding grid / let the next one start
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch() {
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-}
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
 }
 
 // ------------------------------------------------------------------ query prep
@@ -173,30 +126,36 @@ __global__ void __launch_bounds__(256) decode_qprep_kernel(const float* __restri
   }
 }
 
-// Shared-memory layout of the split kernel (byte offsets, host-computed).
+// Word loads as one vector access where the width allows it (4 words are
+// 16-byte aligned, 2 words 8-byte aligned, in every layout read here).
+// Codes are read once: streaming loads that do not keep the lines in L1.
+template <int N>
+__device__ __forceinline__ void ldg_words(uint32_t (&w)[N], const uint32_t* src) {
+  if constexpr (N == 4) {
+    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(src));
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if constexpr (N == 2) {
+    const uint2 v = __ldcs(reinterpret_cast<const uint2*>(src));
+    w[0] = v.x; w[1] = v.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = __ldcs(src + i);
+  }
+}
+
+// Shared memory of the split kernel: the pair tables of K (and of V when its
+// codebook differs), replicated once per lane so that lookups never conflict,
+// and the scratch in which the 8 warps of a CTA combine their softmax states.
 struct DecSmem {
-  int off_vlut, off_kc, off_vc, off_kn, off_vn, off_bar, bytes;
-  int tmax;  // tiles per work item at most
+  int off_vlut, off_comb, bytes;
 };
 
 static DecSmem dec_smem(int bk, int bv, int G, bool same_lut) {
   DecSmem m;
   const int lutk = (1 << (2 * bk)) * 32 * 4, lutv = same_lut ? 0 : (1 << (2 * bv)) * 32 * 4;
-  const int comb = kDecWarps * G * 130 * 4;
-  const int per_tile = kTileTok * (4 * bk + 4 * bv) * 4 + 2 * kTileTok * 4;
-  const int budget = 110 * 1024 - lutk - lutv - 64;
-  int tmax = budget / per_tile;
-  tmax = std::max(8, std::min(kMaxTilesPerItem, tmax / 8 * 8));
-  m.tmax = tmax;
   m.off_vlut = lutk;
-  m.off_kc = lutk + lutv;
-  m.off_vc = m.off_kc + tmax * kTileTok * 4 * bk * 4;
-  m.off_kn = m.off_vc + tmax * kTileTok * 4 * bv * 4;
-  m.off_vn = m.off_kn + tmax * kTileTok * 4;
-  int end_stage = m.off_vn + tmax * kTileTok * 4;
-  int end_comb = m.off_kc + comb;  // the warp-combine scratch reuses the staging area
-  m.off_bar = (std::max(end_stage, end_comb) + 15) / 16 * 16;
-  m.bytes = m.off_bar + 64;
+  m.off_comb = lutk + lutv;
+  m.bytes = m.off_comb + kDecWarps * G * 130 * 4;
   return m;
 }
 
@@ -214,68 +173,68 @@ struct DecParams {
   DecPlan pl;
   const uint2* qfrag;
   float* part;           // [B*Hq][S][130]: m, l, acc[128]
-  int* status;
   DecSmem sm;
   int same_lut;
 };
 
+// One tile's operands, loaded one tile ahead of its use.
+template <int BK, int BV>
+struct TileRegs {
+  uint32_t k0[BK], k1[BK], v0[BV], v1[BV];
+  float nk0, nk1, nv0, nv1;
+};
+
+template <int BK, int BV>
+__device__ __forceinline__ void load_tile(TileRegs<BK, BV>& r, const uint32_t* kb, const uint32_t* vb,
+                                          const float* knb, const float* vnb, int lt0, int g, int t) {
+  constexpr int WK = 4 * BK, WV = 4 * BV;
+  ldg_words<BK>(r.k0, kb + (size_t)(lt0 + g) * WK + t * BK);
+  ldg_words<BK>(r.k1, kb + (size_t)(lt0 + g + 8) * WK + t * BK);
+  // V pair blocks t and t+4 of the tile (tokens 2t,2t+1 and 2t+8,2t+9); coordinates 16g..16g+15
+  ldg_words<BV>(r.v0, vb + (size_t)((lt0 >> 1) + t) * (2 * WV) + g * BV);
+  ldg_words<BV>(r.v1, vb + (size_t)((lt0 >> 1) + 4 + t) * (2 * WV) + g * BV);
+  r.nk0 = __ldcs(knb + lt0 + g);
+  r.nk1 = __ldcs(knb + lt0 + g + 8);
+  r.nv0 = __ldcs(vnb + lt0 + g);
+  r.nv1 = __ldcs(vnb + lt0 + g + 8);
+}
+
 template <int BK, int BV, int G>
-__global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p) {
+__global__ void __launch_bounds__(256, (G >= 8 ? 1 : 2)) decode_split_kernel(const DecParams p) {
   constexpr int NT = (2 * G + 7) / 8;
   constexpr int WK = 4 * BK, WV = 4 * BV;  // words per vector (d = 128)
   constexpr int EK = 1 << (2 * BK), EV = 1 << (2 * BV);
   extern __shared__ __align__(128) unsigned char smem[];
   uint32_t* klut = reinterpret_cast<uint32_t*>(smem);
   uint32_t* vlut = p.same_lut ? klut : reinterpret_cast<uint32_t*>(smem + p.sm.off_vlut);
-  uint32_t* skc = reinterpret_cast<uint32_t*>(smem + p.sm.off_kc);
-  uint32_t* svc = reinterpret_cast<uint32_t*>(smem + p.sm.off_vc);
-  float* skn = reinterpret_cast<float*>(smem + p.sm.off_kn);
-  float* svn = reinterpret_cast<float*>(smem + p.sm.off_vn);
-  float* comb = reinterpret_cast<float*>(smem + p.sm.off_kc);  // reused after the tile loop
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + p.sm.off_bar);
-  volatile int& s_abort = *reinterpret_cast<int*>(smem + p.sm.off_bar + 8 * kMaxRounds);
+  float* comb = reinterpret_cast<float*>(smem + p.sm.off_comb);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
-  for (int i = tid; i < EK * 32; i += blockDim.x) klut[i] = p.klut[i >> 5];
-  if (!p.same_lut)
-    for (int i = tid; i < EV * 32; i += blockDim.x) vlut[i] = p.vlut[i >> 5];
-  if (tid == 0) {
-    for (int r = 0; r < kMaxRounds; ++r) mbar_init(bar + r, 1);
-    fence_mbar_init();
-    s_abort = 0;
+#pragma unroll 8
+  for (int i = tid; i < EK * 32; i += blockDim.x) klut[i] = __ldg(p.klut + (i >> 5));
+  if (!p.same_lut) {
+#pragma unroll 8
+    for (int i = tid; i < EV * 32; i += blockDim.x) vlut[i] = __ldg(p.vlut + (i >> 5));
   }
   __syncthreads();
   griddep_wait();    // codes (appends), query fragments and partials of earlier grids
   griddep_launch();  // the merge grid may start staging its tables
+  const uint32_t* mykl = klut + lane;
+  const uint32_t* myvl = vlut + lane;
 
-  const int groups = p.B * p.Hkv;
-  const int n_items = groups * p.pl.S;
-  uint32_t phases = 0;  // parity bit per round barrier (flipped only when the round was armed)
+  const int n_items = p.B * p.Hkv * p.pl.S;
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int bk = item / p.pl.S, sp = item % p.pl.S;
     const int tile0 = sp * p.pl.per_item;
     const int ntl = min(p.pl.per_item, p.pl.tiles - tile0);
     const int64_t tok0 = (int64_t)tile0 * kTileTok;
-    const int ntok = ntl * kTileTok;  // staged tokens (whole tiles, inside cap)
-    const int64_t vbase = (int64_t)bk * p.cap + tok0;  // vector index of the first token
-    const int nrounds = (ntl + kDecWarps - 1) / kDecWarps;
-    if (tid == 0) {
-      fence_proxy_async();
-      for (int r = 0; r < nrounds; ++r) {
-        const int rt0 = r * kDecWarps * kTileTok;  // first local token of the round
-        const int rtok = min(kDecWarps, ntl - r * kDecWarps) * kTileTok;
-        const uint32_t kb = (uint32_t)rtok * WK * 4, vb = (uint32_t)rtok * WV * 4,
-                       nb = (uint32_t)rtok * 4;
-        mbar_arrive_expect_tx(bar + r, kb + vb + 2 * nb);
-        bulk_g2s(skc + rt0 * WK, p.kcodes + (vbase + rt0) * WK, kb, bar + r);
-        bulk_g2s(svc + rt0 * WV, p.vcodes + (vbase + rt0) * WV, vb, bar + r);  // even: pairs align
-        bulk_g2s(skn + rt0, p.knorm + vbase + rt0, nb, bar + r);
-        bulk_g2s(svn + rt0, p.vnorm + vbase + rt0, nb, bar + r);
-      }
-    }
+    const int64_t vbase = (int64_t)bk * p.cap + tok0;  // vector index of the item's first token
+    const uint32_t* kb = p.kcodes + vbase * WK;
+    const uint32_t* vb = p.vcodes + vbase * WV;  // vbase even: pair blocks align
+    const float* knb = p.knorm + vbase;
+    const float* vnb = p.vnorm + vbase;
 
-    // ---- per-warp state
     uint2 qf[8][NT];
 #pragma unroll
     for (int s = 0; s < 8; ++s)
@@ -290,41 +249,24 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
     }
-    const uint32_t* mykl = klut + lane;
-    const uint32_t* myvl = vlut + lane;
 
+    TileRegs<BK, BV> cur, nxt;
+    if (warp < ntl) load_tile<BK, BV>(cur, kb, vb, knb, vnb, warp * kTileTok, g, t);
     for (int tl = warp; tl < ntl; tl += kDecWarps) {
-      {  // bounded wait for this round's bytes
-        uint32_t spins = 0;
-        bool ok = false;
-        while (!(ok = mbar_try_wait(bar + tl / kDecWarps, (phases >> (tl / kDecWarps)) & 1u)) &&
-               ++spins < kSpinLimit) {
-        }
-        if (!ok) {
-          atomicExch(p.status, 1);
-          s_abort = 1;
-          break;
-        }
-      }
       const int lt0 = tl * kTileTok;  // local token index of the tile
-      // ---------------- K side
-      uint32_t kw0[BK], kw1[BK];
-#pragma unroll
-      for (int w = 0; w < BK; ++w) {
-        kw0[w] = skc[(lt0 + g) * WK + t * BK + w];
-        kw1[w] = skc[(lt0 + g + 8) * WK + t * BK + w];
-      }
-      float sa[NT][4], sb[NT][4];  // even / odd k-steps: two independent MMA chains
+      if (tl + kDecWarps < ntl) load_tile<BK, BV>(nxt, kb, vb, knb, vnb, lt0 + kDecWarps * kTileTok, g, t);
+      // ---------------- K side: S = K̂·Q (two independent MMA chains)
+      float sa[NT][4], sb[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const uint32_t a0 = mykl[get_bits<2 * BK>(kw0, 4 * s * BK) << 5];
-        const uint32_t a1 = mykl[get_bits<2 * BK>(kw1, 4 * s * BK) << 5];
-        const uint32_t a2 = mykl[get_bits<2 * BK>(kw0, (4 * s + 2) * BK) << 5];
-        const uint32_t a3 = mykl[get_bits<2 * BK>(kw1, (4 * s + 2) * BK) << 5];
+        const uint32_t a0 = mykl[get_bits<2 * BK>(cur.k0, 4 * s * BK) << 5];
+        const uint32_t a1 = mykl[get_bits<2 * BK>(cur.k1, 4 * s * BK) << 5];
+        const uint32_t a2 = mykl[get_bits<2 * BK>(cur.k0, (4 * s + 2) * BK) << 5];
+        const uint32_t a3 = mykl[get_bits<2 * BK>(cur.k1, (4 * s + 2) * BK) << 5];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           if (s & 1)
@@ -333,21 +275,15 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
             mma16816(sa[nt], a0, a1, a2, a3, qf[s][nt].x, qf[s][nt].y);
         }
       }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sa[nt][e] += sb[nt][e];
-      const float sk0 = skn[lt0 + g], sk1 = skn[lt0 + g + 8];
       const bool v0 = tok0 + lt0 + g < p.seq, v1 = tok0 + lt0 + g + 8 < p.seq;
-      const float sv0 = svn[lt0 + g], sv1 = svn[lt0 + g + 8];
       // ---------------- online softmax per head h = 4nt + t (lanes of equal t)
       float w0[NT], w1[NT];  // p·s_v·fold for tokens g, g+8 of head 4nt+t
       bool need = false;
       float zz0[NT], zz1[NT], mx[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        zz0[nt] = v0 ? (sa[nt][0] + sa[nt][1]) * sk0 : -INFINITY;
-        zz1[nt] = v1 ? (sa[nt][2] + sa[nt][3]) * sk1 : -INFINITY;
+        zz0[nt] = v0 ? (sa[nt][0] + sb[nt][0] + sa[nt][1] + sb[nt][1]) * cur.nk0 : -INFINITY;
+        zz1[nt] = v1 ? (sa[nt][2] + sb[nt][2] + sa[nt][3] + sb[nt][3]) * cur.nk1 : -INFINITY;
         float m = fmaxf(zz0[nt], zz1[nt]);
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
@@ -371,11 +307,11 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
       }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const float p0 = (m_run[nt] == -INFINITY) ? 0.f : ex2(zz0[nt] - m_run[nt]);
-        const float p1 = (m_run[nt] == -INFINITY) ? 0.f : ex2(zz1[nt] - m_run[nt]);
+        const float p0 = ex2(zz0[nt] - m_run[nt]);
+        const float p1 = ex2(zz1[nt] - m_run[nt]);
         l_run[nt] += p0 + p1;
-        w0[nt] = p0 * sv0 * p.v_fold;
-        w1[nt] = p1 * sv1 * p.v_fold;
+        w0[nt] = p0 * cur.nv0 * p.v_fold;
+        w1[nt] = p1 * cur.nv1 * p.v_fold;
       }
       // ---------------- V side: B[k = token][n = col g] for tokens 2t,2t+1,2t+8,2t+9
       uint32_t bw[NT][2];
@@ -387,49 +323,29 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
         const float x1 = __shfl_sync(kFull, w0[nt], src1);  // token 2t+1
         const float x2 = __shfl_sync(kFull, w1[nt], src0);  // token 2t+8
         const float x3 = __shfl_sync(kFull, w1[nt], src1);  // token 2t+9
-        const bool lo = g & 1;
         const bool head_ok = 4 * nt + h4 < G;
-        float y0 = x0, y1 = x1, y2 = x2, y3 = x3;
-        const float hi0 = __half2float(__float2half_rn(x0)), hi1 = __half2float(__float2half_rn(x1));
-        const float hi2 = __half2float(__float2half_rn(x2)), hi3 = __half2float(__float2half_rn(x3));
-        if (lo) {
-          y0 = x0 - hi0; y1 = x1 - hi1; y2 = x2 - hi2; y3 = x3 - hi3;
+        float y0 = __half2float(__float2half_rn(x0)), y1 = __half2float(__float2half_rn(x1));
+        float y2 = __half2float(__float2half_rn(x2)), y3 = __half2float(__float2half_rn(x3));
+        if (g & 1) {  // lo column: the rounding residual of the hi column
+          y0 = x0 - y0; y1 = x1 - y1; y2 = x2 - y2; y3 = x3 - y3;
         }
         bw[nt][0] = head_ok ? pack_f16x2(y0, y1) : 0u;
         bw[nt][1] = head_ok ? pack_f16x2(y2, y3) : 0u;
       }
-      // V pair blocks t and t+4 of the tile; this lane's BV words at g·BV
-      uint32_t vw0[BV], vw1[BV];
-      const int pb0 = (lt0 >> 1) + t, pb1 = pb0 + 4;
-#pragma unroll
-      for (int w = 0; w < BV; ++w) {
-        vw0[w] = svc[pb0 * (2 * WV) + g * BV + w];
-        vw1[w] = svc[pb1 * (2 * WV) + g * BV + w];
-      }
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         // rows g / g+8 <-> coordinates 16g + 2mt / 16g + 2mt + 1
-        const uint32_t a0 = myvl[get_bits<2 * BV>(vw0, (2 * mt) * 2 * BV) << 5];
-        const uint32_t a1 = myvl[get_bits<2 * BV>(vw0, (2 * mt + 1) * 2 * BV) << 5];
-        const uint32_t a2 = myvl[get_bits<2 * BV>(vw1, (2 * mt) * 2 * BV) << 5];
-        const uint32_t a3 = myvl[get_bits<2 * BV>(vw1, (2 * mt + 1) * 2 * BV) << 5];
+        const uint32_t a0 = myvl[get_bits<2 * BV>(cur.v0, (2 * mt) * 2 * BV) << 5];
+        const uint32_t a1 = myvl[get_bits<2 * BV>(cur.v0, (2 * mt + 1) * 2 * BV) << 5];
+        const uint32_t a2 = myvl[get_bits<2 * BV>(cur.v1, (2 * mt) * 2 * BV) << 5];
+        const uint32_t a3 = myvl[get_bits<2 * BV>(cur.v1, (2 * mt + 1) * 2 * BV) << 5];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma16816(o[mt][nt], a0, a1, a2, a3, bw[nt][0], bw[nt][1]);
       }
+      cur = nxt;
     }
 
     // ---------------- combine the 8 warps of the CTA, write the item's partials
-    __syncthreads();  // every warp is done with the staged codes (comb aliases them)
-    if (s_abort) {
-      if (tid == 0) {  // let the copies in flight land before leaving (bounded waits)
-        for (int r = 0; r < nrounds; ++r) {
-          uint32_t spins = 0;
-          while (!mbar_try_wait(bar + r, (phases >> r) & 1u) && ++spins < kSpinLimit) {
-          }
-        }
-      }
-      return;
-    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float l = l_run[nt];
@@ -437,31 +353,34 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
       l += __shfl_xor_sync(kFull, l, 8);
       l += __shfl_xor_sync(kFull, l, 16);
       const int h = 4 * nt + t;
-      if (g == 0 && h < G) {
-        comb[(warp * G + h) * 130 + 0] = m_run[nt];
-        comb[(warp * G + h) * 130 + 1] = l;
-      }
       if (h < G) {
+        float* cw = comb + (warp * G + h) * 130;
+        if (g == 0) {
+          cw[0] = m_run[nt];
+          cw[1] = l;
+        }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          comb[(warp * G + h) * 130 + 2 + 16 * g + 2 * mt] = o[mt][nt][0] + o[mt][nt][1];
-          comb[(warp * G + h) * 130 + 2 + 16 * g + 2 * mt + 1] = o[mt][nt][2] + o[mt][nt][3];
+          cw[2 + 16 * g + 2 * mt] = o[mt][nt][0] + o[mt][nt][1];
+          cw[2 + 16 * g + 2 * mt + 1] = o[mt][nt][2] + o[mt][nt][3];
         }
       }
     }
     __syncthreads();
+    const int b = bk / p.Hkv, kvh = bk % p.Hkv;
     for (int e = tid; e < G * 128; e += blockDim.x) {
-      const int h = e / 128, dim = e % 128;
+      const int h = e >> 7, dim = e & 127;
       float M = -INFINITY;
+#pragma unroll
       for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, comb[(w * G + h) * 130]);
       float L = 0.f, A = 0.f;
+#pragma unroll
       for (int w = 0; w < kDecWarps; ++w) {
         const float mw = comb[(w * G + h) * 130];
         const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
         L += f * comb[(w * G + h) * 130 + 1];
         A += f * comb[(w * G + h) * 130 + 2 + dim];
       }
-      const int b = bk / p.Hkv, kvh = bk % p.Hkv;
       float* dst = p.part + (((size_t)b * p.Hq + kvh * G + h) * p.pl.S + sp) * 130;
       if (dim == 0) {
         dst[0] = M;
@@ -469,8 +388,7 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecParams p)
       }
       dst[2 + dim] = A;
     }
-    __syncthreads();  // staging and comb are reused by the next item
-    phases ^= (1u << nrounds) - 1u;
+    __syncthreads();  // comb is reused by the next item
   }
 }
 
@@ -578,7 +496,7 @@ static cudaError_t run_split(const DecParams& p, cudaStream_t st) {
     attr_done = 1;
   }
   const int items = p.B * p.Hkv * p.pl.S;
-  const int grid = std::max(1, std::min(items, 2 * num_sms()));
+  const int grid = std::max(1, std::min(items, ctas_per_sm(G) * num_sms()));
   return launch_pdl(k, grid, 256, (size_t)p.sm.bytes, st, p);
 }
 
@@ -613,7 +531,7 @@ tq_status launch_decode(const DevCtx& kc, const DevCtx& vc, const void* q, int q
   bool same_lut = kc.b_mse == vc.b_mse && kc.alpha == vc.alpha;
   for (int k = 0; same_lut && k < (1 << kc.b_mse); ++k) same_lut = kc.cen[k] == vc.cen[k];
   const DecSmem sm = dec_smem(kc.b_mse, vc.b_mse, G, same_lut);
-  const DecPlan pl = make_plan(B, Hq, Hkv, seq, sm.tmax);
+  const DecPlan pl = make_plan(B, Hq, Hkv, seq);
   uint2* frag = static_cast<uint2*>(ws);
   size_t frag_bytes = (size_t)B * Hkv * 8 * pl.NT * 32 * sizeof(uint2);
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + (frag_bytes + 255) / 256 * 256);
@@ -638,7 +556,6 @@ tq_status launch_decode(const DevCtx& kc, const DevCtx& vc, const void* q, int q
   p.pl = pl;
   p.qfrag = frag;
   p.part = part;
-  p.status = kc.status;
   p.sm = sm;
   p.same_lut = same_lut ? 1 : 0;
   switch (kc.b_mse) {

@@ -58,16 +58,39 @@ __device__ __forceinline__ uint32_t pair_slot_mask(int w, int slot) {
 
 template <int BM, bool PROD, bool F16>
 __global__ void __launch_bounds__(256, 1) encode_kernel(const EncParams p) {
-  extern __shared__ uint2 smem[];
+  extern __shared__ __align__(128) uint2 smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_abort;
   const int d = p.c.d;
   const int KS = d >> 4;
   constexpr int kFragPerS = 16 * 2 * 32;
   uint2* sPi = smem;
   uint2* sM = smem + 8 * kFragPerS;
-  for (int i = threadIdx.x; i < KS * kFragPerS; i += blockDim.x) sPi[i] = p.c.enc_pi[i];
-  if (PROD)
-    for (int i = threadIdx.x; i < 8 * kFragPerS; i += blockDim.x) sM[i] = p.c.enc_m[i];
+  // the operand tables arrive by bulk asynchronous copies (one latency, no
+  // per-thread load chains); waits are bounded and report through the status word
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const uint32_t bpi = (uint32_t)(KS * kFragPerS * sizeof(uint2));
+    const uint32_t bm = PROD ? (uint32_t)(8 * kFragPerS * sizeof(uint2)) : 0u;
+    mbar_arrive_expect_tx(&bar, bpi + bm);
+    bulk_g2s(sPi, p.c.enc_pi, bpi, &bar);
+    if (PROD) bulk_g2s(sM, p.c.enc_m, bm, &bar);
+  }
   __syncthreads();
+  {
+    uint32_t spins = 0;
+    bool ok = false;
+    while (!(ok = mbar_try_wait(&bar, 0)) && ++spins < kSpinLimitDev) {
+    }
+    if (!ok) {
+      atomicExch(p.c.status, 1);
+      s_abort = 1;
+    }
+  }
+  __syncthreads();
+  if (s_abort) return;  // the copies were waited for (bounded) by every thread above
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
