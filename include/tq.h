@@ -227,6 +227,33 @@ tq_status tq_decode_attention(const tq_ctx* kctx, const tq_ctx* vctx, const void
                               int Hkv, int64_t seq, int64_t cap, float scale, float* d_out,
                               void* d_ws, size_t ws_bytes, tq_stream stream);
 
+/* ------------------------------------------------------------------ decode, no workspace
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory: code running where cudaMalloc is unavailable
+ * or forbidden (inside a host callback or a driver-managed region, a fixed
+ * memory-budget runtime, or a plugin that may not own allocations) and so
+ * cannot hand tq_decode_attention a workspace either.
+ *
+ * Same computation, arguments and results as tq_decode_attention, minus d_ws
+ * and ws_bytes.  Its scratch is a 2 MiB array built into the library, which
+ * every GPU that loads libtq keeps reserved until the process exits.
+ *   - Shapes whose scratch (tq_decode_workspace_size) exceeds 2 MiB return
+ *     TQ_ERR_UNSUPPORTED before anything is launched.  For B = 1, 8 KV heads,
+ *     head_dim 128 the need is about 0.7 MB at any sequence length.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the array: two calls that overlap on the GPU (different
+ *     streams, no ordering between them) race and corrupt each other's output.
+ *     Order them on one stream.  Nothing in the array needs clearing between
+ *     calls: each call writes every scratch byte it reads.
+ * The call itself allocates nothing (no cudaMalloc or allocating library routine).
+ */
+tq_status tq_decode_attention_noalloc(const tq_ctx* kctx, const tq_ctx* vctx, const void* d_q,
+                                      int q_dtype, const tq_codes* K, const tq_codes* V, int B,
+                                      int Hq, int Hkv, int64_t seq, int64_t cap, float scale,
+                                      float* d_out, tq_stream stream);
+
 /* ------------------------------------------------------------------ views
  * Canonical view of stored codes, for checking: copies vectors
  * [first, first + count) to the host and writes their coordinate indices

@@ -19,6 +19,7 @@
 // merge kernel applies Πᵀ once per head after combining the splits with the
 // usual log-sum-exp rule.
 #include <algorithm>
+#include <mutex>
 #include <utility>
 
 #include "tq_device.cuh"
@@ -576,6 +577,52 @@ tq_status launch_decode(const DevCtx& kc, const DevCtx& vc, const void* q, int q
   e = launch_pdl(decode_merge_kernel, B * Hq, 256, msmem, stream, (const float*)vc.pi, (const float*)part,
                  pl.S, out);
   return e == cudaSuccess ? TQ_OK : set_cuda_error(e);
+}
+
+// ------------------------------------------------------------------ decode without a workspace
+// Scratch for tq_decode_attention_noalloc: the query fragments and the split
+// partials that tq_decode_attention keeps in the caller's workspace.  It is a
+// file-scope device array, so the driver reserves it on every GPU that loads
+// the library, and it stays reserved until the process exits.  Every call
+// writes each byte of it that the call later reads, so nothing in it has to
+// start at zero; concurrent calls (on different streams) would race on it.
+constexpr size_t kNoAllocScratchBytes = (size_t)2 << 20;  // 2 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+size_t decode_noalloc_limit() { return kNoAllocScratchBytes; }
+
+// Device address of the scratch array on the current device.  The host-side
+// symbol is only a stand-in, so the address is asked from the runtime once per
+// device (with that device current) and cached.
+static cudaError_t decode_scratch_address(void** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+tq_status launch_decode_noalloc(const DevCtx& kc, const DevCtx& vc, const void* q, int q_dtype,
+                                const tq_codes* K, const tq_codes* V, int B, int Hq, int Hkv,
+                                int64_t seq, int64_t cap, float scale, float* out,
+                                cudaStream_t stream) {
+  const size_t need = decode_ws_bytes(kc.d, B, Hq, Hkv, seq);
+  if (need > kNoAllocScratchBytes) return TQ_ERR_UNSUPPORTED;
+  void* ws = nullptr;
+  cudaError_t e = decode_scratch_address(&ws);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  return launch_decode(kc, vc, q, q_dtype, K, V, B, Hq, Hkv, seq, cap, scale, out, ws, need, stream);
 }
 
 }  // namespace tq

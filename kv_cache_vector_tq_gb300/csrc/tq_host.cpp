@@ -655,6 +655,35 @@ tq_status tq_decode_attention(const tq_ctx* kctx, const tq_ctx* vctx, const void
                        ws_bytes, (cudaStream_t)stream);
 }
 
+// Same checks as tq_decode_attention, without the workspace arguments.
+tq_status tq_decode_attention_noalloc(const tq_ctx* kctx, const tq_ctx* vctx, const void* d_q,
+                                      int q_dtype, const tq_codes* K, const tq_codes* V, int B,
+                                      int Hq, int Hkv, int64_t seq, int64_t cap, float scale,
+                                      float* d_out, tq_stream stream) {
+  if (!kctx || !vctx || !K || !V) return TQ_ERR_INVALID_ARG;
+  const DevCtx& kc = reinterpret_cast<const Ctx*>(kctx)->dev;
+  const DevCtx& vc = reinterpret_cast<const Ctx*>(vctx)->dev;
+  if (kc.mode != TQ_MSE || vc.mode != TQ_MSE || kc.d != vc.d) return TQ_ERR_INVALID_ARG;
+  tq_status st = check_codes(kc, K);
+  if (st != TQ_OK) return st;
+  st = check_codes(vc, V);
+  if (st != TQ_OK) return st;
+  if (K->layout != TQ_LAYOUT_TOKEN || V->layout != TQ_LAYOUT_PAIR) return TQ_ERR_INVALID_ARG;
+  if (q_dtype != TQ_F32 && q_dtype != TQ_F16) return TQ_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || seq <= 0 || cap < seq || (cap & 1))
+    return TQ_ERR_INVALID_ARG;
+  const int gqa = Hq / Hkv;
+  if (gqa != 1 && gqa != 2 && gqa != 4 && gqa != 8) return TQ_ERR_UNSUPPORTED;
+  if ((int64_t)B * Hkv * cap > K->n || (int64_t)B * Hkv * cap > V->n) return TQ_ERR_INVALID_ARG;
+  if (!d_q || !d_out || !al16(d_q)) return TQ_ERR_INVALID_ARG;
+  if (!al16(K->d_norm) || !al16(V->d_norm)) return TQ_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
+  if (kc.d != kChunk) return TQ_ERR_UNSUPPORTED;
+  if (decode_ws_bytes(kc.d, B, Hq, Hkv, seq) > decode_noalloc_limit()) return TQ_ERR_UNSUPPORTED;
+  return launch_decode_noalloc(kc, vc, d_q, q_dtype, K, V, B, Hq, Hkv, seq, cap, scale, d_out,
+                               (cudaStream_t)stream);
+}
+
 tq_status tq_unpack_indices(const tq_codes* codes, int64_t first, int64_t count, uint8_t* h_idx,
                             uint8_t* h_bits) {
   if (!codes || !codes->d_codes || !h_idx || first < 0 || count < 0 || first + count > codes->n)

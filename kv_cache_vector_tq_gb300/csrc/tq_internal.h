@@ -61,6 +61,11 @@ tq_status launch_decode(const DevCtx& kc, const DevCtx& vc, const void* q, int q
                         int64_t cap, float scale, float* out, void* ws, size_t ws_bytes,
                         cudaStream_t stream);
 size_t decode_ws_bytes(int d, int B, int Hq, int Hkv, int64_t seq);
+tq_status launch_decode_noalloc(const DevCtx& kc, const DevCtx& vc, const void* q, int q_dtype,
+                                const tq_codes* K, const tq_codes* V, int B, int Hq, int Hkv,
+                                int64_t seq, int64_t cap, float scale, float* out,
+                                cudaStream_t stream);
+size_t decode_noalloc_limit();
 int num_sms();
 
 }  // namespace tq

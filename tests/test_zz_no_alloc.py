@@ -1,0 +1,78 @@
+"""tq_decode_attention_noalloc: decode attention for callers that cannot
+allocate device memory (and so cannot pass a workspace either), e.g. code that
+runs where cudaMalloc is unavailable or forbidden.  Its scratch is an array
+built into the library.
+
+This file is collected last on purpose.  The test calls the entry point through
+the C ABI twice in a row and compares each result with tq_decode_attention
+(the call with a caller-provided workspace) at the attention tolerance used by
+the parity tests; it also checks that a shape needing more scratch than the
+built-in array is refused before anything runs.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import kv_cache_vector_tq_gb300 as tq  # noqa: E402
+from kv_cache_vector_tq_gb300 import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tq.lib()
+
+
+def _context(seed, d, b):
+    G = synth.gaussian_matrix(seed, d)
+    return tq.Context(d, b, tq.TQ_MSE, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(G))
+
+
+def test_noalloc_matches_workspace_call_twice():
+    d, b, B, Hq, Hkv, seq = 128, 4, 1, 32, 8, 4099
+    cap = (seq + 15) // 16 * 16
+    ctx = _context(11, d, b)
+    Kh, Vh = synth.kv_layer(11, 0, B, Hkv, seq, d)
+    Kc = tq.CodeSet(ctx, B * Hkv * cap, tq.TQ_LAYOUT_TOKEN)
+    Vc = tq.CodeSet(ctx, B * Hkv * cap, tq.TQ_LAYOUT_PAIR)
+    tq.tq_encode(ctx, torch.from_numpy(Kh.reshape(-1, d)).cuda(), Kc, 0, seq, cap)
+    tq.tq_encode(ctx, torch.from_numpy(Vh.reshape(-1, d)).cuda(), Vc, 0, seq, cap)
+    scale = 1.0 / math.sqrt(d)
+    ws = torch.empty(tq.tq_decode_workspace_size(ctx, B, Hq, Hkv, seq) // 4 + 4, dtype=torch.float32,
+                     device="cuda")
+    for call in range(2):
+        q = torch.from_numpy(synth.queries(20 + call, B * Hq, d).reshape(B, Hq, d)).cuda().half()
+        ref = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+        tq.tq_decode_attention(ctx, ctx, q, Kc, Vc, B, Hq, Hkv, seq, cap, scale, ref, ws)
+        out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device="cuda")
+        tq.tq_decode_attention_noalloc(ctx, ctx, q, Kc, Vc, B, Hq, Hkv, seq, cap, scale, out)
+        torch.cuda.synchronize()
+        r = ref.cpu().numpy().astype(np.float64)
+        o = out.cpu().numpy().astype(np.float64)
+        assert np.isfinite(o).all()
+        rel = np.linalg.norm(o - r, axis=-1) / np.linalg.norm(r, axis=-1)
+        assert rel.max() <= 2e-3, f"call {call}: max per-head relative difference {rel.max()}"
+    assert ctx.poll() == tq.TQ_OK
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    # 64 sequences x 64 KV heads (no GQA) need more than the 2 MiB built in
+    d, b, B, Hq, Hkv, seq, cap = 128, 2, 64, 64, 64, 16, 16
+    ctx = _context(12, d, b)
+    assert tq.tq_decode_workspace_size(ctx, B, Hq, Hkv, seq) > (2 << 20)
+    Kc = tq.CodeSet(ctx, B * Hkv * cap, tq.TQ_LAYOUT_TOKEN)
+    Vc = tq.CodeSet(ctx, B * Hkv * cap, tq.TQ_LAYOUT_PAIR)
+    q = torch.zeros((B, Hq, d), dtype=torch.float16, device="cuda")
+    out = torch.zeros((B, Hq, d), dtype=torch.float32, device="cuda")
+    with pytest.raises(tq.TqError) as err:
+        tq.tq_decode_attention_noalloc(ctx, ctx, q, Kc, Vc, B, Hq, Hkv, seq, cap, 1.0, out)
+    assert err.value.status == tq.TQ_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert (out == 0).all()
