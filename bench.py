@@ -8,8 +8,8 @@ N(0,1) with 4 outlier channels x10, K and V TurboQuant_MSE at b bits (default
 
 One decode step = append the new token (encode its K and V: 2 x 8 vectors into
 the caches, norm -> rotation -> bucketize -> pack) and attend over the 16384
-tokens (query pre-rotation, split-sequence attention over the packed cache,
-merge + inverse rotation).  A benchmark step runs one decode step on each of R
+tokens (query pre-rotation, attention over the packed cache, merge + inverse
+rotation), all in one fused kernel launch (tq_decode_step).  A benchmark step runs one decode step on each of R
 independent replica caches (distinct HBM regions together larger than 4x L2),
 so every step streams its caches from HBM; the R caches are one batch-1 layer
 each.  Timed steps replay a CUDA graph of one benchmark step.
@@ -190,16 +190,16 @@ def run_tq(args, world, rank, local):
     R = max(2, int(math.ceil(4 * L2_BYTES / cache_bytes)))
     ctx, reps, cap, knew, vnew, q = build_replicas(tq, synth, bits, R)
     scale = 1.0 / math.sqrt(D)
-    ws = torch.empty(tq.tq_decode_workspace_size(ctx, B, HQ, HKV, SEQ) // 4 + 64, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(tq.tq_decode_workspace_size(ctx, B, HQ, HKV, SEQ) // 4 + 64, dtype=torch.float32, device="cuda")
     out = torch.empty((B, HQ, D), dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
 
     def decode_step(r, with_append=True):
         K, V = reps[r]
-        if with_append:
-            tq.tq_encode(ctx, knew, K, SEQ - 1, 1, cap)
-            tq.tq_encode(ctx, vnew, V, SEQ - 1, 1, cap)
-        tq.tq_decode_attention(ctx, ctx, q, K, V, B, HQ, HKV, SEQ, cap, scale, out, ws)
+        if with_append:  # one launch: encode the new token's K/V into slot SEQ-1, then attend
+            tq.tq_decode_step(ctx, ctx, q, knew, vnew, K, V, B, HQ, HKV, SEQ, cap, scale, out, ws)
+        else:
+            tq.tq_decode_attention(ctx, ctx, q, K, V, B, HQ, HKV, SEQ, cap, scale, out, ws)
 
     # eager warm-up (sets kernel attributes outside capture), then graphs
     with torch.cuda.stream(stream):
@@ -286,7 +286,7 @@ def run_tq(args, world, rank, local):
     d2h = R * out.numel() * 4
     assert ctx.poll() == tq.TQ_OK
 
-    launches_per_decode = 2 + 3  # two encode launches, query prep, split, merge
+    launches_per_decode = 1  # the fused decode-step kernel
     line = {
         "metric": "decode-attn HBM GB/s",
         "value": round(value_gbs, 2),
@@ -311,7 +311,7 @@ def run_tq(args, world, rank, local):
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": None,
-            "kernel": "decode attention call (query prep + split + merge)", "peak_kind": peak_kind,
+            "kernel": "decode_step_kernel without the append (one launch per call)", "peak_kind": peak_kind,
             "us_per_call": round(attn_us, 3), "bytes_per_call": attn_bytes,
         },
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

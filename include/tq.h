@@ -215,9 +215,15 @@ tq_status tq_scores(const tq_ctx* ctx, const float* d_q, int M, const tq_codes* 
  * d_q       [B, Hq, d], fp32 or fp16 (q_dtype).
  * K         TOKEN layout; V: PAIR layout.  Vector index of token t of
  *           (batch b, kv head h) is (b * Hkv + h) * cap + t; tokens [0, seq)
- *           are read.  cap must be even.
+ *           are read.  cap must be even (TQ_ERR_INVALID_ARG) and a multiple
+ *           of 16 (TQ_ERR_UNSUPPORTED otherwise).
  * d_out     [B, Hq, d] fp32.
- * d_ws      workspace of tq_decode_workspace_size bytes (16-byte aligned).
+ * d_ws      workspace of tq_decode_workspace_size bytes (16-byte aligned),
+ *           zero-filled before its first use (e.g. cudaMemset).  It holds one
+ *           arrival counter per (batch, KV head) and the partial softmax
+ *           states of the CTAs that share a (batch, KV head); every call
+ *           leaves the counters at zero again.  Calls that share a workspace
+ *           must be ordered on one stream.
  * Hq % Hkv == 0 and Hq / Hkv in {1, 2, 4, 8}.
  */
 tq_status tq_decode_workspace_size(const tq_ctx* kctx, int B, int Hq, int Hkv, int64_t seq,
@@ -227,6 +233,26 @@ tq_status tq_decode_attention(const tq_ctx* kctx, const tq_ctx* vctx, const void
                               int Hkv, int64_t seq, int64_t cap, float scale, float* d_out,
                               void* d_ws, size_t ws_bytes, tq_stream stream);
 
+/* ------------------------------------------------------------------ decode step
+ * One decode step with the step's token appended first ([P1] section
+ * "一个具体例子：KV Cache 在 prefill 和 decode 里怎么量化", decode: the token's K/V is
+ * appended to the cache, then its query attends over the whole history).
+ * d_k_new, d_v_new: [B, Hkv, d] (new_dtype fp32 or fp16, 16-byte aligned).
+ * Encodes them as tq_encode does (norm, rotation, bucketize, pack; the same
+ * codes except for coordinates within about 1e-6 of a codebook threshold,
+ * where the two roundings may fall on either side, and the same norm to fp32
+ * rounding) into position seq-1 of every (batch, KV head) block of K and V,
+ * then computes tq_decode_attention over tokens [0, seq) including the new
+ * one, in one kernel launch.  Other arguments, the workspace and errors as
+ * tq_decode_attention.  The V pair block of position seq-1 is updated with atomics, so
+ * its partner token (seq-2 or seq) may be written by an ordered earlier call.
+ */
+tq_status tq_decode_step(const tq_ctx* kctx, const tq_ctx* vctx, const void* d_q, int q_dtype,
+                         const void* d_k_new, const void* d_v_new, int new_dtype, const tq_codes* K,
+                         const tq_codes* V, int B, int Hq, int Hkv, int64_t seq, int64_t cap,
+                         float scale, float* d_out, void* d_ws, size_t ws_bytes,
+                         tq_stream stream);
+
 /* ------------------------------------------------------------------ decode, no workspace
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory: code running where cudaMalloc is unavailable
@@ -235,18 +261,21 @@ tq_status tq_decode_attention(const tq_ctx* kctx, const tq_ctx* vctx, const void
  * cannot hand tq_decode_attention a workspace either.
  *
  * Same computation, arguments and results as tq_decode_attention, minus d_ws
- * and ws_bytes.  Its scratch is a 2 MiB array built into the library, which
- * every GPU that loads libtq keeps reserved until the process exits.
+ * and ws_bytes.  Its scratch (the counters and partial softmax states that
+ * tq_decode_attention keeps in the workspace) is a 2 MiB array built into the
+ * library, which every GPU that loads libtq keeps reserved until the process
+ * exits.  It starts zero-filled and every call leaves its counters at zero.
  *   - Shapes whose scratch (tq_decode_workspace_size) exceeds 2 MiB return
- *     TQ_ERR_UNSUPPORTED before anything is launched.  For B = 1, 8 KV heads,
- *     head_dim 128 the need is about 0.7 MB at any sequence length.
+ *     TQ_ERR_UNSUPPORTED before anything is launched.  The need is 4 bytes per
+ *     (batch, KV head) plus at most about 80 KB per query head of a KV head
+ *     (0.3 MB for 8 KV heads with 4 query heads each, at any sequence length).
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any stream
  *     capture.
  *   - All calls share the array: two calls that overlap on the GPU (different
  *     streams, no ordering between them) race and corrupt each other's output.
  *     Order them on one stream.  Nothing in the array needs clearing between
- *     calls: each call writes every scratch byte it reads.
+ *     calls: each call writes every state it reads and resets its counters.
  * The call itself allocates nothing (no cudaMalloc or allocating library routine).
  */
 tq_status tq_decode_attention_noalloc(const tq_ctx* kctx, const tq_ctx* vctx, const void* d_q,
@@ -264,8 +293,11 @@ tq_status tq_unpack_indices(const tq_codes* codes, int64_t first, int64_t count,
                             uint8_t* h_bits);
 
 /* Reads and clears the context's device status word (synchronises `stream`).
- * Returns TQ_OK, or TQ_ERR_TIMEOUT if a bounded device wait of a kernel
- * launched with this context ran out since the last poll. */
+ * Returns TQ_OK; TQ_ERR_UNSUPPORTED if a decode kernel launched with this
+ * context (as kctx) found dynamic shared memory at another shared-window
+ * offset than the one its 4-bit table lookups are compiled for, and returned
+ * without writing its output; else TQ_ERR_TIMEOUT if a bounded device wait of
+ * a kernel launched with this context ran out since the last poll. */
 tq_status tq_status_poll(const tq_ctx* ctx, tq_stream stream);
 
 #ifdef __cplusplus

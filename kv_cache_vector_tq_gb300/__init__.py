@@ -24,7 +24,7 @@ EXPORTS = (
     "tq_version", "tq_status_string", "tq_last_cuda_error", "tq_codebook_build",
     "tq_rotation_haar", "tq_ctx_create", "tq_ctx_destroy", "tq_codes_layout", "tq_encode",
     "tq_scores_workspace_size", "tq_scores", "tq_decode_workspace_size",
-    "tq_decode_attention", "tq_decode_attention_noalloc", "tq_unpack_indices", "tq_status_poll",
+    "tq_decode_attention", "tq_decode_step", "tq_decode_attention_noalloc", "tq_unpack_indices", "tq_status_poll",
 )
 
 
@@ -84,6 +84,8 @@ def lib():
         "tq_decode_workspace_size": ([_vp, _i, _i, _i, _i64, P(_sz)], _i),
         "tq_decode_attention": ([_vp, _vp, _vp, _i, P(Codes), P(Codes), _i, _i, _i, _i64, _i64,
                                  _f, _vp, _vp, _sz, _vp], _i),
+        "tq_decode_step": ([_vp, _vp, _vp, _i, _vp, _vp, _i, P(Codes), P(Codes), _i, _i, _i, _i64,
+                            _i64, _f, _vp, _vp, _sz, _vp], _i),
         "tq_decode_attention_noalloc": ([_vp, _vp, _vp, _i, P(Codes), P(Codes), _i, _i, _i, _i64,
                                          _i64, _f, _vp, _vp], _i),
         "tq_unpack_indices": ([P(Codes), _i64, _i64, _vp, _vp], _i),
@@ -233,6 +235,19 @@ def tq_decode_attention(kctx, vctx, q, K, V, B, Hq, Hkv, seq, cap, scale, out, w
         kctx.handle, vctx.handle, ctypes.c_void_p(q.data_ptr()), dt, ctypes.byref(K.desc),
         ctypes.byref(V.desc), B, Hq, Hkv, seq, cap, float(scale), ctypes.c_void_p(out.data_ptr()),
         ctypes.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def tq_decode_step(kctx, vctx, q, k_new, v_new, K, V, B, Hq, Hkv, seq, cap, scale, out, ws, stream=None):
+    """Append k_new/v_new ([B, Hkv, d]) at position seq-1, then attend over seq tokens."""
+    import torch
+    dts = {torch.float32: TQ_F32, torch.float16: TQ_F16}
+    assert k_new.dtype == v_new.dtype
+    _check("tq_decode_step", lib().tq_decode_step(
+        kctx.handle, vctx.handle, ctypes.c_void_p(q.data_ptr()), dts[q.dtype],
+        ctypes.c_void_p(k_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()), dts[k_new.dtype],
+        ctypes.byref(K.desc), ctypes.byref(V.desc), B, Hq, Hkv, seq, cap, float(scale),
+        ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
+        _stream(stream)))
 
 
 def tq_decode_attention_noalloc(kctx, vctx, q, K, V, B, Hq, Hkv, seq, cap, scale, out, stream=None):

@@ -106,6 +106,19 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 __device__ __forceinline__ void griddep_launch() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
+// Shared-window address of a lane's copy of table entry `byte k of w`, for
+// tables laid out as 256-byte rows (one row per index, 4-byte entries at
+// lane·4): byte 0 = lane·4, byte 1 = byte k of w, upper bytes zero.
+__device__ __forceinline__ uint32_t byte_row_addr(uint32_t w, uint32_t lane4, int k) {
+  return __byte_perm(w, lane4, 0x5504 | (k << 4));
+}
+// 32-bit shared load at a window address plus a compile-time offset.
+template <int OFF>
+__device__ __forceinline__ uint32_t lds_at(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1+%2];\n" : "=r"(v) : "r"(addr), "n"(OFF));
+  return v;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));

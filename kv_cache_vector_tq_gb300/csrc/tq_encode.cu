@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(256, 1) encode_kernel(const EncParams p) {
     while (!(ok = mbar_try_wait(&bar, 0)) && ++spins < kSpinLimitDev) {
     }
     if (!ok) {
-      atomicExch(p.c.status, 1);
+      atomicOr(p.c.status, 1);
       s_abort = 1;
     }
   }

@@ -468,8 +468,16 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
     v.m_scale = (float)pow2_near(4.0 / std::max(mx, 1e-30));
     encoder_fragments(M.data(), d, v.m_scale, frag_m, true);
   }
-  std::vector<float> pi32(dd), s32;
+  std::vector<float> pi32(dd), s32, slices;
   for (size_t i = 0; i < dd; ++i) pi32[i] = (float)c->h_pi[i];
+  if (d == kChunk) {  // Π in column slices for the decode rotation: [32-column slice][j][row][4]
+    slices.resize(dd);
+    for (int cc = 0; cc < d / 32; ++cc)
+      for (int j = 0; j < 8; ++j)
+        for (int r = 0; r < d; ++r)
+          for (int e = 0; e < 4; ++e)
+            slices[(((size_t)cc * 8 + j) * d + r) * 4 + e] = pi32[(size_t)r * d + 32 * cc + 4 * j + e];
+  }
   if (mode == TQ_PROD) {
     s32.resize(dd);
     for (size_t i = 0; i < dd; ++i) s32[i] = (float)c->h_s[i];
@@ -486,7 +494,8 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   size_t o_m = o_pi + al(frag_pi.size() * sizeof(uint2));
   size_t o_p32 = o_m + al(frag_m.size() * sizeof(uint2));
   size_t o_s32 = o_p32 + al(pi32.size() * sizeof(float));
-  size_t o_lut = o_s32 + al(s32.size() * sizeof(float));
+  size_t o_sl = o_s32 + al(s32.size() * sizeof(float));
+  size_t o_lut = o_sl + al(slices.size() * sizeof(float));
   size_t o_st = o_lut + al(lut.size() * sizeof(uint32_t));
   size_t total = o_st + 256;
   void* dmem = nullptr;
@@ -507,6 +516,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   if (e == cudaSuccess) e = up(o_m, frag_m.data(), frag_m.size() * sizeof(uint2));
   if (e == cudaSuccess) e = up(o_p32, pi32.data(), pi32.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_s32, s32.data(), s32.size() * sizeof(float));
+  if (e == cudaSuccess) e = up(o_sl, slices.data(), slices.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_lut, lut.data(), lut.size() * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(base + o_st, 0, 256);
   if (e != cudaSuccess) {
@@ -522,6 +532,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   v.enc_m = mode == TQ_PROD ? (const uint2*)(base + o_m) : nullptr;
   v.pi = (const float*)(base + o_p32);
   v.s_mat = mode == TQ_PROD ? (const float*)(base + o_s32) : nullptr;
+  v.pi_slices = d == kChunk ? (const float4*)(base + o_sl) : nullptr;
   v.lut = (const uint32_t*)(base + o_lut);
   v.status = (int*)(base + o_st);
   *out = reinterpret_cast<tq_ctx*>(c);
@@ -655,6 +666,38 @@ tq_status tq_decode_attention(const tq_ctx* kctx, const tq_ctx* vctx, const void
                        ws_bytes, (cudaStream_t)stream);
 }
 
+tq_status tq_decode_step(const tq_ctx* kctx, const tq_ctx* vctx, const void* d_q, int q_dtype,
+                         const void* d_k_new, const void* d_v_new, int new_dtype, const tq_codes* K,
+                         const tq_codes* V, int B, int Hq, int Hkv, int64_t seq, int64_t cap,
+                         float scale, float* d_out, void* d_ws, size_t ws_bytes,
+                         tq_stream stream) {
+  if (!kctx || !vctx || !K || !V) return TQ_ERR_INVALID_ARG;
+  const DevCtx& kc = reinterpret_cast<const Ctx*>(kctx)->dev;
+  const DevCtx& vc = reinterpret_cast<const Ctx*>(vctx)->dev;
+  if (kc.mode != TQ_MSE || vc.mode != TQ_MSE || kc.d != vc.d) return TQ_ERR_INVALID_ARG;
+  tq_status st = check_codes(kc, K);
+  if (st != TQ_OK) return st;
+  st = check_codes(vc, V);
+  if (st != TQ_OK) return st;
+  if (K->layout != TQ_LAYOUT_TOKEN || V->layout != TQ_LAYOUT_PAIR) return TQ_ERR_INVALID_ARG;
+  if (q_dtype != TQ_F32 && q_dtype != TQ_F16) return TQ_ERR_INVALID_ARG;
+  if (new_dtype != TQ_F32 && new_dtype != TQ_F16) return TQ_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || seq <= 0 || cap < seq || (cap & 1))
+    return TQ_ERR_INVALID_ARG;
+  const int gqa = Hq / Hkv;
+  if (gqa != 1 && gqa != 2 && gqa != 4 && gqa != 8) return TQ_ERR_UNSUPPORTED;
+  if ((int64_t)B * Hkv * cap > K->n || (int64_t)B * Hkv * cap > V->n) return TQ_ERR_INVALID_ARG;
+  if (!d_q || !d_out || !d_k_new || !d_v_new || !al16(d_q) || !al16(d_k_new) || !al16(d_v_new))
+    return TQ_ERR_INVALID_ARG;
+  if (!d_ws || !al16(d_ws) || ws_bytes < decode_ws_bytes(kc.d, B, Hq, Hkv, seq))
+    return TQ_ERR_INVALID_ARG;
+  if (!al16(K->d_norm) || !al16(V->d_norm)) return TQ_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
+  if (kc.d != kChunk) return TQ_ERR_UNSUPPORTED;
+  return launch_step(kc, vc, d_q, q_dtype, d_k_new, d_v_new, new_dtype, K, V, B, Hq, Hkv, seq, cap,
+                     scale, d_out, d_ws, (cudaStream_t)stream);
+}
+
 // Same checks as tq_decode_attention, without the workspace arguments.
 tq_status tq_decode_attention_noalloc(const tq_ctx* kctx, const tq_ctx* vctx, const void* d_q,
                                       int q_dtype, const tq_codes* K, const tq_codes* V, int B,
@@ -674,12 +717,12 @@ tq_status tq_decode_attention_noalloc(const tq_ctx* kctx, const tq_ctx* vctx, co
     return TQ_ERR_INVALID_ARG;
   const int gqa = Hq / Hkv;
   if (gqa != 1 && gqa != 2 && gqa != 4 && gqa != 8) return TQ_ERR_UNSUPPORTED;
+  if (decode_ws_bytes(kc.d, B, Hq, Hkv, seq) > decode_noalloc_limit()) return TQ_ERR_UNSUPPORTED;
   if ((int64_t)B * Hkv * cap > K->n || (int64_t)B * Hkv * cap > V->n) return TQ_ERR_INVALID_ARG;
   if (!d_q || !d_out || !al16(d_q)) return TQ_ERR_INVALID_ARG;
   if (!al16(K->d_norm) || !al16(V->d_norm)) return TQ_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
   if (kc.d != kChunk) return TQ_ERR_UNSUPPORTED;
-  if (decode_ws_bytes(kc.d, B, Hq, Hkv, seq) > decode_noalloc_limit()) return TQ_ERR_UNSUPPORTED;
   return launch_decode_noalloc(kc, vc, d_q, q_dtype, K, V, B, Hq, Hkv, seq, cap, scale, d_out,
                                (cudaStream_t)stream);
 }
@@ -740,6 +783,7 @@ tq_status tq_status_poll(const tq_ctx* ctx, tq_stream stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e == cudaSuccess && h != 0) e = cudaMemsetAsync(v.status, 0, sizeof(int), (cudaStream_t)stream);
   if (e != cudaSuccess) return set_cuda_error(e);
+  if (h & 2) return TQ_ERR_UNSUPPORTED;  // a decode kernel found another shared-memory layout
   return h == 0 ? TQ_OK : TQ_ERR_TIMEOUT;
 }
 

@@ -29,6 +29,7 @@ struct DevCtx {
   const uint2* enc_m;    // encoder B fragments of S·Πᵀ (hi/lo), Prod only
   const float* pi;       // Π, d×d row-major fp32
   const float* s_mat;    // S, d×d row-major fp32, Prod only
+  const float4* pi_slices;  // d = 128: Π[r][32c + 4j .. +3] at (c·8 + j)·128 + r (decode rotation)
   const uint32_t* lut;   // pair table: 2^(2 b_mse) fp16x2 entries (alpha-scaled)
   int* status;           // device status word
 };
@@ -66,6 +67,10 @@ tq_status launch_decode_noalloc(const DevCtx& kc, const DevCtx& vc, const void* 
                                 int64_t seq, int64_t cap, float scale, float* out,
                                 cudaStream_t stream);
 size_t decode_noalloc_limit();
+tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_dtype,
+                      const void* knew, const void* vnew, int new_dtype, const tq_codes* K,
+                      const tq_codes* V, int B, int Hq, int Hkv, int64_t seq, int64_t cap,
+                      float scale, float* out, void* ws, cudaStream_t stream);
 int num_sms();
 
 }  // namespace tq

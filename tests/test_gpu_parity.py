@@ -254,7 +254,7 @@ def run_decode(b_k, b_v, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float1
     q_np = synth.queries(seed, B * Hq, d).reshape(B, Hq, d)
     q = torch.from_numpy(q_np).cuda().to(q_dtype)
     out = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
-    ws = torch.empty(tq.tq_decode_workspace_size(kctx, B, Hq, Hkv, seq) // 4 + 4, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(tq.tq_decode_workspace_size(kctx, B, Hq, Hkv, seq) // 4 + 4, dtype=torch.float32, device="cuda")
     scale = 1.0 / math.sqrt(d)
     tq.tq_decode_attention(kctx, vctx, q, Kc, Vc, B, Hq, Hkv, seq, cap, scale, out, ws)
     torch.cuda.synchronize()
@@ -345,7 +345,7 @@ def test_decode_config4_layer_subset():
     q_np = synth.queries(0, Hq, d).reshape(1, Hq, d)
     q = torch.from_numpy(q_np).cuda().half()
     out = torch.empty((1, Hq, d), dtype=torch.float32, device="cuda")
-    ws = torch.empty(tq.tq_decode_workspace_size(ctx, 1, Hq, Hkv, seq) // 4 + 4, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(tq.tq_decode_workspace_size(ctx, 1, Hq, Hkv, seq) // 4 + 4, dtype=torch.float32, device="cuda")
     tq.tq_decode_attention(ctx, ctx, q, Kc, Vc, 1, Hq, Hkv, seq, cap, 1 / math.sqrt(d), out, ws)
     torch.cuda.synchronize()
     assert ctx.poll() == tq.TQ_OK
@@ -363,3 +363,51 @@ def test_decode_config4_layer_subset():
         got = out.cpu().numpy()[:, kvh * gqa:(kvh + 1) * gqa].astype(np.float64)
         rel = np.linalg.norm(got - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
         assert rel.max() <= 2e-3, rel.max()
+
+
+# ------------------------------------------------------------------ fused decode step (append + attend)
+@pytest.mark.parametrize("b,B,Hq,Hkv,seq", [(4, 1, 32, 8, 16384), (2, 1, 32, 8, 16383),
+                                             (3, 2, 16, 2, 1001), (3, 1, 64, 8, 4096), (4, 1, 8, 8, 17)])
+def test_decode_step_appends_then_attends(b, B, Hq, Hkv, seq):
+    """The step encodes the new token's K and V into position seq-1 (same codes
+    as the oracle's encoder, outside the near-threshold band) and attends over
+    all seq tokens including it."""
+    d = 128
+    cap = (seq + 15) // 16 * 16 + 16
+    ctx, Pi, _ = make_pair(1, d, b)
+    Kh, Vh = synth.kv_layer(1, 0, B, Hkv, seq, d)
+    Kc = tq.CodeSet(ctx, B * Hkv * cap, tq.TQ_LAYOUT_TOKEN)
+    Vc = tq.CodeSet(ctx, B * Hkv * cap, tq.TQ_LAYOUT_PAIR)
+    if seq > 1:
+        tq.tq_encode(ctx, torch.from_numpy(np.ascontiguousarray(Kh[:, :, :seq - 1].reshape(-1, d))).cuda(),
+                     Kc, 0, seq - 1, cap)
+        tq.tq_encode(ctx, torch.from_numpy(np.ascontiguousarray(Vh[:, :, :seq - 1].reshape(-1, d))).cuda(),
+                     Vc, 0, seq - 1, cap)
+    kn = torch.from_numpy(np.ascontiguousarray(Kh[:, :, seq - 1])).cuda()
+    vn = torch.from_numpy(np.ascontiguousarray(Vh[:, :, seq - 1])).cuda()
+    q = torch.from_numpy(synth.queries(1, B * Hq, d).reshape(B, Hq, d)).cuda().half()
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(tq.tq_decode_workspace_size(ctx, B, Hq, Hkv, seq) // 4 + 4, dtype=torch.float32, device="cuda")
+    tq.tq_decode_step(ctx, ctx, q, kn, vn, Kc, Vc, B, Hq, Hkv, seq, cap, 1 / math.sqrt(d), out, ws)
+    torch.cuda.synchronize()
+    cb = oracle_codebook(d, b)
+    # appended codes and norms
+    for arr, cs in ((Kh, Kc), (Vh, Vc)):
+        X = arr[:, :, seq - 1].reshape(-1, d).astype(np.float64)
+        ref, s_ref, v = oq.mse_quantize(X, Pi, cb["centroids"], math.sqrt(d))
+        band = oq.near_threshold(v, cb["centroids"])
+        got = np.stack([tq.tq_unpack_indices(cs, blk * cap + seq - 1, 1)[0] for blk in range(B * Hkv)])
+        assert not ((got.astype(np.int64) != ref) & ~band).any()
+        norms = cs.norm.cpu().numpy().reshape(B * Hkv, cap)[:, seq - 1].astype(np.float64)
+        np.testing.assert_allclose(norms, s_ref, rtol=1e-6)
+    # attention over all tokens, oracle on the GPU's codes
+    kidx = np.concatenate([tq.tq_unpack_indices(Kc, blk * cap, seq) for blk in range(B * Hkv)])
+    vidx = np.concatenate([tq.tq_unpack_indices(Vc, blk * cap, seq) for blk in range(B * Hkv)])
+    knr = Kc.norm.cpu().numpy().reshape(B * Hkv, cap)[:, :seq].reshape(-1).astype(np.float64)
+    vnr = Vc.norm.cpu().numpy().reshape(B * Hkv, cap)[:, :seq].reshape(-1).astype(np.float64)
+    Khat = oatt.dequantize_cache(kidx, knr, Pi, cb["centroids"], math.sqrt(d), B, Hkv, seq)
+    Vhat = oatt.dequantize_cache(vidx, vnr, Pi, cb["centroids"], math.sqrt(d), B, Hkv, seq)
+    ref = oatt.decode_attention(q.float().cpu().numpy().astype(np.float64), Khat, Vhat, 1 / math.sqrt(d))
+    got = out.cpu().numpy().astype(np.float64)
+    rel = np.linalg.norm(got - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
+    assert rel.max() <= 2e-3, rel.max()

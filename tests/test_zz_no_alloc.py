@@ -45,8 +45,7 @@ def test_noalloc_matches_workspace_call_twice():
     tq.tq_encode(ctx, torch.from_numpy(Kh.reshape(-1, d)).cuda(), Kc, 0, seq, cap)
     tq.tq_encode(ctx, torch.from_numpy(Vh.reshape(-1, d)).cuda(), Vc, 0, seq, cap)
     scale = 1.0 / math.sqrt(d)
-    ws = torch.empty(tq.tq_decode_workspace_size(ctx, B, Hq, Hkv, seq) // 4 + 4, dtype=torch.float32,
-                     device="cuda")
+    ws = torch.zeros(tq.tq_decode_workspace_size(ctx, B, Hq, Hkv, seq) // 4 + 4, dtype=torch.float32, device="cuda")
     for call in range(2):
         q = torch.from_numpy(synth.queries(20 + call, B * Hq, d).reshape(B, Hq, d)).cuda().half()
         ref = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
@@ -63,14 +62,15 @@ def test_noalloc_matches_workspace_call_twice():
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    # 64 sequences x 64 KV heads (no GQA) need more than the 2 MiB built in
-    d, b, B, Hq, Hkv, seq, cap = 128, 2, 64, 64, 64, 16, 16
+    # 4096 sequences x 128 KV heads need more counters than the 2 MiB built in;
+    # the size check comes before anything touches the (tiny) code sets
+    d, b, B, Hq, Hkv, seq, cap = 128, 2, 4096, 128, 128, 16, 16
     ctx = _context(12, d, b)
     assert tq.tq_decode_workspace_size(ctx, B, Hq, Hkv, seq) > (2 << 20)
-    Kc = tq.CodeSet(ctx, B * Hkv * cap, tq.TQ_LAYOUT_TOKEN)
-    Vc = tq.CodeSet(ctx, B * Hkv * cap, tq.TQ_LAYOUT_PAIR)
+    Kc = tq.CodeSet(ctx, 16, tq.TQ_LAYOUT_TOKEN)
+    Vc = tq.CodeSet(ctx, 16, tq.TQ_LAYOUT_PAIR)
     q = torch.zeros((B, Hq, d), dtype=torch.float16, device="cuda")
-    out = torch.zeros((B, Hq, d), dtype=torch.float32, device="cuda")
+    out = torch.zeros((1, 1, d), dtype=torch.float32, device="cuda")
     with pytest.raises(tq.TqError) as err:
         tq.tq_decode_attention_noalloc(ctx, ctx, q, Kc, Vc, B, Hq, Hkv, seq, cap, 1.0, out)
     assert err.value.status == tq.TQ_ERR_UNSUPPORTED
