@@ -42,7 +42,7 @@ namespace tq {
 constexpr int kTileTok = 16;
 constexpr int kStages = 3;            // tiles in flight per warp
 constexpr int kFieldBytes = 32 * 16;  // one 16-byte slot per lane
-constexpr int kStageBytes = 5 * kFieldBytes;
+constexpr int kStageBytes = 4 * kFieldBytes + 128;  // + the tile's 16 K and 16 V norms
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.f;  // rescale only when the running max grows by > 2^8
 constexpr int kPart = 132;    // floats per head in a published partial: m, l, 2 pad, acc[128]
@@ -167,12 +167,20 @@ __host__ __device__ inline int split_begin(int u, int U, int tiles, bool append)
 }
 
 // Shared-memory layout (bytes), computed identically on host and device.
-// Each warp has kStages tile stages of five 512-byte fields (one 16-byte slot
-// per lane: K codes of tokens g and g+8, V pair blocks t and t+4, norms),
+// Each warp has kStages tile stages of four 512-byte fields (one 16-byte slot
+// per lane: K codes of tokens g and g+8, V pair blocks t and t+4) and the
+// tile's 16 K and 16 V norms,
 // which after the tile loop hold its softmax state.
 struct StepSmem {
   int vlut, stage, wreg, mw, qs, qhat, newin, ynew, newcodes, uni, opart, qfs, cpart, outp, flag, bytes;
 };
+
+// Offset in a warp region of its rows of Π_V: after its softmax state
+// ((NT·512 + 16) floats) and its partial outputs (G·128 floats).
+__host__ __device__ inline int pi_off(int G) {
+  const int NT = (2 * G + 7) / 8, a = (NT * 512 + 16) * 4, b = G * 128 * 4;
+  return ((a > b ? a : b) + 127) / 128 * 128;
+}
 
 __host__ __device__ inline StepSmem step_smem(int bk, int bv, int G, int W, bool same_lut) {
   StepSmem m;
@@ -184,7 +192,8 @@ __host__ __device__ inline StepSmem step_smem(int bk, int bv, int G, int W, bool
   else if (!same_lut)
     o += (1 << (2 * bv)) * 32 * 4;
   o = (o + 127) / 128 * 128;
-  const int st = kStages * kStageBytes, cw = (NT * 512 + 16) * 4;
+  // after the loop: its state (then its partial outputs), and its rows of Π_V at pi_off
+  const int st = kStages * kStageBytes, cw = pi_off(G) + (128 / W) * 512;
   m.wreg = ((st > cw ? st : cw) + 127) / 128 * 128;
   m.stage = o;  // after the tile loop: the warps' states, then partial outputs [W][G][128]
   o += W * m.wreg;
@@ -358,11 +367,8 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
       // V pair blocks t and t+4 of the tile; this lane's coordinates 16g..16g+15
       copy_words<BV>(st + 2 * kFieldBytes + lane * 16, p.vcodes + (vb + 2 * t) * WV + g * BV);
       copy_words<BV>(st + 3 * kFieldBytes + lane * 16, p.vcodes + (vb + 2 * t + 8) * WV + g * BV);
-      float* ns = reinterpret_cast<float*>(st + 4 * kFieldBytes + lane * 16);
-      cp_async4(ns + 0, p.knorm + vb + g);
-      cp_async4(ns + 1, p.knorm + vb + g + 8);
-      cp_async4(ns + 2, p.vnorm + vb + g);
-      cp_async4(ns + 3, p.vnorm + vb + g + 8);
+      if (lane < 8)  // lanes 0-3: the 16 K norms, lanes 4-7: the 16 V norms
+        cp_async16(st + 4 * kFieldBytes + lane * 16, (lane < 4 ? p.knorm : p.vnorm) + vb + 4 * (lane & 3));
     }
     cp_async_commit();  // always, so that the group count stays uniform
   };
@@ -544,7 +550,8 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     read_words<BK>(k1, st + 1 * kFieldBytes + lane * 16);
     read_words<BV>(v0w, st + 2 * kFieldBytes + lane * 16);
     read_words<BV>(v1w, st + 3 * kFieldBytes + lane * 16);
-    float4 nrm = *reinterpret_cast<const float4*>(st + 4 * kFieldBytes + lane * 16);
+    const float* ns = reinterpret_cast<const float*>(st + 4 * kFieldBytes);
+    float4 nrm = make_float4(ns[g], ns[g + 8], ns[16 + g], ns[16 + g + 8]);
     if (owner && tile == new_tile) {  // the appended token: use the codes just made
       if (new_row == g) {
 #pragma unroll
@@ -676,6 +683,14 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     }
   }
   cp_async_wait_all();
+  // this warp's rows of Π_V for the output rotation, copied into its own region
+  // while the warps merge (asynchronous: no registers held, nothing waits on them yet)
+  {
+    float* prow = reinterpret_cast<float*>(my_stage + pi_off(G));
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) cp_async16(prow + r * 128 + 4 * lane, p.vpi + (warp * RPW + r) * 128 + 4 * lane);
+    cp_async_commit();
+  }
 
   // ---- 4. merge the warps and rotate back.  Each warp leaves its state in its
   //         own region in fragment order: acc value (nt, mt, e) of lane l at
@@ -700,11 +715,6 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
       }
     }
   }
-  // this warp's rows of Π_V for the output rotation, requested before the
-  // merge waits for the slower warps (and after the stores above)
-  float4 pvr[RPW];
-#pragma unroll
-  for (int r = 0; r < RPW; ++r) pvr[r] = __ldg(reinterpret_cast<const float4*>(p.vpi + (warp * RPW + r) * 128) + lane);
   __syncthreads();
   // 4a. factors f_w = 2^(m_w - M) of the warps, M and Σ_w f_w·l_w per head
   float* fw = qhat;  // [W][G]; the rotated queries are in the fragments now
@@ -736,8 +746,10 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
   }
   __syncthreads();
   // 4b. Πᵀ·acc: warp w sums its RPW rows k of Π_V, lane its 4 output coordinates
-  float* red = reinterpret_cast<float*>(stage);  // [W][G][128] over the warp states
-  {
+  {  // partial outputs [G][128] of warp w at the start of its region (its state is merged)
+    cp_async_wait_all();
+    __syncwarp();
+    const float4* prow = reinterpret_cast<const float4*>(my_stage + pi_off(G));
     float4 op[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) op[h] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -745,23 +757,24 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     for (int r = 0; r < RPW; ++r) {
       const int k = warp * RPW + r;  // coordinate 16gk + 2mtk + ek
       const int base = (((k >> 1) & 7) * 2 + (k & 1)) * 32 + 4 * (k >> 4);
+      const float4 pv4 = prow[r * 32 + lane];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float a = cpart[(h >> 2) * 512 + base + (h & 3)];
-        op[h].x = fmaf(pvr[r].x, a, op[h].x);
-        op[h].y = fmaf(pvr[r].y, a, op[h].y);
-        op[h].z = fmaf(pvr[r].z, a, op[h].z);
-        op[h].w = fmaf(pvr[r].w, a, op[h].w);
+        op[h].x = fmaf(pv4.x, a, op[h].x);
+        op[h].y = fmaf(pv4.y, a, op[h].y);
+        op[h].z = fmaf(pv4.z, a, op[h].z);
+        op[h].w = fmaf(pv4.w, a, op[h].w);
       }
     }
 #pragma unroll
-    for (int h = 0; h < G; ++h) reinterpret_cast<float4*>(red + (warp * G + h) * 128)[lane] = op[h];
+    for (int h = 0; h < G; ++h) reinterpret_cast<float4*>(my_stage + h * 512)[lane] = op[h];
   }
   __syncthreads();
   for (int e = tid; e < G * 128; e += NTH) {
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < W; ++w) s += red[w * G * 128 + e];
+    for (int w = 0; w < W; ++w) s += reinterpret_cast<const float*>(stage + w * L.wreg)[e];
     outp[e] = s;
   }
   __syncthreads();
