@@ -306,7 +306,8 @@ def run_tq(args, world, rank, local):
             "bits": bits, "replicas": R, "seq": SEQ, "heads_q": HQ, "heads_kv": HKV, "head_dim": D,
             "l2": f"inputs larger than L2: {R} distinct caches x {cache_bytes / 1e6:.1f} MB per step",
             "bytes_per_decode": step_bytes, "parallelism": f"replicas x{world}",
-            "tokens_per_s": round(world * args.steps * R / (ms * 1e-3), 1),
+            "decode_steps_per_s": round(world * args.steps * R / (ms * 1e-3), 1),
+            "tokens_scored_per_s": round(world * args.steps * R * SEQ * HQ / (ms * 1e-3), 1),
         },
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
