@@ -468,7 +468,11 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
     v.m_scale = (float)pow2_near(4.0 / std::max(mx, 1e-30));
     encoder_fragments(M.data(), d, v.m_scale, frag_m, true);
   }
-  std::vector<float> pi32(dd), s32, slices;
+  std::vector<float> pi32(dd), s32, slices, signs32;
+  if (rot_kind == TQ_ROT_HADAMARD) {
+    signs32.resize(d);
+    for (int i = 0; i < d; ++i) signs32[i] = (float)h_rot[i];
+  }
   for (size_t i = 0; i < dd; ++i) pi32[i] = (float)c->h_pi[i];
   if (d == kChunk) {  // Π in column slices for the decode rotation: [32-column slice][j][row][4]
     slices.resize(dd);
@@ -495,7 +499,8 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   size_t o_p32 = o_m + al(frag_m.size() * sizeof(uint2));
   size_t o_s32 = o_p32 + al(pi32.size() * sizeof(float));
   size_t o_sl = o_s32 + al(s32.size() * sizeof(float));
-  size_t o_lut = o_sl + al(slices.size() * sizeof(float));
+  size_t o_sg = o_sl + al(slices.size() * sizeof(float));
+  size_t o_lut = o_sg + al(signs32.size() * sizeof(float));
   size_t o_st = o_lut + al(lut.size() * sizeof(uint32_t));
   size_t total = o_st + 256;
   void* dmem = nullptr;
@@ -517,6 +522,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   if (e == cudaSuccess) e = up(o_p32, pi32.data(), pi32.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_s32, s32.data(), s32.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_sl, slices.data(), slices.size() * sizeof(float));
+  if (e == cudaSuccess) e = up(o_sg, signs32.data(), signs32.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_lut, lut.data(), lut.size() * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(base + o_st, 0, 256);
   if (e != cudaSuccess) {
@@ -533,6 +539,15 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   v.pi = (const float*)(base + o_p32);
   v.s_mat = mode == TQ_PROD ? (const float*)(base + o_s32) : nullptr;
   v.pi_slices = d == kChunk ? (const float4*)(base + o_sl) : nullptr;
+  v.signs = rot_kind == TQ_ROT_HADAMARD ? (const float*)(base + o_sg) : nullptr;
+  v.had_m = v.had_p = 0;
+  if (rot_kind == TQ_ROT_HADAMARD) {
+    int hm = 0;
+    bool hp = false;
+    hadamard_order(d, &hm, &hp);
+    v.had_m = hm;
+    v.had_p = hp ? 12 : 1;
+  }
   v.lut = (const uint32_t*)(base + o_lut);
   v.status = (int*)(base + o_st);
   *out = reinterpret_cast<tq_ctx*>(c);
@@ -598,13 +613,16 @@ tq_status tq_encode(const tq_ctx* ctx, const void* d_x, int x_dtype, int64_t N,
   if (st != TQ_OK) return st;
   if (N == 0) return TQ_OK;
   if (!d_x || !al16(d_x)) return TQ_ERR_INVALID_ARG;
-  if (v.d > kChunk) return TQ_ERR_UNSUPPORTED;
+  const bool wht = wht_supported(v) && out->layout == TQ_LAYOUT_TOKEN;
+  if (v.d > kChunk && !wht) return TQ_ERR_UNSUPPORTED;
   // every destination index must lie inside the code set
   int64_t groups = (N + group_rows - 1) / group_rows;
   int64_t last_in_group = std::min<int64_t>(group_rows, N) - 1;
   int64_t max_dst = (groups - 1) * group_stride + offset + last_in_group;
   if (max_dst >= out->n) return TQ_ERR_INVALID_ARG;
   if (groups > 1 && group_stride < group_rows) return TQ_ERR_INVALID_ARG;  // no overlap
+  if (wht)
+    return launch_encode_wht(v, d_x, x_dtype, N, out, offset, group_rows, group_stride, (cudaStream_t)stream);
   return launch_encode(v, d_x, x_dtype, N, out, offset, group_rows, group_stride,
                        (cudaStream_t)stream);
 }

@@ -30,6 +30,8 @@ struct DevCtx {
   const float* pi;       // Π, d×d row-major fp32
   const float* s_mat;    // S, d×d row-major fp32, Prod only
   const float4* pi_slices;  // d = 128: Π[r][32c + 4j .. +3] at (c·8 + j)·128 + r (decode rotation)
+  const float* signs;    // Hadamard rotation: σ, d entries of ±1 (else null)
+  int had_m, had_p;      // Hadamard rotation: H = H12 ⊗ H_m (had_p = 12) or H_m (had_p = 1)
   const uint32_t* lut;   // pair table: 2^(2 b_mse) fp16x2 entries (alpha-scaled)
   int* status;           // device status word
 };
@@ -71,6 +73,9 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
                       const void* knew, const void* vnew, int new_dtype, const tq_codes* K,
                       const tq_codes* V, int B, int Hq, int Hkv, int64_t seq, int64_t cap,
                       float scale, float* out, void* ws, cudaStream_t stream);
+bool wht_supported(const DevCtx& c);
+tq_status launch_encode_wht(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
+                            int64_t offset, int64_t group_rows, int64_t group_stride, cudaStream_t stream);
 int num_sms();
 
 }  // namespace tq

@@ -1,0 +1,108 @@
+"""GPU parity of the encoders for the bulk-indexing workload (b = 4, d = 1536
+and 3072, fp32 rows N(0, 1) with a seeded 1 % of the rows scaled by 50) and of
+the randomized-Hadamard fast transform at every supported order, against the
+fp64 oracle.  Same bars as the other encode parity tests: indices exact
+outside the 1e-6 band around the thresholds (band fraction <= 1e-5), norms
+within 1e-6 relative.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import kv_cache_vector_tq_gb300 as tq  # noqa: E402
+from kv_cache_vector_tq_gb300 import synth  # noqa: E402
+from oracle import codebook as ocb  # noqa: E402
+from oracle import quantizer as oq  # noqa: E402
+from oracle import rotation as orot  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+BAND_FRAC_MAX = 1e-5
+_cb = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tq.lib()
+
+
+def codebook(d, b):
+    if (d, b) not in _cb:
+        _cb[(d, b)] = ocb.build_codebook(d, b)
+    return _cb[(d, b)]
+
+
+def hadamard_pair(seed, d, b):
+    sg = synth.hadamard_signs(seed, d)
+    return tq.Context(d, b, tq.TQ_MSE, tq.TQ_ROT_HADAMARD, sg), orot.hadamard_rotation(d, sg)
+
+
+def encode(ctx, X, dtype=torch.float32):
+    x = torch.from_numpy(np.ascontiguousarray(X)).to(dtype).cuda()
+    cs = tq.CodeSet(ctx, X.shape[0], tq.TQ_LAYOUT_TOKEN)
+    tq.tq_encode(ctx, x, cs)
+    torch.cuda.synchronize()
+    assert ctx.poll() == tq.TQ_OK
+    return cs
+
+
+def check(cs, Pi, X, b, rows=None):
+    """Oracle on the (sampled) rows; rows = None means all."""
+    d = X.shape[1]
+    rows = np.arange(X.shape[0]) if rows is None else np.asarray(rows)
+    Xs = X[rows].astype(np.float64)
+    cb = codebook(d, b)
+    idx_ref, s_ref, v = oq.mse_quantize(Xs, Pi, cb["centroids"], math.sqrt(d))
+    band = oq.near_threshold(v, cb["centroids"])
+    band[s_ref == 0.0] = False
+    idx = np.stack([tq.tq_unpack_indices(cs, int(r), 1)[0] for r in rows]) if len(rows) < X.shape[0] \
+        else tq.tq_unpack_indices(cs, 0, X.shape[0])
+    mism = (idx.astype(np.int64) != idx_ref) & ~band
+    assert not mism.any(), f"{mism.sum()} mismatches outside the band (rows {rows[np.nonzero(mism.any(1))[0][:8]]})"
+    # the band is a rare event: on small samples allow a Poisson fluctuation
+    # above the 1e-5 cap (mean + 4 sigma + 2)
+    lam = BAND_FRAC_MAX * band.size
+    assert band.mean() <= BAND_FRAC_MAX or band.sum() <= lam + 4 * math.sqrt(lam) + 2, band.mean()
+    norm = cs.norm.cpu().numpy().astype(np.float64)[rows]
+    np.testing.assert_allclose(norm, s_ref, rtol=1e-6, atol=0)
+    return idx_ref, band
+
+
+@pytest.mark.parametrize("d", [32, 64, 128, 256, 384, 768, 1536, 3072])
+@pytest.mark.parametrize("b", [1, 2, 3, 4])
+def test_hadamard_fast_transform(d, b):
+    """Orders 2^k and 12·2^k with 32 <= 2^k <= 256 run the fast transform."""
+    n = 257 if d <= 384 else 96
+    ctx, Pi = hadamard_pair(7, d, b)
+    X = synth.bulk_rows(7, n, d)
+    X[n // 3] = 0.0  # zero vector: s = 0, codes 0
+    cs = encode(ctx, X)
+    idx_ref, band = check(cs, Pi, X, b)
+    # raw words equal the canonical packing wherever no coordinate is in the band
+    words = cs.codes.view(torch.int32).cpu().numpy().view(np.uint32).reshape(n, -1)
+    ok = ~band.any(axis=1)
+    np.testing.assert_array_equal(words[ok], oq.pack_codes(idx_ref[ok], b))
+
+
+def test_hadamard_fast_transform_fp16_rows():
+    ctx, Pi = hadamard_pair(8, 128, 3)
+    X = synth.gaussian_rows(8, 500, 128, outlier_cols=4, outlier_scale=10.0, dtype=np.float16)
+    cs = encode(ctx, X, torch.float16)
+    check(cs, Pi, X.astype(np.float32), 3)
+
+
+@pytest.mark.parametrize("d", [1536, 3072])
+def test_hadamard_bulk_indexing_full_size_sampled(d):
+    """N = 100K rows of the bulk-indexing workload, 512 rows checked."""
+    N = 100_000
+    ctx, Pi = hadamard_pair(0, d, 4)
+    X = synth.bulk_rows(0, N, d)
+    cs = encode(ctx, X)
+    rows = np.random.default_rng(1).choice(N, size=512, replace=False)
+    check(cs, Pi, X, 4, rows)
