@@ -614,7 +614,8 @@ tq_status tq_encode(const tq_ctx* ctx, const void* d_x, int x_dtype, int64_t N,
   if (N == 0) return TQ_OK;
   if (!d_x || !al16(d_x)) return TQ_ERR_INVALID_ARG;
   const bool wht = wht_supported(v) && out->layout == TQ_LAYOUT_TOKEN;
-  if (v.d > kChunk && !wht) return TQ_ERR_UNSUPPORTED;
+  const bool wide = !wht && v.d > kChunk;
+  if (wide && (!wide_supported(v) || out->layout != TQ_LAYOUT_TOKEN)) return TQ_ERR_UNSUPPORTED;
   // every destination index must lie inside the code set
   int64_t groups = (N + group_rows - 1) / group_rows;
   int64_t last_in_group = std::min<int64_t>(group_rows, N) - 1;
@@ -623,6 +624,8 @@ tq_status tq_encode(const tq_ctx* ctx, const void* d_x, int x_dtype, int64_t N,
   if (groups > 1 && group_stride < group_rows) return TQ_ERR_INVALID_ARG;  // no overlap
   if (wht)
     return launch_encode_wht(v, d_x, x_dtype, N, out, offset, group_rows, group_stride, (cudaStream_t)stream);
+  if (wide)
+    return launch_encode_wide(v, d_x, x_dtype, N, out, offset, group_rows, group_stride, (cudaStream_t)stream);
   return launch_encode(v, d_x, x_dtype, N, out, offset, group_rows, group_stride,
                        (cudaStream_t)stream);
 }

@@ -74,6 +74,9 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
                       const tq_codes* V, int B, int Hq, int Hkv, int64_t seq, int64_t cap,
                       float scale, float* out, void* ws, cudaStream_t stream);
 bool wht_supported(const DevCtx& c);
+bool wide_supported(const DevCtx& c);
+tq_status launch_encode_wide(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
+                             int64_t offset, int64_t group_rows, int64_t group_stride, cudaStream_t stream);
 tq_status launch_encode_wht(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
                             int64_t offset, int64_t group_rows, int64_t group_stride, cudaStream_t stream);
 int num_sms();

@@ -106,3 +106,59 @@ def test_hadamard_bulk_indexing_full_size_sampled(d):
     cs = encode(ctx, X)
     rows = np.random.default_rng(1).choice(N, size=512, replace=False)
     check(cs, Pi, X, 4, rows)
+
+
+_haar = {}
+
+
+def haar_pair(seed, d, b):
+    if (seed, d) not in _haar:
+        G = synth.gaussian_matrix(seed, d)
+        _haar[(seed, d)] = (tq.tq_rotation_haar(G), orot.haar_rotation(G))
+    pi_lib, pi_ref = _haar[(seed, d)]
+    return tq.Context(d, b, tq.TQ_MSE, tq.TQ_ROT_DENSE, pi_lib), pi_ref
+
+
+@pytest.mark.parametrize("d", [256, 1536, 3072])
+@pytest.mark.parametrize("b", [2, 4])
+def test_dense_wide_encode(d, b):
+    """Dense Haar rotation for d > 128 (tiled tensor-core GEMM, float-float
+    accumulation across 128-wide chunks), ragged row count and a zero row."""
+    n = 300
+    ctx, Pi = haar_pair(11, d, b)
+    X = synth.bulk_rows(11, n, d)
+    X[7] = 0.0
+    cs = encode(ctx, X)
+    idx_ref, band = check(cs, Pi, X, b)
+    words = cs.codes.view(torch.int32).cpu().numpy().view(np.uint32).reshape(n, -1)
+    ok = ~band.any(axis=1)
+    np.testing.assert_array_equal(words[ok], oq.pack_codes(idx_ref[ok], b))
+
+
+def test_dense_wide_encode_fp16_rows():
+    ctx, Pi = haar_pair(12, 1536, 4)
+    X = synth.gaussian_rows(12, 200, 1536, outlier_cols=4, outlier_scale=10.0, dtype=np.float16)
+    cs = encode(ctx, X, torch.float16)
+    check(cs, Pi, X.astype(np.float32), 4)
+
+
+@pytest.mark.parametrize("d", [1536, 3072])
+def test_dense_bulk_indexing_full_size_sampled(d):
+    """N = 100K rows of the bulk-indexing workload with the dense Haar
+    rotation, 512 rows checked."""
+    N = 100_000
+    ctx, Pi = haar_pair(0, d, 4)
+    X = synth.bulk_rows(0, N, d)
+    cs = encode(ctx, X)
+    rows = np.random.default_rng(2).choice(N, size=512, replace=False)
+    check(cs, Pi, X, 4, rows)
+
+
+def test_wide_encode_rejects_unsupported():
+    """d > 128 with the dense rotation: b in {2, 4}, MSE, TOKEN layout only."""
+    ctx, _ = haar_pair(13, 256, 3)
+    x = torch.zeros((4, 256), dtype=torch.float32, device="cuda")
+    cs = tq.CodeSet(ctx, 4, tq.TQ_LAYOUT_TOKEN)
+    with pytest.raises(tq.TqError) as err:
+        tq.tq_encode(ctx, x, cs)
+    assert err.value.status == tq.TQ_ERR_UNSUPPORTED
