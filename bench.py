@@ -45,6 +45,12 @@ def parse_args():
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--bits", type=int, default=4, choices=[1, 2, 3, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="decode", choices=["decode", "encode", "scores", "longctx", "keys"],
+                    help="decode (the headline) or a secondary workload (see bench_workloads.py)")
+    ap.add_argument("--dim", type=int, default=3072, help="encode: vector dimension")
+    ap.add_argument("--rows", type=int, default=100_000, help="encode: number of vectors")
+    ap.add_argument("--rotation", default="dense", choices=["dense", "hadamard"], help="encode: rotation")
+    ap.add_argument("--layers", type=int, default=80, help="longctx: layers run in sequence")
     return ap.parse_args()
 
 
@@ -371,6 +377,50 @@ def cpu_baseline(tq, ctx, reps0, bits, cap, q):
             "sample": f"{runs} full decode steps (8 KV heads x 16384 tokens, fp64 explicit dequantization)"}
 
 
+# ---------------------------------------------------------------- oracle timing, secondary workloads
+def cpu_encode_baseline(d, bits, rot, rotm):
+    """The oracle encoder timed on the host cores on a bounded sample of rows."""
+    import numpy as np
+
+    from kv_cache_vector_tq_gb300 import synth
+    from oracle import codebook as ocb
+    from oracle import quantizer as oq
+    from oracle import rotation as orot
+    Pi = orot.hadamard_rotation(d, rotm) if rot == "hadamard" else np.asarray(rotm)
+    cb = ocb.build_codebook(d, bits)
+    n = 256 if d >= 3072 else 512
+    X = synth.bulk_rows(0, n, d).astype(np.float64)
+    total, done = 0.0, 0
+    while total < 10.0 and done < 64 * n:
+        t0 = time.perf_counter()
+        oq.mse_quantize(X, Pi, cb["centroids"], math.sqrt(d))
+        total += time.perf_counter() - t0
+        done += n
+    return {"value": round(done / total / 1e6, 6), "unit": "Mvec/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "sample": f"{done} rows of d={d} (fp64 dense rotation, exhaustive nearest centroid)"}
+
+
+def cpu_scores_baseline(tq, cs, q, G, S):
+    """Oracle Prod scores (explicit dequantization) on a 64 x 65536-key sample."""
+    import numpy as np
+
+    from oracle import attention as oatt
+    from oracle import codebook as ocb
+    from oracle import rotation as orot
+    n = 65536
+    ids, bits = tq.tq_unpack_indices(cs, 0, n, with_bits=True)
+    Pi = orot.haar_rotation(G)
+    cb = ocb.build_codebook(128, 2)
+    s = cs.norm[:n].cpu().numpy().astype(np.float64)
+    g = cs.rnorm[:n].cpu().numpy().astype(np.float64)
+    Q = q.cpu().numpy().astype(np.float64)
+    t0 = time.perf_counter()
+    oatt.prod_scores(Q, ids.astype(np.int64), s, bits, g, Pi, S, cb["centroids"], math.sqrt(128))
+    t = time.perf_counter() - t0
+    return {"value": round(Q.shape[0] * n / t, 1), "unit": "tokens scored/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "sample": f"64 queries x {n} keys (fp64 explicit dequantization)"}
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, world, rank):
     """The oracle as it stands, timed on the host cores, same metric/config."""
@@ -431,6 +481,12 @@ def main():
     world, rank, local = dist_init(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, world, rank)
+    elif args.workload != "decode":
+        import bench_workloads as bw
+        run = {"encode": bw.run_encode, "scores": bw.run_scores, "longctx": bw.run_longctx,
+               "keys": bw.run_keys}[args.workload]
+        line = run(args, world, rank, local, ROOT, Clocks,
+                   {"encode": cpu_encode_baseline, "scores": cpu_scores_baseline})
     else:
         line = run_tq(args, world, rank, local)
     if line is not None:

@@ -1,0 +1,329 @@
+"""Secondary workloads of bench.py (--workload encode | scores | longctx | keys).
+
+Each prints one JSON line in the same shape as the decode headline:
+  encode   bulk indexing: b = 4, d = --dim (1536 / 3072), N = --rows fp32 rows
+           N(0, 1) with a seeded 1 % of the rows x50, dense Haar or randomized
+           Hadamard rotation (--rotation); metric encode Mvec/s.
+  scores   TurboQuant_Prod b = 3 (2-bit MSE + 1-bit QJL), d = 128, 1M unit-norm
+           keys, 64 queries; metric tokens (query-key pairs) scored/s.
+  longctx  decode at a 70B-like shape: 64 q / 8 kv heads, head_dim 128,
+           seq 131072, batch 1, b = 3 K/V, --layers layers run in sequence
+           (80 by default); per layer the cache is prefilled by tq_encode
+           (timed separately), then one decode step (append + attend) runs
+           over all layers; metric decode-attn HBM GB/s.
+  keys     d = 128, b = 3: encode 4096 fp32 keys (channels 0-3 x20), then score
+           one query against them; metric encode Mvec/s (scores in config).
+Inputs of the large workloads are generated on the device (torch's seeded
+generator) with the same distributions as the seeded host recipes the parity
+tests use; the parity tests cover the same kernels on host-generated rows.
+The host baselines (the oracle timed on the host cores) are passed in by
+bench.py as `cpu`.
+"""
+
+import math
+import os
+import time
+
+
+def _peaks(root):
+    import json
+    try:
+        with open(os.path.join(root, "MEASURED_PEAKS.json")) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _timed(fn, steps, warmup, stream, clocks_cls, local, flush=None):
+    """W warm-up calls, then K timed calls bracketed by events on `stream`.
+    With `flush`, L2 is flushed between calls and only the calls are timed."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+    torch.cuda.synchronize()
+    clocks = clocks_cls(local)
+    clocks.start()
+    time.sleep(0.2)
+    total = 0.0
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        total = e0.elapsed_time(e1)
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                flush()
+                a.record(stream)
+                fn()
+                b.record(stream)
+        torch.cuda.synchronize()
+        total = sum(a.elapsed_time(b) for a, b in evs)
+    clk = clocks.stop()
+    return total, clk
+
+
+def _line(args, world, metric, value, unit, ms_per_step, dtype, data, config, roofline, e2e, launches, clk):
+    return {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": data, "config": config,
+        "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+    }
+
+
+# ---------------------------------------------------------------- bulk encode
+def run_encode(args, world, rank, local, root, clocks_cls, cpu):
+    import numpy as np
+    import torch
+
+    import kv_cache_vector_tq_gb300 as tq
+    from kv_cache_vector_tq_gb300 import synth
+    torch.cuda.set_device(local)
+    d, N, bits, rot = args.dim, args.rows, 4, args.rotation
+    if rot == "hadamard":
+        rotm = synth.hadamard_signs(0, d)
+        ctx = tq.Context(d, bits, tq.TQ_MSE, tq.TQ_ROT_HADAMARD, rotm)
+    else:
+        rotm = tq.tq_rotation_haar(synth.gaussian_matrix(0, d))
+        ctx = tq.Context(d, bits, tq.TQ_MSE, tq.TQ_ROT_DENSE, rotm)
+    gen = torch.Generator(device="cuda").manual_seed(1234 + rank)
+    x = torch.randn((N, d), generator=gen, device="cuda", dtype=torch.float32)
+    k = max(1, N // 100)
+    rows = torch.randperm(N, generator=gen, device="cuda")[:k]
+    x[rows] *= 50.0
+    cs = tq.CodeSet(ctx, N, tq.TQ_LAYOUT_TOKEN)
+    stream = torch.cuda.Stream()
+    total_ms, clk = _timed(lambda: tq.tq_encode(ctx, x, cs, stream=stream), args.steps, args.warmup, stream,
+                           clocks_cls, local)
+    assert ctx.poll() == tq.TQ_OK
+    sec = total_ms * 1e-3
+    mvec = world * args.steps * N / sec / 1e6
+    hbm, bf16, kind = _peaks(root)
+    bytes_per_vec = 4 * d + d * bits // 8 + 4
+    if rot == "hadamard":
+        ach = args.steps * N * bytes_per_vec / sec / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                "traffic": None, "kernel": "encode_wht_kernel", "peak_kind": kind,
+                "bytes_per_vector": bytes_per_vec}
+    else:
+        ach = args.steps * 2.0 * N * d * d / sec / 1e12  # useful flops of Y = X·Πᵀ
+        peak = bf16 / 3.0  # fp32-accurate products: three fp16 tensor passes (hi·hi, lo·hi, hi·lo)
+        roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "traffic": None, "kernel": "encode_wide_kernel",
+                "peak_kind": f"{kind} bf16 dense / 3 split passes (fp16 hi/lo, same tensor rate as bf16)",
+                "passes": 3, "flops_per_vector": 2 * d * d}
+    # end to end: rows from pinned host memory, codes and norms back, per call
+    e2e = None
+    if N * d * 4 <= (2 << 30):
+        xh = x.cpu().pin_memory()
+        ch = torch.empty_like(cs.codes, device="cpu").pin_memory()
+        nh = torch.empty_like(cs.norm, device="cpu").pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, min(args.steps, 10))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                x.copy_(xh, non_blocking=True)
+                tq.tq_encode(ctx, x, cs, stream=stream)
+                ch.copy_(cs.codes, non_blocking=True)
+                nh.copy_(cs.norm, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e2e = {"value": round(world * reps * N / (e0.elapsed_time(e1) * 1e-3) / 1e6, 3), "unit": "Mvec/s",
+               "h2d_bytes_per_step": N * d * 4, "d2h_bytes_per_step": cs.codes.numel() * 4 + cs.norm.numel() * 4}
+    line = _line(args, world, "encode Mvec/s", round(mvec, 3), "Mvec/s", total_ms / args.steps,
+                 "f32 in, u4 codes, f16 hi/lo tensor products, f32 accumulate",
+                 "synthetic (device-generated N(0,1) fp32 rows, a seeded 1% x50)",
+                 {"workload": f"bulk indexing encode, TurboQuant_MSE b=4, d={d}, N={N}, {rot} rotation",
+                  "d": d, "rows": N, "bits": bits, "rotation": rot,
+                  "l2": f"inputs larger than L2: {N * d * 4 / 1e9:.2f} GB of rows per step"},
+                 roof, e2e, args.steps, clk)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu["encode"](d, bits, rot, rotm)
+    return line if rank == 0 else None
+
+
+# ---------------------------------------------------------------- Prod scores
+def run_scores(args, world, rank, local, root, clocks_cls, cpu):
+    import numpy as np
+    import torch
+
+    import kv_cache_vector_tq_gb300 as tq
+    from kv_cache_vector_tq_gb300 import synth
+    torch.cuda.set_device(local)
+    d, N, M = 128, 1 << 20, 64
+    G, S = synth.gaussian_matrix(0, d), synth.qjl_matrix(0, d)
+    ctx = tq.Context(d, 3, tq.TQ_PROD, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(G), S)
+    gen = torch.Generator(device="cuda").manual_seed(99 + rank)
+    keys = torch.randn((N, d), generator=gen, device="cuda")
+    keys /= keys.norm(dim=1, keepdim=True)
+    cs = tq.CodeSet(ctx, N, tq.TQ_LAYOUT_TOKEN)
+    tq.tq_encode(ctx, keys, cs)
+    torch.cuda.synchronize()
+    del keys
+    q = torch.from_numpy(synth.queries(0, M, d)).cuda()
+    out = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(tq.tq_scores_workspace_size(ctx, M) // 4, 4), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    total_ms, clk = _timed(lambda: tq.tq_scores(ctx, q, cs, out, ws, stream=stream), args.steps, args.warmup,
+                           stream, clocks_cls, local)
+    assert ctx.poll() == tq.TQ_OK
+    sec = total_ms * 1e-3
+    pairs = world * args.steps * M * N / sec
+    hbm, _, kind = _peaks(root)
+    bytes_call = N * (32 + 16 + 4 + 4) + M * N * 4
+    ach = args.steps * bytes_call / sec / 1e9
+    roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+            "traffic": None, "kernel": "scores_kernel (Prod)", "peak_kind": kind, "bytes_per_call": bytes_call}
+    qh = q.cpu().pin_memory()
+    oh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    reps = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            q.copy_(qh, non_blocking=True)
+            tq.tq_scores(ctx, q, cs, out, ws, stream=stream)
+            oh.copy_(out, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e = {"value": round(world * reps * M * N / (e0.elapsed_time(e1) * 1e-3), 1), "unit": "tokens scored/s",
+           "h2d_bytes_per_step": M * d * 4, "d2h_bytes_per_step": M * N * 4}
+    line = _line(args, world, "tokens scored/s", round(pairs, 1), "tokens scored/s", total_ms / args.steps,
+                 "u2 codes + 1-bit QJL, f16 operands, f32 accumulate",
+                 "synthetic (device-generated unit-norm Gaussian keys; seeded N(0,1) queries and S)",
+                 {"workload": "TurboQuant_Prod b=3 scores, d=128, 1M keys x 64 queries", "keys": N, "queries": M,
+                  "l2": f"inputs larger than L2: {bytes_call / 1e6:.0f} MB moved per call"},
+                 roof, e2e, args.steps, clk)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu["scores"](tq, cs, q, G, S)
+    return line if rank == 0 else None
+
+
+# ---------------------------------------------------------------- long context
+def run_longctx(args, world, rank, local, root, clocks_cls, cpu):
+    import numpy as np
+    import torch
+
+    import kv_cache_vector_tq_gb300 as tq
+    from kv_cache_vector_tq_gb300 import synth
+    torch.cuda.set_device(local)
+    D, B, HQ, HKV, SEQ, L, bits = 128, 1, 64, 8, 131072, args.layers, 3
+    ctx = tq.Context(D, bits, tq.TQ_MSE, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(synth.gaussian_matrix(0, D)))
+    cap = SEQ
+    gen = torch.Generator(device="cuda").manual_seed(4321 + rank)
+    layers = []
+    stream = torch.cuda.Stream()
+    enc_ms = 0.0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for layer in range(L):
+        K = tq.CodeSet(ctx, B * HKV * cap, tq.TQ_LAYOUT_TOKEN)
+        V = tq.CodeSet(ctx, B * HKV * cap, tq.TQ_LAYOUT_PAIR)
+        kv = torch.randn((2, B * HKV * SEQ, D), generator=gen, device="cuda", dtype=torch.float32)
+        kv[:, :, :4] *= 10.0
+        kv = kv.half()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):  # prefill: all but the last token of every (batch, KV head)
+            e0.record(stream)
+            tq.tq_encode(ctx, kv[0], K, 0, SEQ, cap, stream=stream)
+            tq.tq_encode(ctx, kv[1], V, 0, SEQ, cap, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        enc_ms += e0.elapsed_time(e1)
+        knew = kv[0].view(B * HKV, SEQ, D)[:, SEQ - 1].contiguous()
+        vnew = kv[1].view(B * HKV, SEQ, D)[:, SEQ - 1].contiguous()
+        del kv
+        layers.append((K, V, knew, vnew))
+    q = torch.randn((L, B, HQ, D), generator=gen, device="cuda").half()
+    out = torch.empty((L, B, HQ, D), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(tq.tq_decode_workspace_size(ctx, B, HQ, HKV, SEQ) // 4 + 64, dtype=torch.float32,
+                     device="cuda")
+    scale = 1.0 / math.sqrt(D)
+
+    def step():
+        for i, (K, V, knew, vnew) in enumerate(layers):
+            tq.tq_decode_step(ctx, ctx, q[i], knew, vnew, K, V, B, HQ, HKV, SEQ, cap, scale, out[i], ws,
+                              stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    total_ms, clk = _timed(g.replay, args.steps, args.warmup, stream, clocks_cls, local)
+    assert ctx.poll() == tq.TQ_OK
+    sec = total_ms * 1e-3
+    per_layer = B * HKV * SEQ * 2 * (D * bits // 8 + 4)
+    step_bytes = L * (per_layer + B * HQ * D * 6 + 2 * B * HKV * (D * 2 + D * bits // 8 + 4))
+    gbs = world * args.steps * step_bytes / sec / 1e9
+    hbm, _, kind = _peaks(root)
+    enc_vecs = L * 2 * B * HKV * SEQ
+    line = _line(args, world, "decode-attn HBM GB/s", round(gbs, 2), "GB/s", total_ms / args.steps,
+                 "u3 codes, f16 operands, f32 accumulate",
+                 "synthetic (device-generated N(0,1) fp16 K/V, channels 0-3 x10; N(0,1) queries)",
+                 {"workload": f"long-context decode, {L} layers in sequence, batch 1, 64 q / 8 kv heads, "
+                              f"head_dim 128, seq 131072, K/V TurboQuant_MSE b=3; step = append + attend per layer",
+                  "layers": L, "seq": SEQ, "heads_q": HQ, "heads_kv": HKV, "bits": bits,
+                  "resident_cache_gb": round(L * per_layer / 1e9, 2),
+                  "l2": f"inputs larger than L2: {L * per_layer / 1e9:.1f} GB of caches per step",
+                  "prefill_encode_mvec_s": round(enc_vecs / (enc_ms * 1e-3) / 1e6, 2),
+                  "prefill_encode_gbs": round(enc_vecs * (D * 2 + D * bits // 8 + 4) / (enc_ms * 1e-3) / 1e9, 1),
+                  "ms_per_layer": round(total_ms / args.steps / L, 4)},
+                 {"bound": "hbm", "achieved": round(gbs / world, 1), "peak": hbm, "unit": "GB/s",
+                  "frac": round(gbs / world / hbm, 4), "traffic": None, "kernel": "decode_step_kernel<3,3,8,8>",
+                  "peak_kind": kind, "bytes_per_step": step_bytes},
+                 None, args.steps * L, clk)
+    return line if rank == 0 else None
+
+
+# ---------------------------------------------------------------- keys (encode + one query)
+def run_keys(args, world, rank, local, root, clocks_cls, cpu):
+    import numpy as np
+    import torch
+
+    import kv_cache_vector_tq_gb300 as tq
+    from kv_cache_vector_tq_gb300 import synth
+    torch.cuda.set_device(local)
+    d, N, b = 128, 4096, 3
+    ctx = tq.Context(d, b, tq.TQ_MSE, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(synth.gaussian_matrix(0, d)))
+    x = torch.from_numpy(synth.gaussian_rows(0, N, d, outlier_cols=4, outlier_scale=20.0)).cuda()
+    q = torch.from_numpy(synth.queries(0, 1, d)).cuda()
+    cs = tq.CodeSet(ctx, N, tq.TQ_LAYOUT_TOKEN)
+    out = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(tq.tq_scores_workspace_size(ctx, 1) // 4, 4), dtype=torch.float32, device="cuda")
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def call():
+        tq.tq_encode(ctx, x, cs, stream=stream)
+        tq.tq_scores(ctx, q, cs, out, ws, stream=stream)
+
+    total_ms, clk = _timed(call, args.steps, args.warmup, stream, clocks_cls, local, flush=flush_buf.zero_)
+    assert ctx.poll() == tq.TQ_OK
+    sec = total_ms * 1e-3
+    mvec = world * args.steps * N / sec / 1e6
+    hbm, _, kind = _peaks(root)
+    byts = N * (4 * d + 48 + 4) + N * (48 + 4) + N * 4
+    ach = args.steps * byts / sec / 1e9
+    line = _line(args, world, "encode Mvec/s", round(mvec, 3), "Mvec/s", total_ms / args.steps,
+                 "f32 in, u3 codes, f16 hi/lo tensor products, f32 accumulate",
+                 "synthetic (seeded N(0,1) fp32 keys, channels 0-3 x20; N(0,1) query)",
+                 {"workload": "TurboQuant_MSE b=3, d=128: encode 4096 keys, then score 1 query against them",
+                  "keys": N, "l2": "L2 flushed (256 MB write) before every timed call",
+                  "us_per_encode_plus_score": round(total_ms / args.steps * 1e3, 2)},
+                 {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                  "traffic": None, "kernel": "encode_kernel + scores_kernel (latency-bound at this size)",
+                  "peak_kind": kind},
+                 None, 2 * args.steps, clk)
+    return line if rank == 0 else None
