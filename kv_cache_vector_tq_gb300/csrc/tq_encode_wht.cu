@@ -11,11 +11,10 @@
 // Per vector ("TurboQuant 详解", section 一个具体例子 steps 1-6): s = ‖x‖,
 // idx_i = #{k : v_i >= t_k}, pack, store s.
 //
-// Work split: m threads per vector (m in 32..256), 256/m vectors per CTA;
-// thread i' holds element a·m + i' of each of the P blocks a.  The Sylvester
-// stages pair threads i' and i' ^ h: by warp shuffles for h < 32, through
-// shared memory above; the 12 x 12 Paley stage is a fixed signed sum of the
-// thread's own P values.  Plain fp32 butterflies: each output sees one
+// Work split: one warp per Hadamard block of a vector (the twelve blocks of a
+// d = 12·m vector are the twelve warps of a CTA; for d = m, eight vectors per
+// CTA), lane L holding elements 32k + L of its block.  Rows stream into a
+// shared-memory ring by cp.async, three row groups ahead.  Plain fp32 butterflies: each output sees one
 // rounding per stage, so the error in v stays near √(log2 d)·2^-24 (about
 // 2e-7 at d = 3072), inside the 1e-6 band around the codebook thresholds.
 #include <algorithm>
@@ -51,116 +50,172 @@ __host__ __device__ constexpr int paley12_sign(int a, int b) {
              : -1;
 }
 
-template <int BM, int P, bool F16>
-__global__ void __launch_bounds__(256) encode_wht_kernel(const WhtParams p) {
-  extern __shared__ __align__(16) float wsm[];  // [256/m vectors][P][m], then the norm partials
-  const int m = p.m;
-  const int vpc = 256 / m;  // vectors per CTA
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int vloc = tid / m, ip = tid % m;  // vector within the CTA, element index within a block
-  float* my = wsm + vloc * P * m;
-  float* red = wsm + vpc * P * m;  // [8 warps]
-  float sg[P];
-#pragma unroll
-  for (int a = 0; a < P; ++a) sg[a] = p.signs[a * m + ip];
+constexpr int kWhtStages = 3;  // row groups in flight per CTA (cp.async ring)
 
-  for (int64_t base = (int64_t)blockIdx.x * vpc; base < p.N; base += (int64_t)gridDim.x * vpc) {
-    const int64_t r = base + vloc;
-    const bool have = r < p.N;
-    float x[P];
-#pragma unroll
-    for (int a = 0; a < P; ++a) {
-      float v = 0.f;
-      if (have) {
-        const int64_t o = r * p.d + a * m + ip;
-        v = F16 ? __half2float(__ldcs(static_cast<const __half*>(p.x) + o)) : __ldcs(static_cast<const float*>(p.x) + o);
-      }
-      x[a] = v;
+__device__ __forceinline__ void wcp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void wcp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void wcp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Pack the vector's codes (one byte per coordinate in `cb`) into word w of
+// the canonical stream: code j at bits [j·BM, j·BM + BM).
+template <int BM>
+__device__ __forceinline__ uint32_t pack_word(const unsigned char* cb, int w, int d) {
+  if constexpr (BM == 4) {  // eight codes: two 4-byte reads, bytes folded into nibbles
+    const uint2 u = *reinterpret_cast<const uint2*>(cb + 8 * w);
+    uint32_t lo = (u.x | (u.x >> 4)) & 0x00FF00FFu, hi = (u.y | (u.y >> 4)) & 0x00FF00FFu;
+    lo = (lo | (lo >> 8)) & 0xFFFFu;
+    hi = (hi | (hi >> 8)) & 0xFFFFu;
+    return lo | (hi << 16);
+  } else {
+    uint32_t word = 0u;
+    const int c0 = (32 * w) / BM, c1 = min(d, (32 * w + 32 + BM - 1) / BM);
+    for (int c = c0; c < c1; ++c) {
+      const int sh = c * BM - 32 * w;  // negative for a code straddling into this word
+      const uint32_t code = cb[c];
+      word |= sh >= 0 ? code << sh : code >> (-sh);
     }
-    // s = ‖x‖: the thread's P squares, then a tree over the vector's m threads
+    return word;
+  }
+}
+
+// Warp w of a CTA owns block a of one vector: P = 12 -> the CTA is one vector
+// (12 warps, a = w); P = 1 -> eight vectors, one warp each.  Lane L holds the
+// E = m/32 elements i' = 32k + L of its block, so the Sylvester stages with
+// h >= 32 run in registers and those with h < 32 by warp shuffles; the Paley
+// stage (P = 12) is the one exchange through shared memory.
+template <int BM, int P, int E, bool F16>
+__global__ void __launch_bounds__(P == 12 ? 384 : 256) encode_wht_kernel(const WhtParams p) {
+  constexpr int NW = P == 12 ? 12 : 8;  // warps per CTA
+  constexpr int VPC = P == 12 ? 1 : 8;  // vectors per CTA
+  constexpr int M = 32 * E;             // Sylvester order
+  constexpr int D = P * M;
+  constexpr int ES = F16 ? 2 : 4;
+  constexpr int SLOT = VPC * D * ES;    // a ring slot: the CTA's VPC consecutive rows
+  extern __shared__ __align__(16) unsigned char wsm[];
+  float* zs = reinterpret_cast<float*>(wsm);                    // [D] Paley exchange (P = 12)
+  float* part = zs + (P == 12 ? D : 0);                        // [12] warp norm partials
+  unsigned char* cbuf = reinterpret_cast<unsigned char*>(part + 16);  // [VPC][D] code bytes
+  unsigned char* ring = cbuf + ((VPC * D + 15) / 16) * 16;
+  __shared__ float thr_s[16];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int vloc = P == 12 ? 0 : warp, a = P == 12 ? warp : 0;
+  if (tid < 16) thr_s[tid] = tid < (1 << BM) - 1 ? p.thr[tid] : INFINITY;
+  float sg[E];
+#pragma unroll
+  for (int k = 0; k < E; ++k) sg[k] = p.signs[a * M + 32 * k + lane];
+  const int64_t stride_rows = (int64_t)gridDim.x * VPC;
+  auto fetch = [&](int64_t first_row, int slot) {
+    unsigned char* dst = ring + slot * SLOT;
+    const int64_t avail = min((int64_t)VPC, p.N - first_row);
+    for (int i = tid; i < SLOT / 16; i += NW * 32) {
+      if (i / (D * ES / 16) < avail)
+        wcp16(dst + i * 16, static_cast<const unsigned char*>(p.x) + first_row * D * ES + (int64_t)i * 16);
+      else
+        *reinterpret_cast<uint4*>(dst + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    wcp_commit();
+  };
+#pragma unroll
+  for (int k = 0; k < kWhtStages - 1; ++k) fetch((int64_t)blockIdx.x * VPC + k * stride_rows, k);
+  __syncthreads();
+
+  int it = 0;
+  for (int64_t base = (int64_t)blockIdx.x * VPC; base < p.N; base += stride_rows, ++it) {
+    // the slot refilled now was read last iteration; with P = 1 the warps do
+    // not meet after that read, so they do here
+    if constexpr (P == 1) __syncthreads();
+    fetch(base + (kWhtStages - 1) * stride_rows, (it + kWhtStages - 1) % kWhtStages);
+    wcp_wait<kWhtStages - 1>();
+    __syncthreads();  // this group's rows are in; the previous group's buffers are free
+    const unsigned char* src = ring + (it % kWhtStages) * SLOT + vloc * D * ES;
+    float x[E];
     float ss = 0.f;
 #pragma unroll
-    for (int a = 0; a < P; ++a) ss = fmaf(x[a], x[a], ss);
+    for (int k = 0; k < E; ++k) {
+      const int o = a * M + 32 * k + lane;
+      x[k] = F16 ? __half2float(reinterpret_cast<const __half*>(src)[o]) : reinterpret_cast<const float*>(src)[o];
+      ss = fmaf(x[k], x[k], ss);
+      x[k] *= sg[k];
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(kFull, ss, off);
-    if (m > 32) {
-      __syncthreads();  // the previous vector's readers of red are done
-      if (lane == 0) red[tid >> 5] = ss;
-      __syncthreads();
-      ss = 0.f;
-      for (int w = 0; w < m / 32; ++w) ss += red[vloc * (m / 32) + w];
-    }
-    const float s = sqrtf(ss);
-    // σ ∘ x, then the Sylvester stages over i'
+    // Sylvester stages of order M over i' = 32k + L
 #pragma unroll
-    for (int a = 0; a < P; ++a) x[a] *= sg[a];
-    for (int h = 1; h < m; h <<= 1) {
-      if (h < 32) {
+    for (int hk = 1; hk < E; hk <<= 1)  // h = 32·hk: partners k and k ^ hk, in registers
 #pragma unroll
-        for (int a = 0; a < P; ++a) {
-          const float o = __shfl_xor_sync(kFull, x[a], h);
-          x[a] = (ip & h) ? (o - x[a]) : (x[a] + o);
+      for (int k = 0; k < E; ++k)
+        if (!(k & hk)) {
+          const float u = x[k], v = x[k | hk];
+          x[k] = u + v;
+          x[k | hk] = u - v;
         }
-      } else {
-        __syncthreads();
 #pragma unroll
-        for (int a = 0; a < P; ++a) my[a * m + ip] = x[a];
-        __syncthreads();
+    for (int h = 1; h < 32; h <<= 1) {  // h < 32: partner lane L ^ h
+      const float sgn = (lane & h) ? -1.f : 1.f;
 #pragma unroll
-        for (int a = 0; a < P; ++a) {
-          const float o = my[a * m + (ip ^ h)];
-          x[a] = (ip & h) ? (o - x[a]) : (x[a] + o);
+      for (int k = 0; k < E; ++k) x[k] = fmaf(sgn, x[k], __shfl_xor_sync(kFull, x[k], h));
+    }
+    const int64_t r = base + vloc;
+    if constexpr (P == 12) {
+      // the Paley stage (z_a = Σ_b H12[a][b]·x_b per column i'), one exchange
+#pragma unroll
+      for (int k = 0; k < E; ++k) zs[a * M + 32 * k + lane] = x[k];
+      if (lane == 0) part[a] = ss;
+      __syncthreads();
+      float s2 = 0.f;
+#pragma unroll
+      for (int b = 0; b < 12; ++b) s2 += part[b];
+      const float s = sqrtf(s2);
+      // the Paley stage: thread T < M takes column i' = T of all twelve blocks
+      if (tid < M) {
+        float xb[12];
+#pragma unroll
+        for (int b = 0; b < 12; ++b) xb[b] = zs[b * M + tid];
+        const float inv = s > 0.f ? 1.f / s : 0.f;
+#pragma unroll
+        for (int aa = 0; aa < 12; ++aa) {
+          float acc = 0.f;
+#pragma unroll
+          for (int b = 0; b < 12; ++b) acc = paley12_sign(aa, b) > 0 ? acc + xb[b] : acc - xb[b];
+          const float v = acc * inv;  // v = z/s
+          int code = 0;
+#pragma unroll
+          for (int step = 1 << (BM - 1); step > 0; step >>= 1) code += v >= thr_s[code + step - 1] ? step : 0;
+          cbuf[aa * M + tid] = (unsigned char)(s > 0.f ? code : 0);
         }
       }
-    }
-    // the Paley stage across the blocks: z_a = Σ_b H12[a][b]·x_b
-    float z[P];
-    if constexpr (P == 12) {
-#pragma unroll
-      for (int a = 0; a < 12; ++a) {
-        float acc = 0.f;
-#pragma unroll
-        for (int bb = 0; bb < 12; ++bb) acc = paley12_sign(a, bb) > 0 ? acc + x[bb] : acc - x[bb];
-        z[a] = acc;
+      __syncthreads();
+      if (r < p.N) {
+        const int64_t dv = (r / p.group_rows) * p.group_stride + p.offset + (r % p.group_rows);
+        const int nw = (D * BM + 31) >> 5;
+        for (int w = tid; w < p.W; w += NW * 32) p.codes[dv * p.W + w] = w < nw ? pack_word<BM>(cbuf, w, D) : 0u;
+        if (tid == 0) p.norm[dv] = s;
       }
     } else {
+      // P = 1: the warp holds the whole vector
+      const float s = sqrtf(ss);
+      const float inv = s > 0.f ? 1.f / s : 0.f;
+      unsigned char* cw = cbuf + vloc * D;
 #pragma unroll
-      for (int a = 0; a < P; ++a) z[a] = x[a];
-    }
-    // bucketize v = z/s and pack: the 32 coordinates of a warp's lanes share BM words
-    const float inv = s > 0.f ? 1.f / s : 0.f;
-    const int64_t dv = have ? (r / p.group_rows) * p.group_stride + p.offset + (r % p.group_rows) : 0;
+      for (int k = 0; k < E; ++k) {
+        const float v = x[k] * inv;
+        int code = 0;
 #pragma unroll
-    for (int a = 0; a < P; ++a) {
-      const float v = z[a] * inv;
-      uint32_t code = 0;
-#pragma unroll
-      for (int k = 0; k < (1 << BM) - 1; ++k) code += v >= p.thr[k] ? 1u : 0u;
-      if (!(s > 0.f)) code = 0;
-      const int pos = lane * BM;  // bit position within the 32-coordinate group
-      uint32_t w[BM];
-#pragma unroll
-      for (int k = 0; k < BM; ++k) {
-        uint32_t c = 0;
-        if ((pos >> 5) == k) c = code << (pos & 31);
-        if ((pos >> 5) + 1 == k && (pos & 31) + BM > 32) c = code >> (32 - (pos & 31));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) c |= __shfl_xor_sync(kFull, c, off);
-        w[k] = c;
+        for (int step = 1 << (BM - 1); step > 0; step >>= 1) code += v >= thr_s[code + step - 1] ? step : 0;
+        cw[32 * k + lane] = (unsigned char)(s > 0.f ? code : 0);
       }
-      if (have && lane < BM) {
-        // group of coordinates a·m + 32q .. +31, q = i' / 32: words from (a·m + 32q)·BM / 32
-        const int word0 = ((a * m + (ip & ~31)) * BM) >> 5;
-        uint32_t val = w[0];
-#pragma unroll
-        for (int k = 1; k < BM; ++k)
-          if (lane == k) val = w[k];
-        p.codes[dv * p.W + word0 + lane] = val;
+      __syncwarp();
+      if (r < p.N) {
+        const int64_t dv = (r / p.group_rows) * p.group_stride + p.offset + (r % p.group_rows);
+        const int nw = (D * BM + 31) >> 5;
+        for (int w = lane; w < p.W; w += 32) p.codes[dv * p.W + w] = w < nw ? pack_word<BM>(cw, w, D) : 0u;
+        if (lane == 0) p.norm[dv] = s;
       }
-    }
-    if (have && ip == 0) {
-      p.norm[dv] = s;
-      for (int w = (p.d * BM + 31) / 32; w < p.W; ++w) p.codes[dv * p.W + w] = 0u;
     }
   }
 }
@@ -170,22 +225,43 @@ bool wht_supported(const DevCtx& c) {
          c.had_m <= 256 && (c.had_p == 1 || c.had_p == 12);
 }
 
-template <int BM, int P>
+template <int BM, int P, int E>
 static cudaError_t launch_wht_t(const WhtParams& p, bool f16, cudaStream_t st) {
-  const int vpc = 256 / p.m;
-  const int64_t ctas = (p.N + vpc - 1) / vpc;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * 8));
-  const size_t smem = ((size_t)vpc * P * p.m + 8) * sizeof(float);
+  constexpr int NW = P == 12 ? 12 : 8, VPC = P == 12 ? 1 : 8, D = P * 32 * E;
+  const int64_t ctas = (p.N + VPC - 1) / VPC;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * (P == 12 ? 4 : 8)));
+  const size_t smem = (size_t)(P == 12 ? D : 0) * 4 + 16 * 4 + (size_t)((VPC * D + 15) / 16) * 16 +
+                      (size_t)kWhtStages * VPC * D * (f16 ? 2 : 4);
+  static int attr_done[2] = {0, 0};  // set once, before any stream capture
+  if (!attr_done[f16 ? 1 : 0]) {
+    cudaError_t e = f16 ? cudaFuncSetAttribute(encode_wht_kernel<BM, P, E, true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024)
+                        : cudaFuncSetAttribute(encode_wht_kernel<BM, P, E, false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_done[f16 ? 1 : 0] = 1;
+  }
   if (f16)
-    encode_wht_kernel<BM, P, true><<<grid, 256, smem, st>>>(p);
+    encode_wht_kernel<BM, P, E, true><<<grid, NW * 32, smem, st>>>(p);
   else
-    encode_wht_kernel<BM, P, false><<<grid, 256, smem, st>>>(p);
+    encode_wht_kernel<BM, P, E, false><<<grid, NW * 32, smem, st>>>(p);
   return cudaGetLastError();
+}
+
+template <int BM, int P>
+static cudaError_t launch_wht_e(const WhtParams& p, bool f16, cudaStream_t st) {
+  switch (p.m) {
+    case 32: return launch_wht_t<BM, P, 1>(p, f16, st);
+    case 64: return launch_wht_t<BM, P, 2>(p, f16, st);
+    case 128: return launch_wht_t<BM, P, 4>(p, f16, st);
+    case 256: return launch_wht_t<BM, P, 8>(p, f16, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <int BM>
 static cudaError_t launch_wht_b(const WhtParams& p, int P, bool f16, cudaStream_t st) {
-  return P == 12 ? launch_wht_t<BM, 12>(p, f16, st) : launch_wht_t<BM, 1>(p, f16, st);
+  return P == 12 ? launch_wht_e<BM, 12>(p, f16, st) : launch_wht_e<BM, 1>(p, f16, st);
 }
 
 tq_status launch_encode_wht(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
