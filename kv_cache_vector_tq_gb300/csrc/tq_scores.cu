@@ -98,7 +98,7 @@ struct ScoreParams {
 };
 
 template <int BM, bool PROD>
-__global__ void __launch_bounds__(256) scores_kernel(const ScoreParams p) {
+__global__ void __launch_bounds__(256, 2) scores_kernel(const ScoreParams p) {
   extern __shared__ uint32_t sh[];
   constexpr int E = 1 << (2 * BM);
   uint32_t* lut = sh;                             // [E][32] replicated per lane
