@@ -117,9 +117,10 @@ def run_encode(args, world, rank, local, root, clocks_cls, cpu):
         ach = args.steps * 2.0 * N * d * d / sec / 1e12  # useful flops of Y = X·Πᵀ
         peak = bf16 / 3.0  # fp32-accurate products: three fp16 tensor passes (hi·hi, lo·hi, hi·lo)
         roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4), "traffic": None, "kernel": "encode_wide_kernel",
+                "frac": round(ach / peak, 4), "traffic": None, "kernel": "encode_umma_kernel",
                 "peak_kind": f"{kind} bf16 dense / 3 split passes (fp16 hi/lo, same tensor rate as bf16)",
-                "passes": 3, "flops_per_vector": 2 * d * d}
+                "passes": 3, "flops_per_vector": 2 * d * d,
+                "timed": "whole tq_encode call (row_norm_kernel + encode_umma_kernel)"}
     # end to end: rows from pinned host memory, codes and norms back, per call
     e2e = None
     if N * d * 4 <= (2 << 30):

@@ -179,6 +179,11 @@ tq_status tq_codes_layout(const tq_ctx* ctx, int layout, int64_t n, tq_codes* de
  * γ = 0 and all-zero QJL bits.  In PAIR layout, writes of vectors whose
  * partner vector is not in the same call are read-modify-write with atomics;
  * calls that write the same pair block must be ordered on one stream.
+ * d > 128 (MSE, TOKEN layout, d a multiple of 128 for the dense rotation;
+ * TQ_ERR_UNSUPPORTED otherwise): two kernels on `stream`, a norm pass and a
+ * tensor-core GEMM whose coordinates lying near a threshold are recomputed in
+ * float-float arithmetic, so codes match the fp64 definition outside a band
+ * of ~1e-6 around each threshold, as on every other path.
  */
 tq_status tq_encode(const tq_ctx* ctx, const void* d_x, int x_dtype, int64_t N,
                     const tq_codes* out, int64_t offset, int64_t group_rows,

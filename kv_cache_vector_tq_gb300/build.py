@@ -18,7 +18,7 @@ LIB = os.path.join(PKG, "libtq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["tq_host.cpp", "tq_encode.cu", "tq_encode_wht.cu", "tq_encode_wide.cu", "tq_scores.cu", "tq_decode.cu"]
+SOURCES = ["tq_host.cpp", "tq_encode.cu", "tq_encode_wht.cu", "tq_encode_umma.cu", "tq_scores.cu", "tq_decode.cu"]
 
 
 def _nvcc():
@@ -51,7 +51,7 @@ def build(verbose_ptxas=False, quiet=True):
         for _, log in results:
             sys.stderr.write(log)
     tmp = LIB + ".tmp"
-    cmd = [_nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-lcuda"]
+    cmd = [_nvcc(), "-shared", "-o", tmp] + objs + ARCH
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

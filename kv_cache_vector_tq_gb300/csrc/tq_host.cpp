@@ -322,6 +322,33 @@ static void encoder_fragments(const double* W, int d, double scale, std::vector<
           }
 }
 
+// pi_scale·Π as the B operand of the tcgen05 encoder (d > 128): for output
+// block ob (kUmmaTN coordinates), input chunk kc (kUmmaKC coordinates) and
+// plane (0: fp16 of w, 1: fp16 of the remainder w - hi), one kUmmaTN x kUmmaKC
+// tile in the no-swizzle K-major core-matrix order: 8 rows x 16 bytes per core
+// matrix, 128 bytes between core matrices along K, 1024 bytes between 8-row
+// groups.  Tile (ob, kc, plane) starts at ((ob·nkc + kc)·2 + plane)·kUmmaPlaneBytes.
+static void umma_tiles(const double* W, int d, double scale, std::vector<uint16_t>& out) {
+  const int nkc = d / kUmmaKC, nob = d / kUmmaTN;
+  const size_t plane = kUmmaPlaneBytes / 2;
+  out.assign((size_t)d * d * 2, 0);
+  parallel_for(nob, 1, [&](int a, int bb) {
+    for (int ob = a; ob < bb; ++ob)
+      for (int kc = 0; kc < nkc; ++kc) {
+        uint16_t* hi = out.data() + ((size_t)ob * nkc + kc) * 2 * plane;
+        uint16_t* lo = hi + plane;
+        for (int n = 0; n < kUmmaTN; ++n)
+          for (int kk = 0; kk < kUmmaKC; ++kk) {
+            const double w = scale * W[(size_t)(ob * kUmmaTN + n) * d + kc * kUmmaKC + kk];
+            const uint16_t hb = h_bits((float)w);
+            const size_t at = (size_t)(n / 8) * 512 + (kk / 8) * 64 + (n % 8) * 8 + (kk % 8);
+            hi[at] = hb;
+            lo[at] = h_bits((float)(w - (double)h_val(hb)));
+          }
+      }
+  });
+}
+
 }  // namespace tq
 
 using namespace tq;
@@ -379,8 +406,8 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   if (cb->d != d || cb->b != b_mse) return TQ_ERR_INVALID_ARG;
   if (mode == TQ_PROD && !h_S) return TQ_ERR_INVALID_ARG;
   if (mode == TQ_PROD && d > kChunk) return TQ_ERR_UNSUPPORTED;
-  int hm;
-  bool hp;
+  int hm = 0;
+  bool hp = false;
   if (rot_kind == TQ_ROT_HADAMARD && !hadamard_order(d, &hm, &hp)) return TQ_ERR_UNSUPPORTED;
 
   Ctx* c = new (std::nothrow) Ctx();
@@ -450,8 +477,19 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   }
 
   // ---- device tables
+  v.had_m = v.had_p = 0;
+  if (rot_kind == TQ_ROT_HADAMARD) {
+    v.had_m = hm;
+    v.had_p = hp ? 12 : 1;
+  }
+  // d <= 128: mma.sync fragments; d > 128: tcgen05 tiles (unless the Hadamard
+  // fast transform encodes without Π)
+  const bool wht_path = rot_kind == TQ_ROT_HADAMARD && mode == TQ_MSE && v.had_m >= 32 && v.had_m <= 256;
+  const bool umma_path = d > kChunk && d % kUmmaTN == 0 && mode == TQ_MSE && !wht_path;
   std::vector<uint2> frag_pi, frag_m;
-  encoder_fragments(c->h_pi, d, v.pi_scale, frag_pi, false);
+  std::vector<uint16_t> umma;
+  if (d <= kChunk) encoder_fragments(c->h_pi, d, v.pi_scale, frag_pi, false);
+  if (umma_path) umma_tiles(c->h_pi, d, v.pi_scale, umma);
   std::vector<double> M;
   if (mode == TQ_PROD) {
     M.assign(dd, 0.0);  // M = S·Πᵀ
@@ -500,7 +538,8 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   size_t o_s32 = o_p32 + al(pi32.size() * sizeof(float));
   size_t o_sl = o_s32 + al(s32.size() * sizeof(float));
   size_t o_sg = o_sl + al(slices.size() * sizeof(float));
-  size_t o_lut = o_sg + al(signs32.size() * sizeof(float));
+  size_t o_um = o_sg + al(signs32.size() * sizeof(float));
+  size_t o_lut = o_um + al(umma.size() * sizeof(uint16_t));
   size_t o_st = o_lut + al(lut.size() * sizeof(uint32_t));
   size_t total = o_st + 256;
   void* dmem = nullptr;
@@ -523,6 +562,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   if (e == cudaSuccess) e = up(o_s32, s32.data(), s32.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_sl, slices.data(), slices.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_sg, signs32.data(), signs32.size() * sizeof(float));
+  if (e == cudaSuccess) e = up(o_um, umma.data(), umma.size() * sizeof(uint16_t));
   if (e == cudaSuccess) e = up(o_lut, lut.data(), lut.size() * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(base + o_st, 0, 256);
   if (e != cudaSuccess) {
@@ -534,20 +574,13 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   }
   c->d_alloc = dmem;
   c->d_bytes = total;
-  v.enc_pi = (const uint2*)(base + o_pi);
+  v.enc_pi = d <= kChunk ? (const uint2*)(base + o_pi) : nullptr;
+  v.umma_tab = umma_path ? (const unsigned char*)(base + o_um) : nullptr;
   v.enc_m = mode == TQ_PROD ? (const uint2*)(base + o_m) : nullptr;
   v.pi = (const float*)(base + o_p32);
   v.s_mat = mode == TQ_PROD ? (const float*)(base + o_s32) : nullptr;
   v.pi_slices = d == kChunk ? (const float4*)(base + o_sl) : nullptr;
   v.signs = rot_kind == TQ_ROT_HADAMARD ? (const float*)(base + o_sg) : nullptr;
-  v.had_m = v.had_p = 0;
-  if (rot_kind == TQ_ROT_HADAMARD) {
-    int hm = 0;
-    bool hp = false;
-    hadamard_order(d, &hm, &hp);
-    v.had_m = hm;
-    v.had_p = hp ? 12 : 1;
-  }
   v.lut = (const uint32_t*)(base + o_lut);
   v.status = (int*)(base + o_st);
   *out = reinterpret_cast<tq_ctx*>(c);
@@ -615,7 +648,7 @@ tq_status tq_encode(const tq_ctx* ctx, const void* d_x, int x_dtype, int64_t N,
   if (!d_x || !al16(d_x)) return TQ_ERR_INVALID_ARG;
   const bool wht = wht_supported(v) && out->layout == TQ_LAYOUT_TOKEN;
   const bool wide = !wht && v.d > kChunk;
-  if (wide && (!wide_supported(v) || out->layout != TQ_LAYOUT_TOKEN)) return TQ_ERR_UNSUPPORTED;
+  if (wide && (!umma_supported(v) || out->layout != TQ_LAYOUT_TOKEN)) return TQ_ERR_UNSUPPORTED;
   // every destination index must lie inside the code set
   int64_t groups = (N + group_rows - 1) / group_rows;
   int64_t last_in_group = std::min<int64_t>(group_rows, N) - 1;
@@ -625,7 +658,7 @@ tq_status tq_encode(const tq_ctx* ctx, const void* d_x, int x_dtype, int64_t N,
   if (wht)
     return launch_encode_wht(v, d_x, x_dtype, N, out, offset, group_rows, group_stride, (cudaStream_t)stream);
   if (wide)
-    return launch_encode_wide(v, d_x, x_dtype, N, out, offset, group_rows, group_stride, (cudaStream_t)stream);
+    return launch_encode_umma(v, d_x, x_dtype, N, out, offset, group_rows, group_stride, (cudaStream_t)stream);
   return launch_encode(v, d_x, x_dtype, N, out, offset, group_rows, group_stride,
                        (cudaStream_t)stream);
 }

@@ -16,6 +16,11 @@ constexpr int kWarpRows = 16;     // rows (vectors) per warp tile of the encoder
 constexpr int kEncWarps = 8;      // warps per encoder CTA
 
 // Device-side view of a context, passed by value to kernels.
+// tcgen05 encoder for d > 128: Π tiles of kUmmaTN outputs x kUmmaKC inputs, two fp16 planes each
+constexpr int kUmmaTN = 128;
+constexpr int kUmmaKC = 64;
+constexpr int kUmmaPlaneBytes = kUmmaTN * kUmmaKC * 2;
+
 struct DevCtx {
   int d, b, b_mse, mode, rot;
   int words_per_vec, qjl_words_per_vec;
@@ -30,6 +35,7 @@ struct DevCtx {
   const float* pi;       // Π, d×d row-major fp32
   const float* s_mat;    // S, d×d row-major fp32, Prod only
   const float4* pi_slices;  // d = 128: Π[r][32c + 4j .. +3] at (c·8 + j)·128 + r (decode rotation)
+  const unsigned char* umma_tab;  // d > 128, MSE: pi_scale·Π hi/lo tiles for the tcgen05 encoder (else null)
   const float* signs;    // Hadamard rotation: σ, d entries of ±1 (else null)
   int had_m, had_p;      // Hadamard rotation: H = H12 ⊗ H_m (had_p = 12) or H_m (had_p = 1)
   const uint32_t* lut;   // pair table: 2^(2 b_mse) fp16x2 entries (alpha-scaled)
@@ -74,8 +80,8 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
                       const tq_codes* V, int B, int Hq, int Hkv, int64_t seq, int64_t cap,
                       float scale, float* out, void* ws, cudaStream_t stream);
 bool wht_supported(const DevCtx& c);
-bool wide_supported(const DevCtx& c);
-tq_status launch_encode_wide(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
+bool umma_supported(const DevCtx& c);
+tq_status launch_encode_umma(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
                              int64_t offset, int64_t group_rows, int64_t group_stride, cudaStream_t stream);
 tq_status launch_encode_wht(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
                             int64_t offset, int64_t group_rows, int64_t group_stride, cudaStream_t stream);

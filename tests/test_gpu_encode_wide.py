@@ -119,15 +119,18 @@ def haar_pair(seed, d, b):
     return tq.Context(d, b, tq.TQ_MSE, tq.TQ_ROT_DENSE, pi_lib), pi_ref
 
 
-@pytest.mark.parametrize("d", [256, 1536, 3072])
-@pytest.mark.parametrize("b", [2, 4])
+@pytest.mark.parametrize("d", [256, 384, 1536, 3072])
+@pytest.mark.parametrize("b", [1, 2, 3, 4])
 def test_dense_wide_encode(d, b):
-    """Dense Haar rotation for d > 128 (tiled tensor-core GEMM, float-float
-    accumulation across 128-wide chunks), ragged row count and a zero row."""
+    """Dense Haar rotation for d > 128 (tcgen05 GEMM over 128-row tiles plus
+    the exact recomputation of near-threshold coordinates): a ragged row
+    count (three tiles, the last one partial), a zero row and a row scaled by
+    1e4."""
     n = 300
     ctx, Pi = haar_pair(11, d, b)
     X = synth.bulk_rows(11, n, d)
     X[7] = 0.0
+    X[150] *= 1e4
     cs = encode(ctx, X)
     idx_ref, band = check(cs, Pi, X, b)
     words = cs.codes.view(torch.int32).cpu().numpy().view(np.uint32).reshape(n, -1)
@@ -154,11 +157,31 @@ def test_dense_bulk_indexing_full_size_sampled(d):
     check(cs, Pi, X, 4, rows)
 
 
+def test_dense_wide_encode_grouped_destination():
+    """Rows scattered into a larger code set (group_rows / group_stride /
+    offset), as when appending to (batch, head) blocks of a cache."""
+    d, b, n = 256, 4, 200
+    ctx, Pi = haar_pair(14, d, b)
+    X = synth.bulk_rows(14, n, d)
+    x = torch.from_numpy(X).cuda()
+    cs = tq.CodeSet(ctx, 1000, tq.TQ_LAYOUT_TOKEN)
+    tq.tq_encode(ctx, x, cs, offset=3, group_rows=50, group_stride=240)
+    torch.cuda.synchronize()
+    assert ctx.poll() == tq.TQ_OK
+    dst = np.array([(r // 50) * 240 + 3 + r % 50 for r in range(n)])
+    cb = codebook(d, b)
+    idx_ref, s_ref, v = oq.mse_quantize(X.astype(np.float64), Pi, cb["centroids"], math.sqrt(d))
+    band = oq.near_threshold(v, cb["centroids"])
+    idx = np.stack([tq.tq_unpack_indices(cs, int(r), 1)[0] for r in dst])
+    assert not ((idx.astype(np.int64) != idx_ref) & ~band).any()
+    np.testing.assert_allclose(cs.norm.cpu().numpy().astype(np.float64)[dst], s_ref, rtol=1e-6, atol=0)
+
+
 def test_wide_encode_rejects_unsupported():
-    """d > 128 with the dense rotation: b in {2, 4}, MSE, TOKEN layout only."""
+    """d > 128 with the dense rotation: MSE and TOKEN layout only."""
     ctx, _ = haar_pair(13, 256, 3)
     x = torch.zeros((4, 256), dtype=torch.float32, device="cuda")
-    cs = tq.CodeSet(ctx, 4, tq.TQ_LAYOUT_TOKEN)
+    cs = tq.CodeSet(ctx, 4, tq.TQ_LAYOUT_PAIR)
     with pytest.raises(tq.TqError) as err:
         tq.tq_encode(ctx, x, cs)
     assert err.value.status == tq.TQ_ERR_UNSUPPORTED
