@@ -216,7 +216,15 @@ tq_status tq_scores(const tq_ctx* ctx, const float* d_q, int M, const tq_codes* 
  *   k̂ = s · Πᵀ ŷ, kv = h / (Hq / Hkv).
  * The value sum is accumulated in the rotated domain and rotated back once per
  * head at the end (linearity of Πᵀ).
- * kctx, vctx  contexts of the K and V codes (TQ_MSE); may be the same.
+ * Keys may be TurboQuant_Prod (kctx in TQ_PROD; [P1] section
+ * "TurboQuant_prod", [P2] "内积偏差问题与 QJL 修正器"): then
+ *   k̂ = s · (Πᵀ ŷ + γ · √(π/2)/d · Sᵀ (2·bits − 1)),
+ * the unbiased inner-product estimate, computed as ⟨Π q, ŷ⟩ plus
+ * γ·√(π/2)/d·⟨S q, 2·bits − 1⟩ with both query rotations done once per call.
+ * K then needs its QJL words and γ (qjl, rnorm), and Hq / Hkv <= 4
+ * (TQ_ERR_UNSUPPORTED otherwise).
+ * kctx, vctx  contexts of the K (TQ_MSE or TQ_PROD) and V (TQ_MSE) codes; may
+ *             be the same.
  * d_q       [B, Hq, d], fp32 or fp16 (q_dtype).
  * K         TOKEN layout; V: PAIR layout.  Vector index of token t of
  *           (batch b, kv head h) is (b * Hkv + h) * cap + t; tokens [0, seq)
@@ -248,7 +256,9 @@ tq_status tq_decode_attention(const tq_ctx* kctx, const tq_ctx* vctx, const void
  * where the two roundings may fall on either side, and the same norm to fp32
  * rounding) into position seq-1 of every (batch, KV head) block of K and V,
  * then computes tq_decode_attention over tokens [0, seq) including the new
- * one, in one kernel launch.  Other arguments, the workspace and errors as
+ * one, in one kernel launch.  Keys must be TurboQuant_MSE here
+ * (TQ_ERR_UNSUPPORTED for TQ_PROD: append with tq_encode, then call
+ * tq_decode_attention).  Other arguments, the workspace and errors as
  * tq_decode_attention.  The V pair block of position seq-1 is updated with atomics, so
  * its partner token (seq-2 or seq) may be written by an ordered earlier call.
  */

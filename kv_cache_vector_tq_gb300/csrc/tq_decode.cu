@@ -1,61 +1,10 @@
-// Decode attention over a TurboQuant_MSE KV cache (d = 128), one fused kernel
-// per decode step.
-//
-// "TurboQuant 详解", section decode 阶段到底怎么“用”这些压缩后的 KV (second route):
-// the kernel unpacks, looks up, scales and consumes the codes inside attention,
-// never materialising fp16 K/V; and (same page, "decode 阶段") the token of the
-// step is appended to the cache first.  "sub-byte-kv-cache-quantization-
-// turboquant", section 工程实现的关键路径: the query is rotated once and query head
-// h reads kv_head = h / (Hq / Hkv).
-//
-// Work split: S CTAs per (batch, KV head), each over a contiguous range of
-// 16-token tiles; the grid fits the GPU in one wave (one CTA per SM).
-//  1. Every CTA rotates the query heads of its KV head itself, q̂_h = Π·q_h,
-//     with its slice of Π loaded before it waits for the previous grid (Π is
-//     constant data), so the G·128·128 products cost no extra launch.
-//  2. The CTA whose range holds position seq-1 also rotates the new K and V
-//     (compensated dot products), encodes them (norm, bucketize against the
-//     codebook thresholds, pack), writes them to the cache and patches them
-//     into its staged tile; it takes half a share of the tiles to make room.
-//  3. Every CTA streams its tiles: each lane copies its own 16-byte chunks
-//     with cp.async into lane-private shared-memory slots, three tiles ahead,
-//     and the warp runs
-//       K side  S[t][n] = Σ_κ K̂[t][κ]·Q[κ][n]   (mma.m16n8k16: A from a pair
-//               table indexed by two codes, B = pre-rotated queries, hi/lo)
-//       softmax online per head in base 2 (scale folded into Q), lazy rescale
-//       V side  O[μ][n] += Σ_t V̂[μ][t]·W[t][n]  (A from V pair blocks, which
-//               hold two consecutive tokens' codes side by side; B = p·s_v)
-//  4. The warps of a CTA merge their softmax states.  O stays in the rotated
-//     domain up to here (Σ_t p_t s_t Πᵀŷ_t = Πᵀ Σ_t p_t s_t ŷ_t); the CTA applies
-//     Πᵀ to its own partial, which commutes with the rescaled merge.
-//  5. With S > 1 each CTA publishes (m, l, Πᵀ·acc) and the last CTA of the
-//     (batch, KV head) to arrive merges the S partials into the output.
-#include <algorithm>
+// Host side of decode attention: parameters, the launch, and the variant
+// without a workspace.  The kernel is in tq_decode_kernel.cuh.
 #include <mutex>
-#include <utility>
 
-#include "tq_device.cuh"
-#include "tq_internal.h"
+#include "tq_decode_kernel.cuh"
 
 namespace tq {
-
-constexpr int kTileTok = 16;
-constexpr int kStages = 3;            // tiles in flight per warp
-constexpr int kFieldBytes = 32 * 16;  // one 16-byte slot per lane
-constexpr int kStageBytes = 4 * kFieldBytes + 128;  // + the tile's 16 K and 16 V norms
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLazy = 8.f;  // rescale only when the running max grows by > 2^8
-constexpr int kPart = 132;    // floats per head in a published partial: m, l, 2 pad, acc[128]
-// Shared-window offset of dynamic shared memory in a kernel without static
-// shared memory (the runtime reserves the window's first KB).  The 4-bit
-// decode addresses its tables from it at compile time and checks it at run time.
-constexpr uint32_t kSmemWindow = 0x400;
-
-// Workspace: one arrival counter per (batch, KV head), then the partial state
-// (m, l, Πᵀ·acc[128]) of every CTA when a (batch, KV head) is split over more
-// than one CTA.  Splits are only made while the grid fits one CTA per SM, so
-// the number of partials is bounded by the SM count.
-static size_t ws_counter_bytes(int groups) { return ((size_t)groups * 4 + 255) / 256 * 256; }
 
 size_t decode_ws_bytes(int d, int B, int Hq, int Hkv, int64_t seq) {
   (void)d;
@@ -65,848 +14,6 @@ size_t decode_ws_bytes(int d, int B, int Hq, int Hkv, int64_t seq) {
   return ws_counter_bytes(B * Hkv) + (size_t)num_sms() * G * kPart * sizeof(float) + 256;
 }
 
-// ------------------------------------------------------------------ cp.async
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void copy_words(void* dst, const uint32_t* src) {
-  if constexpr (N == 4) {
-    cp_async16(dst, src);
-  } else if constexpr (N == 2) {
-    cp_async8(dst, src);
-  } else {
-#pragma unroll
-    for (int i = 0; i < N; ++i) cp_async4(static_cast<uint32_t*>(dst) + i, src + i);
-  }
-}
-
-// ------------------------------------------------------------------ small helpers
-template <int N>
-__device__ __forceinline__ void read_words(uint32_t (&w)[N], const unsigned char* src) {
-  if constexpr (N == 4) {
-    const uint4 v = *reinterpret_cast<const uint4*>(src);
-    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-  } else if constexpr (N == 2) {
-    const uint2 v = *reinterpret_cast<const uint2*>(src);
-    w[0] = v.x; w[1] = v.y;
-  } else {
-#pragma unroll
-    for (int i = 0; i < N; ++i) w[i] = reinterpret_cast<const uint32_t*>(src)[i];
-  }
-}
-
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = a + b;
-  const float bb = s - a;
-  e = (a - (s - bb)) + (b - bb);
-}
-
-// Read-only 16-byte load kept in program order with the grid-dependency wait
-// (volatile), so that loads of constant data are in flight while it waits.
-__device__ __forceinline__ float4 ldg_early(const float4* p) {
-  float4 v;
-  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];\n"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p));
-  return v;
-}
-
-
-// ------------------------------------------------------------------ parameters
-struct StepParams {
-  const float4* kslices;  // Π of the K context in column slices (see the rotation below)
-  const float4* vslices;  // the same for the V context
-  const float* vpi;       // Π of the V context, 128 x 128 row-major fp32 (output rotation)
-  const uint32_t* klut;
-  const uint32_t* vlut;
-  int same_lut;
-  float kthr[15];
-  float vthr[15];
-  float kfold;  // scale·log2(e) / (√d·α_K)
-  float vfold;  // 1 / (α_V·√d)
-  float sqrt_d;
-  uint32_t* kcodes;
-  float* knorm;
-  uint32_t* vcodes;
-  float* vnorm;
-  int64_t seq, cap;
-  int B, Hq, Hkv, S, tiles;
-  int* status;    // device status word of the K context
-  int* counters;  // [B*Hkv] arrival counters (zero between calls)
-  float* part;    // [B*Hkv][S][G][kPart] per-CTA (m, l, Πᵀ·acc) when S > 1
-  const void* q;
-  int q_f16;
-  const void* knew;
-  const void* vnew;
-  int new_f16;
-  int append;
-  float* out;
-};
-
-// First tile of CTA u of the U CTAs that share a (batch, KV head).  With an
-// appended token the last CTA, which owns position seq-1 and encodes the new
-// K and V before it streams, takes half a share.
-__host__ __device__ inline int split_begin(int u, int U, int tiles, bool append) {
-  if (u >= U) return tiles;
-  if (!append || U == 1) return (int)((int64_t)u * tiles / U);
-  return (int)((int64_t)2 * u * tiles / (2 * U - 1));
-}
-
-// Shared-memory layout (bytes), computed identically on host and device.
-// Each warp has kStages tile stages of four 512-byte fields (one 16-byte slot
-// per lane: K codes of tokens g and g+8, V pair blocks t and t+4) and the
-// tile's 16 K and 16 V norms,
-// which after the tile loop hold its softmax state.
-struct StepSmem {
-  int vlut, stage, wreg, mw, qs, qhat, newin, ynew, newcodes, uni, opart, qfs, cpart, outp, flag, bytes;
-};
-
-// Offset in a warp region of its rows of Π_V: after its softmax state
-// ((NT·512 + 16) floats) and its partial outputs (G·128 floats).
-__host__ __device__ inline int pi_off(int G) {
-  const int NT = (2 * G + 7) / 8, a = (NT * 512 + 16) * 4, b = G * 128 * 4;
-  return ((a > b ? a : b) + 127) / 128 * 128;
-}
-
-__host__ __device__ inline StepSmem step_smem(int bk, int bv, int G, int W, bool same_lut) {
-  StepSmem m;
-  const int NT = (2 * G + 7) / 8, NCH = W / 4;
-  int o = (1 << (2 * bk)) * 32 * 4;
-  m.vlut = o;
-  if (bk == 4 && bv == 4)
-    o = 256 * 256;  // byte-indexed rows: K entries at lane·4, V entries at 128 + lane·4
-  else if (!same_lut)
-    o += (1 << (2 * bv)) * 32 * 4;
-  o = (o + 127) / 128 * 128;
-  // after the loop: its state (then its partial outputs), and its rows of Π_V at pi_off
-  const int st = kStages * kStageBytes, cw = pi_off(G) + (128 / W) * 512;
-  m.wreg = ((st > cw ? st : cw) + 127) / 128 * 128;
-  m.stage = o;  // after the tile loop: the warps' states, then partial outputs [W][G][128]
-  o += W * m.wreg;
-  // [0, o) also holds the S published partials while the last CTA merges them
-  m.mw = o;
-  o += 16;
-  m.qs = o;
-  o += G * 128 * 4;  // the query heads in fp32
-  m.qhat = o;
-  o += G * 128 * 4;  // rotated queries
-  m.newin = o;
-  o += 2 * 128 * 4;  // k_new, v_new as fp32
-  m.ynew = o;
-  o += 2 * 128 * 4;  // rotated k_new, v_new
-  m.newcodes = o;
-  o += (16 + 32 + 32 + 4) * 4;  // K words, V slot bits, V slot mask, norms
-  // one region used twice: the rotation's partial sums (and the appended
-  // token's), then the query fragments, the warp-merged state and the output
-  m.uni = o;
-  m.opart = o + NCH * G * 128 * 4;
-  m.qfs = o;
-  m.cpart = o + 8 * NT * 32 * 8;
-  m.outp = m.cpart + (NT * 512 + 16) * 4;
-  const int u1 = NCH * G * 128 * 4 + NCH * 128 * 16, u2 = m.outp + G * 128 * 4 - o;
-  o += u1 > u2 ? u1 : u2;
-  m.flag = o;
-  o += 16;
-  m.bytes = (o + 127) / 128 * 128;
-  return m;
-}
-
-// ------------------------------------------------------------------ the kernel
-template <int BK, int BV, int G, int W>
-__global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams p) {
-  constexpr int NT = (2 * G + 7) / 8;
-  constexpr int WK = 4 * BK, WV = 4 * BV;  // words per vector
-  constexpr int EK = 1 << (2 * BK), EV = 1 << (2 * BV);
-  constexpr int NTH = W * 32;
-  constexpr int NCH = W / 4;    // column chunks of the rotation (4 warps, 128 rows, per chunk)
-  constexpr int CW = 128 / NCH;  // columns per chunk
-  constexpr int NF4 = CW / 4;
-  constexpr int RPW = 128 / W;  // Π_V rows per warp in the output rotation
-  constexpr int QPT = (G * 128 + NTH - 1) / NTH;  // query elements per thread
-  constexpr bool kByte = BK == 4 && BV == 4;      // pair codes are whole bytes
-  static_assert(W % 4 == 0 && NTH >= 256, "4 warps per rotation chunk; a thread per new-token element");
-  extern __shared__ __align__(128) unsigned char smem[];
-  if (kByte && smem_u32(smem) != kSmemWindow) {  // the table addresses below assume it
-    if (threadIdx.x == 0) atomicOr(p.status, 2);
-    return;
-  }
-  const StepSmem L = step_smem(BK, BV, G, W, p.same_lut != 0);
-  uint32_t* klut = reinterpret_cast<uint32_t*>(smem);
-  uint32_t* vlut = p.same_lut ? klut : reinterpret_cast<uint32_t*>(smem + L.vlut);
-  unsigned char* stage = smem + L.stage;
-  float* qs = reinterpret_cast<float*>(smem + L.qs);      // [G][128]
-  float* qhat = reinterpret_cast<float*>(smem + L.qhat);  // [G][128]
-  float* newin = reinterpret_cast<float*>(smem + L.newin);  // [2][128]
-  float* ynew = reinterpret_cast<float*>(smem + L.ynew);    // [2][128]
-  uint32_t* nk_words = reinterpret_cast<uint32_t*>(smem + L.newcodes);  // [16]
-  uint32_t* nv_bits = nk_words + 16;                                     // [32]
-  uint32_t* nv_mask = nv_bits + 32;                                      // [32]
-  float* new_norm = reinterpret_cast<float*>(nv_mask + 32);              // [2]
-  float* rpart = reinterpret_cast<float*>(smem + L.uni);     // [NCH][G][128]
-  float4* opart = reinterpret_cast<float4*>(smem + L.opart);  // [NCH][128]
-  uint2* qfs = reinterpret_cast<uint2*>(smem + L.qfs);       // [8][NT][32]
-  float* cpart = reinterpret_cast<float*>(smem + L.cpart);   // [NT*512] fragment order, M[8], L[8]
-  float* cM = cpart + NT * 512;
-  float* cL = cM + 8;
-  float* outp = reinterpret_cast<float*>(smem + L.outp);  // [G][128]
-  int* flag = reinterpret_cast<int*>(smem + L.flag);
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int grp = blockIdx.x / p.S, split = blockIdx.x % p.S;  // grp = b * Hkv + kvh
-  const int b = grp / p.Hkv, kvh = grp % p.Hkv;
-  const bool append = p.append != 0;
-  const int t_begin = split_begin(split, p.S, p.tiles, append);
-  const int t_end = split_begin(split + 1, p.S, p.tiles, append);
-  const int ntl = t_end - t_begin;
-  const int64_t gbase = (int64_t)grp * p.cap;  // vector index of token 0 of the group
-  const int new_tile = (int)((p.seq - 1) / kTileTok), new_row = (int)((p.seq - 1) % kTileTok);
-  const bool owner = append && new_tile >= t_begin && new_tile < t_end;
-  unsigned char* my_stage = stage + warp * L.wreg;
-
-  // ---- prologue on constant data (overlaps the previous grid where an SM is
-  //      free): this thread's slice of Π_K (and, in the owner, of Π_V), the
-  //      barriers, and the pair tables replicated per lane.  Thread (row, chunk)
-  //      = (32(w%4) + lane, w/4) reads Π[row][chunk·CW ..+CW) from the slice
-  //      table, where a warp's 32 rows of one slice column are contiguous.
-  const int rrow = 32 * (warp & 3) + lane, rc0 = (warp >> 2) * CW;
-  float4 pk[NF4], pv[NF4];
-#pragma unroll
-  for (int j = 0; j < NF4; ++j) {
-    const int col = rc0 + 4 * j;
-    pk[j] = ldg_early(p.kslices + ((col >> 5) * 8 + ((col & 31) >> 2)) * 128 + rrow);
-  }
-  if (owner) {
-#pragma unroll
-    for (int j = 0; j < NF4; ++j) {
-      const int col = rc0 + 4 * j;
-      pv[j] = ldg_early(p.vslices + ((col >> 5) * 8 + ((col & 31) >> 2)) * 128 + rrow);
-    }
-  }
-  for (int i = tid; i < 16 + 32 + 32; i += NTH) nk_words[i] = 0u;
-  if constexpr (kByte) {  // row i: K entry x32 lanes, then V entry x32 lanes
-    constexpr int NB = 256 * 16 / NTH;
-    uint32_t v[NB];
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-      const int i = tid + k * NTH;
-      v[k] = __ldg(((i >> 3) & 1 ? p.vlut : p.klut) + (i >> 4));
-    }
-#pragma unroll
-    for (int k = 0; k < NB; ++k) reinterpret_cast<uint4*>(smem)[tid + k * NTH] = make_uint4(v[k], v[k], v[k], v[k]);
-  } else {
-    constexpr int NK = (EK * 8 + NTH - 1) / NTH;
-    uint32_t v[NK];
-#pragma unroll
-    for (int k = 0; k < NK; ++k) {
-      const int i = tid + k * NTH;
-      v[k] = i < EK * 8 ? __ldg(p.klut + (i >> 3)) : 0u;
-    }
-#pragma unroll
-    for (int k = 0; k < NK; ++k) {
-      const int i = tid + k * NTH;
-      if (i < EK * 8) reinterpret_cast<uint4*>(klut)[i] = make_uint4(v[k], v[k], v[k], v[k]);
-    }
-    if (!p.same_lut) {
-      constexpr int NV = (EV * 8 + NTH - 1) / NTH;
-      uint32_t u[NV];
-#pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        const int i = tid + k * NTH;
-        u[k] = i < EV * 8 ? __ldg(p.vlut + (i >> 3)) : 0u;
-      }
-#pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        const int i = tid + k * NTH;
-        if (i < EV * 8) reinterpret_cast<uint4*>(vlut)[i] = make_uint4(u[k], u[k], u[k], u[k]);
-      }
-    }
-  }
-  __syncthreads();
-  griddep_wait();    // the cache, q and the new token may come from earlier grids
-  griddep_launch();  // the next grid may start its own prologue as SMs free up
-
-  // ---- inputs of the step, requested before the tile copies queue up
-  float qv[QPT];
-#pragma unroll
-  for (int k = 0; k < QPT; ++k) {
-    const int e = tid + k * NTH;
-    qv[k] = 0.f;
-    if (e < G * 128) {
-      const int64_t off = ((int64_t)b * p.Hq + kvh * G + (e >> 7)) * 128 + (e & 127);
-      qv[k] = p.q_f16 ? __half2float(static_cast<const __half*>(p.q)[off]) : static_cast<const float*>(p.q)[off];
-    }
-  }
-  float nv = 0.f;  // owner: element tid of [k_new; v_new]
-  if (owner && tid < 256) {
-    const void* src = tid >= 128 ? p.vnew : p.knew;
-    const int64_t off = (int64_t)grp * 128 + (tid & 127);
-    nv = p.new_f16 ? __half2float(static_cast<const __half*>(src)[off]) : static_cast<const float*>(src)[off];
-  }
-  auto issue = [&](int j) {  // warp-local tile j -> stage j % kStages, one 16-byte slot per lane
-    const int tile = t_begin + warp + j * W;
-    if (tile < t_end) {
-      unsigned char* st = my_stage + (j % kStages) * kStageBytes;
-      const int64_t vb = gbase + (int64_t)tile * kTileTok;
-      copy_words<BK>(st + 0 * kFieldBytes + lane * 16, p.kcodes + (vb + g) * WK + t * BK);
-      copy_words<BK>(st + 1 * kFieldBytes + lane * 16, p.kcodes + (vb + g + 8) * WK + t * BK);
-      // V pair blocks t and t+4 of the tile; this lane's coordinates 16g..16g+15
-      copy_words<BV>(st + 2 * kFieldBytes + lane * 16, p.vcodes + (vb + 2 * t) * WV + g * BV);
-      copy_words<BV>(st + 3 * kFieldBytes + lane * 16, p.vcodes + (vb + 2 * t + 8) * WV + g * BV);
-      if (lane < 8)  // lanes 0-3: the 16 K norms, lanes 4-7: the 16 V norms
-        cp_async16(st + 4 * kFieldBytes + lane * 16, (lane < 4 ? p.knorm : p.vnorm) + vb + 4 * (lane & 3));
-    }
-    cp_async_commit();  // always, so that the group count stays uniform
-  };
-  issue(0);  // one tile per warp now; the rest after the rotation, which would queue behind them
-#pragma unroll
-  for (int k = 0; k < QPT; ++k)
-    if (tid + k * NTH < G * 128) qs[tid + k * NTH] = qv[k];
-  if (owner && tid < 256) newin[tid] = nv;
-  __syncthreads();
-
-  // ---- 1. q̂_h = Π_K·q_h: thread (row, chunk) sums over its chunk's columns
-  //         (all lanes read the same query words), the chunks meet in rpart
-  {
-    float acc[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = 0.f;
-#pragma unroll
-    for (int j = 0; j < NF4; ++j) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float4 x = *reinterpret_cast<const float4*>(qs + h * 128 + rc0 + 4 * j);
-        acc[h] = fmaf(pk[j].x, x.x, fmaf(pk[j].y, x.y, fmaf(pk[j].z, x.z, fmaf(pk[j].w, x.w, acc[h]))));
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) rpart[((warp >> 2) * G + h) * 128 + rrow] = acc[h];
-  }
-  if (owner) {
-    // ---- 2a. the appended token, rotated as a compensated dot product
-    //          (products split exactly with an FMA, sums by error-free
-    //          two-sums) so that its codes agree with the encoder's up to
-    //          coordinates within ~1e-6 of a codebook threshold
-    auto dot2 = [&](const float4 (&pr)[NF4], const float* x, float& hi, float& lo) {
-      hi = 0.f;
-      lo = 0.f;
-#pragma unroll
-      for (int j = 0; j < NF4; ++j) {
-        const float4 xv = *reinterpret_cast<const float4*>(x + rc0 + 4 * j);
-        const float pa[4] = {pr[j].x, pr[j].y, pr[j].z, pr[j].w}, xa[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pp = pa[e] * xa[e];
-          const float er = fmaf(pa[e], xa[e], -pp);
-          float s, err;
-          two_sum(hi, pp, s, err);
-          hi = s;
-          lo += err + er;
-        }
-      }
-    };
-    float kh, kl, vh, vl;
-    dot2(pk, newin, kh, kl);
-    dot2(pv, newin + 128, vh, vl);
-    opart[(warp >> 2) * 128 + rrow] = make_float4(kh, kl, vh, vl);
-  }
-  __syncthreads();
-  for (int e = tid; e < G * 128; e += NTH) {  // sum the column chunks
-    const int h = e >> 7, row = e & 127;
-    float s = 0.f;
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) s += rpart[(c * G + h) * 128 + row];
-    qhat[e] = s;
-  }
-  if (owner) {
-    // ---- 2b. encode the appended K and V: norm, bucketize, pack, store
-    if (tid < 256) {
-      const int which = tid >> 7, row = tid & 127;
-      float hi = 0.f, lo = 0.f;
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        const float4 v = opart[c * 128 + row];
-        float s, err;
-        two_sum(hi, which ? v.z : v.x, s, err);
-        hi = s;
-        lo += (which ? v.w : v.y) + err;
-      }
-      ynew[tid] = hi + lo;
-    }
-    if (tid < 64) {  // norms (warp 0: K, warp 1: V), each lane 4 squares, then a tree
-      const int which = tid >> 5;
-      float ss = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float x = newin[which * 128 + lane + 32 * i];
-        ss = fmaf(x, x, ss);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(kFull, ss, off);
-      if (lane == 0) new_norm[which] = sqrtf(ss);
-    }
-    __syncthreads();
-    // unit-variance coordinate √d·y/‖x‖ against the codebook thresholds
-    const int slot = (int)((p.seq - 1) & 1);
-    if (tid < 256) {
-      const int which = tid >> 7, i = tid & 127;
-      const float s = new_norm[which];
-      uint32_t code = 0;
-      if (s > 0.f) {
-        const float v = ynew[tid] * (p.sqrt_d / s);
-        const int nb = which ? BV : BK;
-        const float* thr = which ? p.vthr : p.kthr;
-        for (int k = 0; k < (1 << nb) - 1; ++k) code += v >= thr[k] ? 1u : 0u;
-      }
-      if (which == 0) {
-        const int pos = i * BK;
-        atomicOr(&nk_words[pos >> 5], code << (pos & 31));
-        if ((pos & 31) + BK > 32) atomicOr(&nk_words[(pos >> 5) + 1], code >> (32 - (pos & 31)));
-      } else {
-        const int pos = (2 * i + slot) * BV;
-        const uint32_t m = (1u << BV) - 1u;
-        atomicOr(&nv_bits[pos >> 5], code << (pos & 31));
-        atomicOr(&nv_mask[pos >> 5], m << (pos & 31));
-        if ((pos & 31) + BV > 32) {
-          atomicOr(&nv_bits[(pos >> 5) + 1], code >> (32 - (pos & 31)));
-          atomicOr(&nv_mask[(pos >> 5) + 1], m >> (32 - (pos & 31)));
-        }
-      }
-    }
-    __syncthreads();
-    const int64_t pos = gbase + p.seq - 1;
-    if (tid < WK) p.kcodes[pos * WK + tid] = nk_words[tid];
-    if (tid < 2 * WV) {
-      uint32_t* w = p.vcodes + (pos >> 1) * (2 * WV) + tid;
-      atomicAnd(w, ~nv_mask[tid]);
-      atomicOr(w, nv_bits[tid]);
-    }
-    if (tid == 0) {
-      p.knorm[pos] = new_norm[0];
-      p.vnorm[pos] = new_norm[1];
-    }
-  }
-  __syncthreads();
-
-  // ---- query B fragments, built once for all warps: b0 = (K index 16s+2t.., col g),
-  //      b1 = (16s+8+2t.., col g); K index 16s+8h+2t+e <-> coordinate 32t+4s+2h+e;
-  //      col n = 2·head + (1 for the fp16 rounding residual).  The merged state
-  //      beside them starts at zero.
-  for (int e = tid; e < 8 * NT * 32; e += NTH) {
-    const int ln = e & 31, nt = (e >> 5) % NT, s8 = (e >> 5) / NT;
-    const int n = nt * 8 + (ln >> 2), h = n >> 1;
-    uint2 f = make_uint2(0u, 0u);
-    if (h < G) {
-      const float4 x = *reinterpret_cast<const float4*>(qhat + h * 128 + 32 * (ln & 3) + 4 * s8);
-      uint32_t h0, l0, h1, l1;
-      split2(x.x * p.kfold, x.y * p.kfold, h0, l0);
-      split2(x.z * p.kfold, x.w * p.kfold, h1, l1);
-      f = (n & 1) ? make_uint2(l0, l1) : make_uint2(h0, h1);
-    }
-    qfs[e] = f;
-  }
-  __syncthreads();
-  uint2 qf[8][NT];
-#pragma unroll
-  for (int s = 0; s < 8; ++s)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) qf[s][nt] = qfs[(s * NT + nt) * 32 + lane];
-#pragma unroll
-  for (int j = 1; j < kStages; ++j) issue(j);
-
-  // ---- 3. stream the tiles
-  const uint32_t* mykl = klut + lane;
-  const uint32_t* myvl = vlut + lane;
-  const uint32_t lane4 = lane * 4;
-  float m_run[NT], l_run[NT];
-  float o[8][NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m_run[nt] = -INFINITY;
-    l_run[nt] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
-  }
-  for (int j = 0; warp + j * W < ntl; ++j) {
-    const int tile = t_begin + warp + j * W;
-    cp_async_wait<kStages - 1>();
-    const unsigned char* st = my_stage + (j % kStages) * kStageBytes;
-    uint32_t k0[BK], k1[BK], v0w[BV], v1w[BV];
-    read_words<BK>(k0, st + 0 * kFieldBytes + lane * 16);
-    read_words<BK>(k1, st + 1 * kFieldBytes + lane * 16);
-    read_words<BV>(v0w, st + 2 * kFieldBytes + lane * 16);
-    read_words<BV>(v1w, st + 3 * kFieldBytes + lane * 16);
-    const float* ns = reinterpret_cast<const float*>(st + 4 * kFieldBytes);
-    float4 nrm = make_float4(ns[g], ns[g + 8], ns[16 + g], ns[16 + g + 8]);
-    if (owner && tile == new_tile) {  // the appended token: use the codes just made
-      if (new_row == g) {
-#pragma unroll
-        for (int w = 0; w < BK; ++w) k0[w] = nk_words[t * BK + w];
-        nrm.x = new_norm[0];
-        nrm.z = new_norm[1];
-      }
-      if (new_row == g + 8) {
-#pragma unroll
-        for (int w = 0; w < BK; ++w) k1[w] = nk_words[t * BK + w];
-        nrm.y = new_norm[0];
-        nrm.w = new_norm[1];
-      }
-      const int pbn = new_row >> 1;
-      if ((pbn & 3) == t) {
-#pragma unroll
-        for (int w = 0; w < BV; ++w) {
-          const uint32_t m = nv_mask[g * BV + w], nb = nv_bits[g * BV + w];
-          if (pbn < 4)
-            v0w[w] = (v0w[w] & ~m) | nb;
-          else
-            v1w[w] = (v1w[w] & ~m) | nb;
-        }
-      }
-    }
-    // every lane's words are in registers: refill this stage
-    issue(j + kStages);
-    const int lt0 = tile * kTileTok;
-    // K side: S = K̂·Q with two independent MMA chains
-    float sa[NT][4], sb[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      uint32_t a0, a1, a2, a3;
-      if constexpr (kByte) {  // a0/a2: bytes 2(s&1), 2(s&1)+1 of word s/2 (a1/a3 likewise from k1)
-        a0 = lds_at<kSmemWindow>(byte_row_addr(k0[s >> 1], lane4, 2 * (s & 1)));
-        a1 = lds_at<kSmemWindow>(byte_row_addr(k1[s >> 1], lane4, 2 * (s & 1)));
-        a2 = lds_at<kSmemWindow>(byte_row_addr(k0[s >> 1], lane4, 2 * (s & 1) + 1));
-        a3 = lds_at<kSmemWindow>(byte_row_addr(k1[s >> 1], lane4, 2 * (s & 1) + 1));
-      } else {
-        a0 = mykl[get_bits<2 * BK>(k0, 4 * s * BK) << 5];
-        a1 = mykl[get_bits<2 * BK>(k1, 4 * s * BK) << 5];
-        a2 = mykl[get_bits<2 * BK>(k0, (4 * s + 2) * BK) << 5];
-        a3 = mykl[get_bits<2 * BK>(k1, (4 * s + 2) * BK) << 5];
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (s & 1)
-          mma16816(sb[nt], a0, a1, a2, a3, qf[s][nt].x, qf[s][nt].y);
-        else
-          mma16816(sa[nt], a0, a1, a2, a3, qf[s][nt].x, qf[s][nt].y);
-      }
-    }
-    const bool ok0 = lt0 + g < p.seq, ok1 = lt0 + g + 8 < p.seq;
-    // online softmax per head h = 4nt + t (lanes of equal t share a head)
-    float w0[NT], w1[NT];
-    bool need = false;
-    float zz0[NT], zz1[NT], mx[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      zz0[nt] = ok0 ? (sa[nt][0] + sb[nt][0] + sa[nt][1] + sb[nt][1]) * nrm.x : -INFINITY;
-      zz1[nt] = ok1 ? (sa[nt][2] + sb[nt][2] + sa[nt][3] + sb[nt][3]) * nrm.y : -INFINITY;
-      float m = fmaxf(zz0[nt], zz1[nt]);
-      m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
-      m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
-      m = fmaxf(m, __shfl_xor_sync(kFull, m, 16));
-      mx[nt] = m;
-      need |= m > m_run[nt] + kLazy;
-    }
-    if (__any_sync(kFull, need)) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (mx[nt] > m_run[nt] + kLazy) {
-          const float f = (m_run[nt] == -INFINITY) ? 0.f : ex2(m_run[nt] - mx[nt]);
-          m_run[nt] = mx[nt];
-          l_run[nt] *= f;
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[mt][nt][e] *= f;
-        }
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const float p0 = ex2(zz0[nt] - m_run[nt]);
-      const float p1 = ex2(zz1[nt] - m_run[nt]);
-      l_run[nt] += p0 + p1;
-      w0[nt] = p0 * nrm.z * p.vfold;
-      w1[nt] = p1 * nrm.w * p.vfold;
-    }
-    // V side: B[k = token][n = col g] for tokens 2t, 2t+1, 2t+8, 2t+9
-    uint32_t bw[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int h4 = g >> 1;  // head within this n-tile (col g = 2·h4 + lo)
-      const int src0 = 4 * (2 * t) + h4, src1 = 4 * (2 * t + 1) + h4;
-      const float x0 = __shfl_sync(kFull, w0[nt], src0);
-      const float x1 = __shfl_sync(kFull, w0[nt], src1);
-      const float x2 = __shfl_sync(kFull, w1[nt], src0);
-      const float x3 = __shfl_sync(kFull, w1[nt], src1);
-      uint32_t h0, l0, h1, l1;
-      split2(x0, x1, h0, l0);
-      split2(x2, x3, h1, l1);
-      const bool head_ok = 4 * nt + h4 < G;
-      bw[nt][0] = head_ok ? ((g & 1) ? l0 : h0) : 0u;  // odd columns: the rounding residual
-      bw[nt][1] = head_ok ? ((g & 1) ? l1 : h1) : 0u;
-    }
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      // rows g / g+8 <-> coordinates 16g + 2mt / 16g + 2mt + 1
-      uint32_t a0, a1, a2, a3;
-      if constexpr (kByte) {  // bytes 2(mt&1), 2(mt&1)+1 of word mt/2
-        a0 = lds_at<kSmemWindow + 128>(byte_row_addr(v0w[mt >> 1], lane4, 2 * (mt & 1)));
-        a1 = lds_at<kSmemWindow + 128>(byte_row_addr(v0w[mt >> 1], lane4, 2 * (mt & 1) + 1));
-        a2 = lds_at<kSmemWindow + 128>(byte_row_addr(v1w[mt >> 1], lane4, 2 * (mt & 1)));
-        a3 = lds_at<kSmemWindow + 128>(byte_row_addr(v1w[mt >> 1], lane4, 2 * (mt & 1) + 1));
-      } else {
-        a0 = myvl[get_bits<2 * BV>(v0w, (2 * mt) * 2 * BV) << 5];
-        a1 = myvl[get_bits<2 * BV>(v0w, (2 * mt + 1) * 2 * BV) << 5];
-        a2 = myvl[get_bits<2 * BV>(v1w, (2 * mt) * 2 * BV) << 5];
-        a3 = myvl[get_bits<2 * BV>(v1w, (2 * mt + 1) * 2 * BV) << 5];
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816(o[mt][nt], a0, a1, a2, a3, bw[nt][0], bw[nt][1]);
-    }
-  }
-  cp_async_wait_all();
-  // this warp's rows of Π_V for the output rotation, copied into its own region
-  // while the warps merge (asynchronous: no registers held, nothing waits on them yet)
-  {
-    float* prow = reinterpret_cast<float*>(my_stage + pi_off(G));
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) cp_async16(prow + r * 128 + 4 * lane, p.vpi + (warp * RPW + r) * 128 + 4 * lane);
-    cp_async_commit();
-  }
-
-  // ---- 4. merge the warps and rotate back.  Each warp leaves its state in its
-  //         own region in fragment order: acc value (nt, mt, e) of lane l at
-  //         ((nt·8 + mt)·2 + e)·32 + l, head 4nt + (l & 3), coordinate
-  //         16(l >> 2) + 2mt + e; then m[8], l[8].
-  {
-    float* cw = reinterpret_cast<float*>(my_stage);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float l = l_run[nt];
-      l += __shfl_xor_sync(kFull, l, 4);
-      l += __shfl_xor_sync(kFull, l, 8);
-      l += __shfl_xor_sync(kFull, l, 16);
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        cw[((nt * 8 + mt) * 2 + 0) * 32 + lane] = o[mt][nt][0] + o[mt][nt][1];
-        cw[((nt * 8 + mt) * 2 + 1) * 32 + lane] = o[mt][nt][2] + o[mt][nt][3];
-      }
-      if (g == 0 && 4 * nt + t < G) {
-        cw[NT * 512 + 4 * nt + t] = m_run[nt];
-        cw[NT * 512 + 8 + 4 * nt + t] = l;
-      }
-    }
-  }
-  __syncthreads();
-  // 4a. factors f_w = 2^(m_w - M) of the warps, M and Σ_w f_w·l_w per head
-  float* fw = qhat;  // [W][G]; the rotated queries are in the fragments now
-  if (tid < W * G) {
-    const int w = tid / G, h = tid % G;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w2 = 0; w2 < W; ++w2) M = fmaxf(M, reinterpret_cast<const float*>(stage + w2 * L.wreg)[NT * 512 + h]);
-    const float mv = reinterpret_cast<const float*>(stage + w * L.wreg)[NT * 512 + h];
-    fw[tid] = (mv == -INFINITY) ? 0.f : ex2(mv - M);
-    if (w == 0) cM[h] = M;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float Lw = 0.f;
-#pragma unroll
-    for (int w = 0; w < W; ++w)
-      Lw = fmaf(fw[w * G + tid], reinterpret_cast<const float*>(stage + w * L.wreg)[NT * 512 + 8 + tid], Lw);
-    cL[tid] = Lw;
-  }
-  for (int e = tid; e < NT * 512; e += NTH) {
-    const int h = 4 * (e >> 9) + (e & 3);
-    if (h < G) {
-      float A = 0.f;
-#pragma unroll
-      for (int w = 0; w < W; ++w) A = fmaf(fw[w * G + h], reinterpret_cast<const float*>(stage + w * L.wreg)[e], A);
-      cpart[e] = A;
-    }
-  }
-  __syncthreads();
-  // 4b. Πᵀ·acc: warp w sums its RPW rows k of Π_V, lane its 4 output coordinates
-  {  // partial outputs [G][128] of warp w at the start of its region (its state is merged)
-    cp_async_wait_all();
-    __syncwarp();
-    const float4* prow = reinterpret_cast<const float4*>(my_stage + pi_off(G));
-    float4 op[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) op[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-      const int k = warp * RPW + r;  // coordinate 16gk + 2mtk + ek
-      const int base = (((k >> 1) & 7) * 2 + (k & 1)) * 32 + 4 * (k >> 4);
-      const float4 pv4 = prow[r * 32 + lane];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float a = cpart[(h >> 2) * 512 + base + (h & 3)];
-        op[h].x = fmaf(pv4.x, a, op[h].x);
-        op[h].y = fmaf(pv4.y, a, op[h].y);
-        op[h].z = fmaf(pv4.z, a, op[h].z);
-        op[h].w = fmaf(pv4.w, a, op[h].w);
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) reinterpret_cast<float4*>(my_stage + h * 512)[lane] = op[h];
-  }
-  __syncthreads();
-  for (int e = tid; e < G * 128; e += NTH) {
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < W; ++w) s += reinterpret_cast<const float*>(stage + w * L.wreg)[e];
-    outp[e] = s;
-  }
-  __syncthreads();
-  float* outg = p.out + ((int64_t)b * p.Hq + kvh * G) * 128;  // [G][128] of this KV head
-  if (p.S == 1) {
-    for (int e = tid; e < G * 128; e += NTH) outg[e] = outp[e] / cL[e >> 7];
-    return;
-  }
-  // ---- 5. publish (m, l, Πᵀ·acc); the last CTA of the (batch, KV head) merges
-  {
-    float* dst = p.part + ((size_t)grp * p.S + split) * G * kPart;
-    for (int e = tid; e < G * kPart; e += NTH) {
-      const int h = e / kPart, k = e % kPart;
-      dst[e] = k == 0 ? cM[h] : (k == 1 ? cL[h] : (k < 4 ? 0.f : outp[h * 128 + k - 4]));
-    }
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();  // releases the CTA's stores above (ordered by the barrier)
-      const int old = atomicAdd(p.counters + grp, 1);
-      const int last = old == p.S - 1;
-      if (last) p.counters[grp] = 0;  // ready for the next call
-      __threadfence();
-      *flag = last;
-    }
-    __syncthreads();
-  }
-  if (!*flag) return;
-  // all S partials into shared memory in one round trip (the tables and the ring are dead)
-  float* mb = reinterpret_cast<float*>(smem);  // [S][G][kPart]
-  {
-    const float4* src4 = reinterpret_cast<const float4*>(p.part + (size_t)grp * p.S * G * kPart);
-    const int n4 = p.S * G * (kPart / 4);
-    for (int e0 = tid; e0 < n4; e0 += 8 * NTH) {
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (e0 + u * NTH < n4) v[u] = __ldcg(src4 + e0 + u * NTH);
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (e0 + u * NTH < n4) reinterpret_cast<float4*>(mb)[e0 + u * NTH] = v[u];
-    }
-  }
-  __syncthreads();
-  // factor 2^(m_s - M) of every partial, into its first pad slot
-  for (int e = tid; e < p.S * G; e += NTH) {
-    const int h = e % G;
-    float M = -INFINITY;
-    for (int sp = 0; sp < p.S; ++sp) M = fmaxf(M, mb[(sp * G + h) * kPart]);
-    const float ms = mb[e * kPart];
-    mb[e * kPart + 2] = (ms == -INFINITY) ? 0.f : ex2(ms - M);
-  }
-  __syncthreads();
-  for (int e = tid; e < G * 128; e += NTH) {
-    const int h = e >> 7, dim = e & 127;
-    float A = 0.f, Ls = 0.f;
-    for (int sp = 0; sp < p.S; ++sp) {
-      const float* ps = mb + (sp * G + h) * kPart;
-      A = fmaf(ps[2], ps[4 + dim], A);
-      Ls = fmaf(ps[2], ps[1], Ls);
-    }
-    outg[e] = A / Ls;
-  }
-}
-
-// ------------------------------------------------------------------ launch
-// CTAs per (batch, KV head): the whole grid resident at once (one CTA per SM),
-// and no more partials than the last CTA can stage; among those, the fewest
-// CTAs that reach the smallest number of tiles per warp (a split costs about
-// one tile time for the merge through memory).
-static int choose_splits(int tiles, int groups, int W, bool append, int merge_cap) {
-  const int smax = std::max(1, std::min(std::min(num_sms() / std::max(1, groups), tiles), merge_cap));
-  int bestS = 1;
-  long best = -1;
-  for (int S = 1; S <= smax; ++S) {
-    // largest share of a CTA: ceil of the mean share (the owner's is smaller)
-    const int worst = (!append || S == 1) ? (tiles + S - 1) / S : (2 * tiles + 2 * S - 2) / (2 * S - 1);
-    const long cost = (worst + W - 1) / W + (S > 1 ? 1 : 0);
-    if (best < 0 || cost < best) {
-      best = cost;
-      bestS = S;
-    }
-  }
-  return bestS;
-}
-
-template <int BK, int BV, int G>
-static cudaError_t run_step(const StepParams& p, int groups, cudaStream_t st) {
-  constexpr int W = G >= 8 ? 8 : 16;
-  auto kern = decode_step_kernel<BK, BV, G, W>;
-  static int attr_done = 0;  // set once, before any stream capture
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_done = 1;
-  }
-  const StepSmem L = step_smem(BK, BV, G, W, p.same_lut != 0);
-  StepParams pp = p;
-  pp.S = choose_splits(p.tiles, groups, W, p.append != 0, L.mw / (G * kPart * 4));
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(groups * pp.S);
-  cfg.blockDim = dim3(W * 32);
-  cfg.dynamicSmemBytes = L.bytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, pp);
-}
-
-template <int BK, int BV>
-static cudaError_t run_step_g(const StepParams& p, int G, int groups, cudaStream_t st) {
-  switch (G) {
-    case 1: return run_step<BK, BV, 1>(p, groups, st);
-    case 2: return run_step<BK, BV, 2>(p, groups, st);
-    case 4: return run_step<BK, BV, 4>(p, groups, st);
-    case 8: return run_step<BK, BV, 8>(p, groups, st);
-  }
-  return cudaErrorInvalidValue;
-}
-
-template <int BK>
-static cudaError_t run_step_v(const StepParams& p, int bv, int G, int groups, cudaStream_t st) {
-  switch (bv) {
-    case 1: return run_step_g<BK, 1>(p, G, groups, st);
-    case 2: return run_step_g<BK, 2>(p, G, groups, st);
-    case 3: return run_step_g<BK, 3>(p, G, groups, st);
-    case 4: return run_step_g<BK, 4>(p, G, groups, st);
-  }
-  return cudaErrorInvalidValue;
-}
 
 tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_dtype,
                       const void* knew, const void* vnew, int new_dtype, const tq_codes* K,
@@ -914,6 +21,10 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
                       float scale, float* out, void* ws, cudaStream_t stream) {
   if (cap % 16 != 0) return TQ_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
+  const bool prod = kc.mode == TQ_PROD;
+  if (prod && (knew != nullptr || G > 4 || kc.b_mse > 3 || !kc.s_slices || !K->d_qjl || !K->d_rnorm ||
+               K->qjl_words_per_vec != 4))
+    return TQ_ERR_UNSUPPORTED;
   bool same_lut = kc.b_mse == vc.b_mse && kc.alpha == vc.alpha;
   for (int k = 0; same_lut && k < (1 << kc.b_mse); ++k) same_lut = kc.cen[k] == vc.cen[k];
   StepParams p;
@@ -929,6 +40,10 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
     p.vthr[k] = vc.thr[k];
   }
   p.kfold = scale * kLog2e / (kc.sqrt_d * kc.alpha);
+  p.qfold = prod ? (float)(scale * kLog2e * std::sqrt(3.14159265358979323846 / 2.0) / kc.d) : 0.f;
+  p.sslices = prod ? kc.s_slices : nullptr;
+  p.kqjl = prod ? K->d_qjl : nullptr;
+  p.krn = prod ? K->d_rnorm : nullptr;
   p.vfold = 1.f / (vc.alpha * vc.sqrt_d);
   p.sqrt_d = kc.sqrt_d;
   p.kcodes = K->d_codes;
@@ -953,13 +68,14 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
   p.counters = static_cast<int*>(ws);
   p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + ws_counter_bytes(groups));
   cudaError_t e;
-  switch (kc.b_mse) {
-    case 1: e = run_step_v<1>(p, vc.b_mse, G, groups, stream); break;
-    case 2: e = run_step_v<2>(p, vc.b_mse, G, groups, stream); break;
-    case 3: e = run_step_v<3>(p, vc.b_mse, G, groups, stream); break;
-    case 4: e = run_step_v<4>(p, vc.b_mse, G, groups, stream); break;
-    default: return TQ_ERR_UNSUPPORTED;
-  }
+  if (prod)
+    e = decode_run_prod(p, kc.b_mse, vc.b_mse, G, groups, stream);
+  else if (kc.b_mse == 1 || kc.b_mse == 2)
+    e = decode_run_k12(p, kc.b_mse, vc.b_mse, G, groups, stream);
+  else if (kc.b_mse == 3 || kc.b_mse == 4)
+    e = decode_run_k34(p, kc.b_mse, vc.b_mse, G, groups, stream);
+  else
+    return TQ_ERR_UNSUPPORTED;
   return e == cudaSuccess ? TQ_OK : set_cuda_error(e);
 }
 

@@ -520,9 +520,18 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
           for (int e = 0; e < 4; ++e)
             slices[(((size_t)cc * 8 + j) * d + r) * 4 + e] = pi32[(size_t)r * d + 32 * cc + 4 * j + e];
   }
+  std::vector<float> sslices;
   if (mode == TQ_PROD) {
     s32.resize(dd);
     for (size_t i = 0; i < dd; ++i) s32[i] = (float)c->h_s[i];
+    if (d == kChunk) {  // S in the same column slices, for the query's S-rotation in decode
+      sslices.resize(dd);
+      for (int cc = 0; cc < d / 32; ++cc)
+        for (int j = 0; j < 8; ++j)
+          for (int r = 0; r < d; ++r)
+            for (int e = 0; e < 4; ++e)
+              sslices[(((size_t)cc * 8 + j) * d + r) * 4 + e] = s32[(size_t)r * d + 32 * cc + 4 * j + e];
+    }
   }
   const int E = 1 << (2 * b_mse);
   std::vector<uint32_t> lut(E);
@@ -538,7 +547,8 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   size_t o_s32 = o_p32 + al(pi32.size() * sizeof(float));
   size_t o_sl = o_s32 + al(s32.size() * sizeof(float));
   size_t o_sg = o_sl + al(slices.size() * sizeof(float));
-  size_t o_um = o_sg + al(signs32.size() * sizeof(float));
+  size_t o_ss = o_sg + al(signs32.size() * sizeof(float));
+  size_t o_um = o_ss + al(sslices.size() * sizeof(float));
   size_t o_lut = o_um + al(umma.size() * sizeof(uint16_t));
   size_t o_st = o_lut + al(lut.size() * sizeof(uint32_t));
   size_t total = o_st + 256;
@@ -562,6 +572,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   if (e == cudaSuccess) e = up(o_s32, s32.data(), s32.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_sl, slices.data(), slices.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_sg, signs32.data(), signs32.size() * sizeof(float));
+  if (e == cudaSuccess) e = up(o_ss, sslices.data(), sslices.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_um, umma.data(), umma.size() * sizeof(uint16_t));
   if (e == cudaSuccess) e = up(o_lut, lut.data(), lut.size() * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(base + o_st, 0, 256);
@@ -576,6 +587,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   c->d_bytes = total;
   v.enc_pi = d <= kChunk ? (const uint2*)(base + o_pi) : nullptr;
   v.umma_tab = umma_path ? (const unsigned char*)(base + o_um) : nullptr;
+  v.s_slices = sslices.empty() ? nullptr : (const float4*)(base + o_ss);
   v.enc_m = mode == TQ_PROD ? (const uint2*)(base + o_m) : nullptr;
   v.pi = (const float*)(base + o_p32);
   v.s_mat = mode == TQ_PROD ? (const float*)(base + o_s32) : nullptr;
@@ -699,7 +711,7 @@ tq_status tq_decode_attention(const tq_ctx* kctx, const tq_ctx* vctx, const void
   if (!kctx || !vctx || !K || !V) return TQ_ERR_INVALID_ARG;
   const DevCtx& kc = reinterpret_cast<const Ctx*>(kctx)->dev;
   const DevCtx& vc = reinterpret_cast<const Ctx*>(vctx)->dev;
-  if (kc.mode != TQ_MSE || vc.mode != TQ_MSE || kc.d != vc.d) return TQ_ERR_INVALID_ARG;
+  if (vc.mode != TQ_MSE || kc.d != vc.d) return TQ_ERR_INVALID_ARG;  // keys MSE or Prod, values MSE
   tq_status st = check_codes(kc, K);
   if (st != TQ_OK) return st;
   st = check_codes(vc, V);
@@ -728,7 +740,8 @@ tq_status tq_decode_step(const tq_ctx* kctx, const tq_ctx* vctx, const void* d_q
   if (!kctx || !vctx || !K || !V) return TQ_ERR_INVALID_ARG;
   const DevCtx& kc = reinterpret_cast<const Ctx*>(kctx)->dev;
   const DevCtx& vc = reinterpret_cast<const Ctx*>(vctx)->dev;
-  if (kc.mode != TQ_MSE || vc.mode != TQ_MSE || kc.d != vc.d) return TQ_ERR_INVALID_ARG;
+  if (vc.mode != TQ_MSE || kc.d != vc.d) return TQ_ERR_INVALID_ARG;
+  if (kc.mode != TQ_MSE) return TQ_ERR_UNSUPPORTED;  // the fused append encodes MSE keys only
   tq_status st = check_codes(kc, K);
   if (st != TQ_OK) return st;
   st = check_codes(vc, V);
@@ -760,7 +773,7 @@ tq_status tq_decode_attention_noalloc(const tq_ctx* kctx, const tq_ctx* vctx, co
   if (!kctx || !vctx || !K || !V) return TQ_ERR_INVALID_ARG;
   const DevCtx& kc = reinterpret_cast<const Ctx*>(kctx)->dev;
   const DevCtx& vc = reinterpret_cast<const Ctx*>(vctx)->dev;
-  if (kc.mode != TQ_MSE || vc.mode != TQ_MSE || kc.d != vc.d) return TQ_ERR_INVALID_ARG;
+  if (vc.mode != TQ_MSE || kc.d != vc.d) return TQ_ERR_INVALID_ARG;  // keys MSE or Prod, values MSE
   tq_status st = check_codes(kc, K);
   if (st != TQ_OK) return st;
   st = check_codes(vc, V);

@@ -35,6 +35,7 @@ struct DevCtx {
   const float* pi;       // Π, d×d row-major fp32
   const float* s_mat;    // S, d×d row-major fp32, Prod only
   const float4* pi_slices;  // d = 128: Π[r][32c + 4j .. +3] at (c·8 + j)·128 + r (decode rotation)
+  const float4* s_slices;   // d = 128, Prod: S in the same slices (decode S-rotation of the query)
   const unsigned char* umma_tab;  // d > 128, MSE: pi_scale·Π hi/lo tiles for the tcgen05 encoder (else null)
   const float* signs;    // Hadamard rotation: σ, d entries of ±1 (else null)
   int had_m, had_p;      // Hadamard rotation: H = H12 ⊗ H_m (had_p = 12) or H_m (had_p = 1)

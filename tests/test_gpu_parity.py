@@ -296,6 +296,87 @@ def test_decode_asymmetric_bits():
     run_decode(4, 2, 1, 16, 4, 2048)
 
 
+def run_decode_prod(b_k, b_v, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float16):
+    """Decode attention with TurboQuant_Prod keys ((b_k - 1)-bit MSE codes plus
+    QJL sign bits and γ) and TurboQuant_MSE values, against attention over the
+    explicitly dequantized Prod keys x̂ = s·(Πᵀŷ + γ·√(π/2)/d·Sᵀ·sign) built
+    from the GPU's own codes."""
+    d = 128
+    cap = cap or (seq + 15) // 16 * 16
+    kctx, Pi_k, S = make_pair(seed, d, b_k, tq.TQ_PROD)
+    vctx, Pi_v, _ = make_pair(seed + 100, d, b_v)
+    Kh, Vh = synth.kv_layer(seed, 0, B, Hkv, seq, d)
+    Kc = tq.CodeSet(kctx, B * Hkv * cap, tq.TQ_LAYOUT_TOKEN)
+    Vc = tq.CodeSet(vctx, B * Hkv * cap, tq.TQ_LAYOUT_PAIR)
+    kx = torch.from_numpy(np.ascontiguousarray(Kh.reshape(-1, d))).cuda()
+    vx = torch.from_numpy(np.ascontiguousarray(Vh.reshape(-1, d))).cuda()
+    tq.tq_encode(kctx, kx, Kc, offset=0, group_rows=seq, group_stride=cap)
+    tq.tq_encode(vctx, vx, Vc, offset=0, group_rows=seq, group_stride=cap)
+    q_np = synth.queries(seed, B * Hq, d).reshape(B, Hq, d)
+    q = torch.from_numpy(q_np).cuda().to(q_dtype)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(tq.tq_decode_workspace_size(kctx, B, Hq, Hkv, seq) // 4 + 4, dtype=torch.float32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    tq.tq_decode_attention(kctx, vctx, q, Kc, Vc, B, Hq, Hkv, seq, cap, scale, out, ws)
+    torch.cuda.synchronize()
+    assert kctx.poll() == tq.TQ_OK and vctx.poll() == tq.TQ_OK
+    kidx, kbits = [], []
+    for blk in range(B * Hkv):
+        i, bt = tq.tq_unpack_indices(Kc, blk * cap, seq, with_bits=True)
+        kidx.append(i)
+        kbits.append(bt)
+    kidx, kbits = np.concatenate(kidx), np.concatenate(kbits)
+    vidx = np.concatenate([tq.tq_unpack_indices(Vc, blk * cap, seq) for blk in range(B * Hkv)])
+    kn = Kc.norm.cpu().numpy().reshape(B * Hkv, cap)[:, :seq].reshape(-1).astype(np.float64)
+    kg = Kc.rnorm.cpu().numpy()[:B * Hkv * cap].reshape(B * Hkv, cap)[:, :seq].reshape(-1).astype(np.float64)
+    vn = Vc.norm.cpu().numpy().reshape(B * Hkv, cap)[:, :seq].reshape(-1).astype(np.float64)
+    cbk, cbv = oracle_codebook(d, b_k - 1), oracle_codebook(d, b_v)
+    Khat = oq.prod_dequantize(kidx, kn, kbits, kg, Pi_k, S, cbk["centroids"], math.sqrt(d)).reshape(B, Hkv, seq, d)
+    Vhat = oatt.dequantize_cache(vidx, vn, Pi_v, cbv["centroids"], math.sqrt(d), B, Hkv, seq)
+    qref = q.float().cpu().numpy().astype(np.float64)
+    ref = oatt.decode_attention(qref, Khat, Vhat, scale)
+    got = out.cpu().numpy().astype(np.float64)
+    rel = np.linalg.norm(got - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
+    assert rel.max() <= 2e-3, f"max per-head relative error {rel.max()}"
+    # the QJL term matters: attention over the MSE part alone is measurably different
+    Kmse = oq.mse_dequantize(kidx, kn, Pi_k, cbk["centroids"], math.sqrt(d)).reshape(B, Hkv, seq, d)
+    alt = oatt.decode_attention(qref, Kmse, Vhat, scale)
+    assert np.linalg.norm(alt - ref) > 10 * np.linalg.norm(got - ref)
+    return rel.max()
+
+
+@pytest.mark.parametrize("b_k,b_v,B,Hq,Hkv,seq", [
+    (3, 3, 1, 32, 8, 4096),   # GQA 4, the config-2 head shape
+    (4, 2, 2, 8, 4, 1000),    # ragged tail, two batches
+    (2, 4, 1, 4, 4, 33),      # GQA 1, a few tiles
+    (3, 2, 1, 16, 8, 777),    # GQA 2
+])
+def test_decode_prod_keys(b_k, b_v, B, Hq, Hkv, seq):
+    run_decode_prod(b_k, b_v, B, Hq, Hkv, seq)
+
+
+def test_decode_prod_keys_rejected_where_unsupported():
+    """Prod keys: no fused append (the step encodes MSE keys only) and at most
+    4 query heads per KV head."""
+    d, seq, cap = 128, 64, 64
+    kctx, _, _ = make_pair(3, d, 3, tq.TQ_PROD)
+    vctx, _, _ = make_pair(4, d, 3)
+    Kc = tq.CodeSet(kctx, 8 * cap, tq.TQ_LAYOUT_TOKEN)
+    Vc = tq.CodeSet(vctx, 8 * cap, tq.TQ_LAYOUT_PAIR)
+    ws = torch.zeros(tq.tq_decode_workspace_size(kctx, 1, 64, 8, seq) // 4 + 4, dtype=torch.float32, device="cuda")
+    q = torch.zeros((1, 64, d), dtype=torch.float16, device="cuda")
+    out = torch.empty((1, 64, d), dtype=torch.float32, device="cuda")
+    with pytest.raises(tq.TqError) as err:  # GQA 8
+        tq.tq_decode_attention(kctx, vctx, q, Kc, Vc, 1, 64, 8, seq, cap, 1 / math.sqrt(d), out, ws)
+    assert err.value.status == tq.TQ_ERR_UNSUPPORTED
+    q4 = torch.zeros((1, 32, d), dtype=torch.float16, device="cuda")
+    out4 = torch.empty((1, 32, d), dtype=torch.float32, device="cuda")
+    kn = torch.zeros((8, d), dtype=torch.float16, device="cuda")
+    with pytest.raises(tq.TqError) as err:  # fused append
+        tq.tq_decode_step(kctx, vctx, q4, kn, kn, Kc, Vc, 1, 32, 8, seq, cap, 1 / math.sqrt(d), out4, ws)
+    assert err.value.status == tq.TQ_ERR_UNSUPPORTED
+
+
 # ------------------------------------------------------------------ full sizes
 def test_prod_full_config3_sampled():
     """1M unit-norm keys, 64 queries, Prod b=3: encode and scores at full size,
