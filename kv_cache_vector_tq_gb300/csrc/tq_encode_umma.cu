@@ -141,21 +141,6 @@ __global__ void __launch_bounds__(256) row_norm_kernel(const void* x, int64_t N,
 }
 
 // ------------------------------------------------------------------ pass 2 helpers
-// Bounded wait on an mbarrier phase; gives up when another thread aborted.
-__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
-  for (uint32_t n = 0;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63u) == 63u) {
-      if (*abort_flag) return false;
-      if (n > kSpinLimitDev) {
-        *abort_flag = 1;
-        atomicOr(status, 1);
-        return false;
-      }
-    }
-  }
-}
-
 // code = #{k : v >= t_k} by binary search over thr (2^BM - 1 thresholds,
 // padded with +inf to 16); near = v lies within m of a neighbouring threshold.
 template <int BM>

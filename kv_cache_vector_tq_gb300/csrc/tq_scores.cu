@@ -1,19 +1,41 @@
-// Inner-product scores over TurboQuant codes (d = 128).
+// Inner-product scores over TurboQuant codes (d = 128), on the fifth-generation
+// tensor cores.
 //
 // "sub-byte-kv-cache-quantization-turboquant", section 工程实现的关键路径: the
 // query is rotated once (q̂ = Π·q) so that each key costs a table lookup and a
-// dot product.  Here the dot products of a 16-key tile with up to 64 queries
-// run on tensor cores (mma.m16n8k16): the A operand is built in registers from
-// the packed codes through a shared-memory pair table (two coordinates per
-// lookup, fp16 values α·c_k), the B operand is q̂/α.
+// dot product:
 //   MSE : score = s · ⟨q̂, ŷ⟩ = s · Σ_i q̂_i c[idx_i] / √d
 //   Prod: + s · γ · √(π/2)/d · Σ_j (S q)_j (2·bit_j − 1)        ("TurboQuant 详解",
 //         section TurboQuant_prod; "turboquant-first-principles-walkthrough",
-//         section 内积偏差问题与 QJL 修正器), with ±1 A operands built from the
-//         sign bits.
-// Lane t of each quad reads the 32 consecutive coordinates 32t..32t+31 of its
-// two keys (whole words); the MMA K index is permuted to match:
-//   K index 16s + 8h + 2t + e  <->  coordinate 32t + 4s + 2h + e.
+//         section 内积偏差问题与 QJL 修正器).
+//
+// Both sums are contractions over the same 128-wide K: the A row of a key is
+// [α·c[idx_i] for its 128 coordinates | ±1 for its 128 sign bits] in fp16 (one
+// operand of K = 256), the B row of a query [q̂_i/α | (S q)_j] in fp16; the two
+// halves of K accumulate into separate tensor-memory columns, D_mse and D_qjl,
+// so that γ is applied exactly in the epilogue:
+//   score = s/√d · (D_mse + γ·√(π/2)/√d · D_qjl).
+//
+// Two launches per 64 queries.
+//  1. scores_qprep_kernel: q̂/α and S·q per query (warp-wide row dot products),
+//     written as the B operand in the tensor cores' K-major core-matrix order.
+//  2. scores_kernel: a persistent CTA per SM walks tiles of 128 keys:
+//       warps 0-3  decode: thread = key; codes and sign words straight from
+//                  global memory (one tile ahead in registers), pair-table
+//                  lookups (two codes per lookup), A rows written into one of
+//                  two shared-memory stages
+//       warp 4     issues 16 (MSE: 8) tcgen05.mma of M = 128 keys, N = the
+//                  queries (up to 64), K = 16 into one of four accumulator
+//                  pairs (D_mse, D_qjl: 2 x 64 columns) in tensor memory
+//       warps 5-12 epilogue, two groups of four on alternating tiles: thread =
+//                  key; reads all 64 results, returns the accumulator pair,
+//                  then s/√d·(D_mse + γ'·D_qjl) as one coalesced 128-byte
+//                  streaming store per query per warp (measured faster than
+//                  16-byte stores after a quad transpose, and than rows staged
+//                  in shared memory for the bulk-copy engine); one group's
+//                  stores overlap the other's tensor-memory reads.
+// 13 warps: the register file is split over the four SM sub-partitions, so a
+// block of more than 16 warps could not have 128 registers per thread.
 #include <algorithm>
 
 #include "tq_device.cuh"
@@ -21,14 +43,25 @@
 
 namespace tq {
 
-constexpr int kQTile = 64;  // queries per launch of the scan kernel
+namespace {
 
-// Query preparation, one block (8 warps) per query: q̂ = Π·q / α and, for
-// Prod, S·q, computed with coalesced float4 row loads (warp w: rows
-// 16w..16w+15), then written as B fragments (uint2 per lane):
-//   b0 = (K index 16s+2t.., col g), b1 = (16s+8+2t.., col g),
-//   K index 16s+8h+2t+e <-> coordinate 32t+4s+2h+e, query = 8·tile + g.
-// ws layout: [mse | qjl] x [qtile][kstep][lane] uint2.
+constexpr int kQTile = 64;       // queries per scan launch (MMA N)
+constexpr int kKeyTile = 128;    // keys per tile (MMA M, TMEM lanes)
+constexpr int kK = 256;          // contraction: 128 coordinates + 128 sign bits
+constexpr int kAStage = kKeyTile * kK * 2;  // 64 KB
+constexpr int kBBytes = kQTile * kK * 2;    // 32 KB
+constexpr int kSbo = (kK / 8) * 128;        // bytes between 8-row groups of an operand
+constexpr int kAccBufs = 4;                 // accumulator pairs (D_mse, D_qjl) in tensor memory
+constexpr int kAccCols = 2 * kQTile;        // columns per pair
+constexpr int kThreads = 13 * 32;
+
+// Byte offset of element (row r, K index k) in a K-major core-matrix operand
+// with kK columns: 8x8 core matrices of 128 bytes, 128 bytes apart along K,
+// kSbo bytes apart along the rows.
+__host__ __device__ constexpr int core_off(int r, int k) {
+  return (r >> 3) * kSbo + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
 __device__ __forceinline__ float warp_dot4(float4 a, float4 b) {
   float x = a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
 #pragma unroll
@@ -36,9 +69,11 @@ __device__ __forceinline__ float warp_dot4(float4 a, float4 b) {
   return x;
 }
 
+// Query preparation, one block (8 warps, rows 16w..16w+15) per query: the B
+// row [q̂/α | S·q] of query m in tile m/64, fp16, core-matrix order (zeros for
+// the rows m >= M that pad the last tile).
 __global__ void __launch_bounds__(256) scores_qprep_kernel(const DevCtx c, const float* __restrict__ q, int M,
-                                                           uint2* __restrict__ frag_mse,
-                                                           uint2* __restrict__ frag_qjl) {
+                                                           unsigned char* __restrict__ btiles) {
   const int m = blockIdx.x;
   __shared__ float qs[128], qr[128], sq[128];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -66,176 +101,261 @@ __global__ void __launch_bounds__(256) scores_qprep_kernel(const DevCtx c, const
     }
   }
   __syncthreads();
-  if (tid < 32) {
-    const int s = tid >> 2, t = tid & 3, g = m & 7, nt = m >> 3;
-    const int ln = 4 * g + t;
-    const int c0 = 32 * t + 4 * s, c1 = c0 + 2;
-    uint2 f;
-    f.x = pack_f16x2(qr[c0], qr[c0 + 1]);
-    f.y = pack_f16x2(qr[c1], qr[c1 + 1]);
-    frag_mse[((size_t)nt * 8 + s) * 32 + ln] = f;
-    if (prod) {
-      f.x = pack_f16x2(sq[c0], sq[c0 + 1]);
-      f.y = pack_f16x2(sq[c1], sq[c1 + 1]);
-      frag_qjl[((size_t)nt * 8 + s) * 32 + ln] = f;
-    }
+  unsigned char* tile = btiles + (size_t)(m / kQTile) * kBBytes;
+  const int row = m % kQTile;
+  if (tid < kK / 2) {  // thread: K index pair 2·tid, 2·tid + 1
+    const int k = 2 * tid;
+    const float x0 = k < 128 ? qr[k] : (prod ? sq[k - 128] : 0.f);
+    const float x1 = k < 128 ? qr[k + 1] : (prod ? sq[k - 127] : 0.f);
+    *reinterpret_cast<uint32_t*>(tile + core_off(row, k)) = pack_f16x2(x0, x1);
   }
 }
 
 struct ScoreParams {
-  DevCtx c;
   const uint32_t* codes;
   const float* norm;
   const uint32_t* qjl;
   const float* rnorm;
+  const uint32_t* lut;  // pair table: 2^(2b) fp16x2 entries α·c_k
   int64_t first, N;
   int W, QW;
-  const uint2* frag_mse;  // this launch's query tiles
-  const uint2* frag_qjl;
-  int m0, mq;             // first query, queries in this launch (<= 64)
-  int M;                  // total queries (row count of scores)
+  const unsigned char* btile;  // this launch's B operand (kBBytes)
+  int m0, mq;                  // first query, queries in this launch (<= 64)
+  float inv_sd;                // 1/√d
+  float gscale;                // √(π/2)/√d: γ' = γ·gscale
   float* scores;
+  int* status;
 };
 
 template <int BM, bool PROD>
-__global__ void __launch_bounds__(256, 2) scores_kernel(const ScoreParams p) {
-  extern __shared__ uint32_t sh[];
+__global__ void __launch_bounds__(kThreads, 1) scores_kernel(const ScoreParams p) {
   constexpr int E = 1 << (2 * BM);
-  uint32_t* lut = sh;                             // [E][32] replicated per lane
-  uint2* fm = reinterpret_cast<uint2*>(sh + E * 32);  // [8 qtiles][8 ksteps][32]
-  uint2* fq = fm + 8 * 8 * 32;
-  const int nqt = (p.mq + 7) >> 3;
-  for (int i = threadIdx.x; i < E * 32; i += blockDim.x) lut[i] = p.c.lut[i >> 5];
-  for (int i = threadIdx.x; i < nqt * 8 * 32; i += blockDim.x) {
-    fm[i] = p.frag_mse[i];
-    if (PROD) fq[i] = p.frag_qjl[i];
-  }
-  __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const uint32_t* mylut = lut + lane;
-  const float inv_sd = 1.f / p.c.sqrt_d;
-  const float qjl_c = 1.2533141373155001f / (float)p.c.d;  // √(π/2)/d
-  const int64_t ntile = (p.N + 15) >> 4;
-  for (int64_t tile = (int64_t)blockIdx.x * 8 + warp; tile < ntile; tile += (int64_t)gridDim.x * 8) {
-    const int64_t k0 = tile * 16 + g, k1 = k0 + 8;
-    const bool h0 = k0 < p.N, h1 = k1 < p.N;
-    uint32_t w0[BM], w1[BM];
-#pragma unroll
-    for (int w = 0; w < BM; ++w) {
-      w0[w] = h0 ? __ldcs(p.codes + (p.first + k0) * p.W + t * BM + w) : 0u;
-      w1[w] = h1 ? __ldcs(p.codes + (p.first + k1) * p.W + t * BM + w) : 0u;
-    }
-    uint32_t qb0 = 0, qb1 = 0;
-    float g0 = 0.f, g1 = 0.f;
-    if (PROD) {
-      qb0 = h0 ? __ldcs(p.qjl + (p.first + k0) * p.QW + t) : 0u;
-      qb1 = h1 ? __ldcs(p.qjl + (p.first + k1) * p.QW + t) : 0u;
-      g0 = h0 ? p.rnorm[p.first + k0] : 0.f;
-      g1 = h1 ? p.rnorm[p.first + k1] : 0.f;
-    }
-    const float s0 = h0 ? p.norm[p.first + k0] : 0.f;
-    const float s1 = h1 ? p.norm[p.first + k1] : 0.f;
-    float acc[8][4], acq[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[n][e] = acq[n][e] = 0.f;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t a0 = mylut[get_bits<2 * BM>(w0, 4 * s * BM) << 5];
-      const uint32_t a1 = mylut[get_bits<2 * BM>(w1, 4 * s * BM) << 5];
-      const uint32_t a2 = mylut[get_bits<2 * BM>(w0, (4 * s + 2) * BM) << 5];
-      const uint32_t a3 = mylut[get_bits<2 * BM>(w1, (4 * s + 2) * BM) << 5];
-      uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
-      if (PROD) {
-        // ±1 from sign bits: bit 1 -> +1 (0x3C00), bit 0 -> -1 (0xBC00)
-        const uint32_t y0 = ~(qb0 >> (4 * s)), y1 = ~(qb1 >> (4 * s));
-        c0 = 0x3C003C00u | ((y0 & 1u) << 15) | ((y0 & 2u) << 30);
-        c1 = 0x3C003C00u | ((y1 & 1u) << 15) | ((y1 & 2u) << 30);
-        c2 = 0x3C003C00u | ((y0 & 4u) << 13) | ((y0 & 8u) << 28);
-        c3 = 0x3C003C00u | ((y1 & 4u) << 13) | ((y1 & 8u) << 28);
-      }
-#pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        if (n < nqt) {
-          const uint2 b = fm[(n * 8 + s) * 32 + lane];
-          mma16816(acc[n], a0, a1, a2, a3, b.x, b.y);
-          if (PROD) {
-            const uint2 bq = fq[(n * 8 + s) * 32 + lane];
-            mma16816(acq[n], c0, c1, c2, c3, bq.x, bq.y);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      if (n < nqt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int qi = 8 * n + 2 * t + (e & 1);
-          const bool hi = e >= 2;
-          const int64_t key = hi ? k1 : k0;
-          if (qi < p.mq && key < p.N) {
-            const float s = hi ? s1 : s0;
-            float v = acc[n][e] * inv_sd;
-            if (PROD) v = fmaf((hi ? g1 : g0) * qjl_c, acq[n][e], v);
-            p.scores[(int64_t)(p.m0 + qi) * p.N + key] = s * v;
-          }
-        }
-      }
-    }
-  }
-}
+  constexpr int KS = PROD ? kK / 16 : 128 / 16;  // MMAs per tile
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* sA = smem;                        // 2 stages
+  unsigned char* sB = smem + 2 * kAStage;
+  uint32_t* lut = reinterpret_cast<uint32_t*>(sB + kBBytes);  // [E][32] replicated per lane
+  uint64_t* bars = reinterpret_cast<uint64_t*>(lut + E * 32);
+  uint64_t* a_full = bars;              // [2] 4 decode warps
+  uint64_t* a_empty = bars + 2;         // [2] MMA commit
+  uint64_t* acc_full = bars + 4;        // [4] MMA commit
+  uint64_t* acc_empty = bars + 8;       // [4] the 4 warps of one epilogue group
+  uint64_t* b_full = bars + 12;         // the B operand's bulk copy
+  uint64_t* drain = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-size_t scores_ws_bytes(const DevCtx& c, int M) {
-  size_t tiles = (size_t)(M + 7) / 8;
-  return tiles * 8 * 32 * sizeof(uint2) * 2 + 256;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t ntiles = (p.N + kKeyTile - 1) / kKeyTile;
+
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&a_full[s], 4);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(b_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = tid; i < E * 32; i += kThreads) lut[i] = __ldg(p.lut + (i >> 5));
+  if (warp == 0) tmem_alloc(tmem_slot, kAccBufs * kAccCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(b_full, kBBytes);
+    bulk_g2s(sB, p.btile, kBBytes, b_full);
+  }
+
+  if (warp < 4) {
+    // ---------------- decode: key r = 32·warp + lane of the tile, all 128 coordinates
+    const int r = 32 * warp + lane;
+    const uint32_t* mylut = lut + lane;
+    constexpr int CW = 4 * BM;  // code words of a key
+    uint32_t cw[CW], sw[4];
+    auto fetch = [&](int64_t tile) {
+      const int64_t key = tile * kKeyTile + r;
+      const bool ok = key < p.N;
+      const int64_t v = p.first + key;
+#pragma unroll
+      for (int w = 0; w < CW; ++w) cw[w] = ok ? __ldg(p.codes + v * p.W + w) : 0u;
+      if constexpr (PROD) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) sw[w] = ok ? __ldg(p.qjl + v * p.QW + w) : 0u;
+      }
+    };
+    uint32_t i = 0;
+    int64_t t = blockIdx.x;
+    if (t < ntiles) fetch(t);
+    for (; t < ntiles; t += gridDim.x, ++i) {
+      uint32_t c[CW], sb[4];
+#pragma unroll
+      for (int w = 0; w < CW; ++w) c[w] = cw[w];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) sb[w] = sw[w];
+      if (t + gridDim.x < ntiles) fetch(t + gridDim.x);  // next tile's words in flight
+      const uint32_t s = i & 1u;
+      if (!__all_sync(kFull, bar_wait(&a_empty[s], ((i >> 1) & 1u) ^ 1u, abort_flag, p.status))) break;
+      unsigned char* A = sA + s * kAStage;
+      // 128 coordinates = 16 core rows of 8 fp16 (pairs from the table)
+#pragma unroll
+      for (int k8 = 0; k8 < 16; ++k8) {
+        uint32_t v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = mylut[get_bits<2 * BM>(c, (8 * k8 + 2 * e) * BM) << 5];
+        *reinterpret_cast<uint4*>(A + core_off(r, 8 * k8)) = make_uint4(v[0], v[1], v[2], v[3]);
+      }
+      if constexpr (PROD) {  // ±1 for 128 sign bits
+#pragma unroll
+        for (int k8 = 0; k8 < 16; ++k8) {
+          const uint32_t byte = (sb[k8 >> 2] >> (8 * (k8 & 3))) & 0xFFu;
+          uint32_t v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)  // −1 in both halves; bit 1 flips its half to +1
+            v[e] = 0xBC00BC00u ^ (((byte >> (2 * e)) & 1u) << 15) ^ (((byte >> (2 * e + 1)) & 1u) << 31);
+          *reinterpret_cast<uint4*>(A + core_off(r, 128 + 8 * k8)) = make_uint4(v[0], v[1], v[2], v[3]);
+        }
+      }
+      fence_proxy_async();  // generic-proxy stores, read next by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full[s]);
+    }
+  } else if (warp == 4) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_f16(kKeyTile, kQTile);
+      bool ok = bar_wait(b_full, 0u, abort_flag, p.status);
+      const uint32_t bbase = smem_u32(sB);
+      uint32_t i = 0;
+      for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++i) {
+        const uint32_t s = i & 1u, b = i % kAccBufs;
+        if (!bar_wait(&acc_empty[b], ((i / kAccBufs) & 1u) ^ 1u, abort_flag, p.status) ||
+            !bar_wait(&a_full[s], (i >> 1) & 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t abase = smem_u32(sA + s * kAStage);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)  // K steps 0-7 into D_mse, 8-15 into D_qjl
+          umma_f16(tmem + b * kAccCols + (ks >= 8 ? kQTile : 0), umma_desc(abase + ks * 256, 128, kSbo),
+                   umma_desc(bbase + ks * 256, 128, kSbo), idesc, (ks & 7) > 0 ? 1u : 0u);
+        umma_commit(&a_empty[s]);
+        umma_commit(&acc_full[b]);
+      }
+      umma_commit(drain);  // every MMA issued completes before tensor memory is released
+      for (uint32_t n = 0; n < kSpinLimitDev && !mbar_try_wait(drain, 0u); ++n) {
+      }
+    }
+  } else {
+    // ---------------- epilogue: group grp takes tiles i ≡ grp (mod 2); thread = key
+    //                  (TMEM lane 32·(warp % 4) + lane)
+    const int grp = (warp - 5) >> 2, q4 = warp & 3, r = 32 * q4 + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    uint32_t i = grp;
+    for (int64_t t = blockIdx.x + (int64_t)grp * gridDim.x; t < ntiles; t += 2 * (int64_t)gridDim.x, i += 2) {
+      const uint32_t b = i % kAccBufs;
+      const int64_t key = t * kKeyTile + r;
+      const bool ok = key < p.N;
+      const float sc = ok ? __ldg(p.norm + p.first + key) * p.inv_sd : 0.f;
+      const float gq = (PROD && ok) ? __ldg(p.rnorm + p.first + key) * p.gscale : 0.f;
+      if (!__all_sync(kFull, bar_wait(&acc_full[b], (i / kAccBufs) & 1u, abort_flag, p.status))) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + lane_base + b * kAccCols;
+      float* out = p.scores + (int64_t)p.m0 * p.N + key;
+      float o0[32];  // queries 0-31, stored once the pair is returned
+      uint32_t dm[32], dq[32];
+      tmem_ld32_nw(acc, dm);
+      if constexpr (PROD) tmem_ld32_nw(acc + kQTile, dq);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        o0[j] = sc * (PROD ? fmaf(gq, __uint_as_float(dq[j]), __uint_as_float(dm[j])) : __uint_as_float(dm[j]));
+      tmem_ld32_nw(acc + 32, dm);  // queries 32-63
+      if constexpr (PROD) tmem_ld32_nw(acc + kQTile + 32, dq);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      if (ok) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (32 + j < p.mq)
+            __stcs(out + (int64_t)(32 + j) * p.N,
+                   sc * (PROD ? fmaf(gq, __uint_as_float(dq[j]), __uint_as_float(dm[j])) : __uint_as_float(dm[j])));
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < p.mq) __stcs(out + (int64_t)j * p.N, o0[j]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kAccBufs * kAccCols);
+  }
 }
 
 template <int BM, bool PROD>
-static cudaError_t run_scores(ScoreParams p, cudaStream_t st) {
+cudaError_t run_scores(const ScoreParams& p, cudaStream_t st) {
   constexpr int E = 1 << (2 * BM);
-  const size_t smem = (size_t)E * 32 * 4 + 2 * 8 * 8 * 32 * sizeof(uint2);
+  constexpr size_t smem = 2 * kAStage + kBBytes + E * 32 * 4 + 256;
   auto k = scores_kernel<BM, PROD>;
-  static int attr_done = 0;  // set once, outside any later stream capture
+  static bool attr_done = false;  // set once, outside any later stream capture
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attr_done = 1;
+    attr_done = true;
   }
-  const int64_t tiles = (p.N + 15) / 16;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((tiles + 7) / 8, (int64_t)num_sms() * 4));
-  k<<<grid, 256, smem, st>>>(p);
+  const int64_t tiles = (p.N + kKeyTile - 1) / kKeyTile;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms()));
+  k<<<grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t scores_ws_bytes(const DevCtx& c, int M) {
+  (void)c;
+  return (size_t)((M + kQTile - 1) / kQTile) * kBBytes + 256;
 }
 
 tq_status launch_scores(const DevCtx& c, const float* q, int M, const tq_codes* keys, int64_t first,
                         int64_t N, float* scores, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  const size_t tiles = (size_t)(M + 7) / 8;
-  uint2* fm = static_cast<uint2*>(ws);
-  uint2* fq = fm + tiles * 8 * 32;
-  scores_qprep_kernel<<<(int)(tiles * 8), 256, 0, stream>>>(c, q, M, fm, fq);
+  if (c.d != 128) return TQ_ERR_UNSUPPORTED;
+  if (ws_bytes < scores_ws_bytes(c, M)) return TQ_ERR_INVALID_ARG;
+  unsigned char* bt = static_cast<unsigned char*>(ws);
+  const int nqt = (M + kQTile - 1) / kQTile;
+  scores_qprep_kernel<<<nqt * kQTile, 256, 0, stream>>>(c, q, M, bt);  // rows past M written as zeros
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e);
   ScoreParams p;
-  p.c = c;
   p.codes = keys->d_codes;
   p.norm = keys->d_norm;
   p.qjl = keys->d_qjl;
   p.rnorm = keys->d_rnorm;
+  p.lut = c.lut;
   p.first = first;
   p.N = N;
   p.W = c.words_per_vec;
   p.QW = c.qjl_words_per_vec;
-  p.M = M;
+  p.inv_sd = 1.f / c.sqrt_d;
+  p.gscale = (float)(1.2533141373155002 / std::sqrt((double)c.d));
   p.scores = scores;
+  p.status = c.status;
   const bool prod = c.mode == TQ_PROD;
   for (int m0 = 0; m0 < M; m0 += kQTile) {
     p.m0 = m0;
     p.mq = std::min(kQTile, M - m0);
-    p.frag_mse = fm + (size_t)(m0 / 8) * 8 * 32;
-    p.frag_qjl = fq + (size_t)(m0 / 8) * 8 * 32;
+    p.btile = bt + (size_t)(m0 / kQTile) * kBBytes;
     switch (c.b_mse) {
       case 1: e = prod ? run_scores<1, true>(p, stream) : run_scores<1, false>(p, stream); break;
       case 2: e = prod ? run_scores<2, true>(p, stream) : run_scores<2, false>(p, stream); break;
