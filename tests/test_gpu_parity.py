@@ -228,6 +228,47 @@ def test_scores_mse_bits_and_ragged(b):
     _scores_check(ctx, Pi, None, X, Q, b, False)
 
 
+@pytest.mark.parametrize("first,N,M,prod", [
+    (0, 1, 1, False),       # one key, one query
+    (37, 100, 3, True),     # a key range inside the code set, less than one 128-key tile
+    (5, 1000, 130, True),   # three query launches (64, 64, 2), ragged last key tile
+    (0, 4096, 64, False),   # whole tiles, a full query launch
+])
+def test_scores_key_ranges_and_query_counts(first, N, M, prod):
+    """Scores over keys [first, first + N) of a larger code set: tiny and
+    ragged key counts, key counts that are not multiples of 4, more than one
+    64-query launch."""
+    d = 128
+    mode = tq.TQ_PROD if prod else tq.TQ_MSE
+    b = 3
+    ctx, Pi, S = make_pair(21, d, b, mode)
+    total = first + N + 11
+    X = synth.unit_rows(21, total, d) if prod else synth.gaussian_rows(21, total, d, outlier_cols=4, outlier_scale=20.0)
+    cs = gpu_encode(ctx, X)
+    Q = synth.queries(21, M, d)
+    q = torch.from_numpy(np.ascontiguousarray(Q)).cuda()
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(tq.tq_scores_workspace_size(ctx, M) // 4 + 4, dtype=torch.float32, device="cuda")
+    tq.tq_scores(ctx, q, cs, out, ws, first=first, N=N)
+    torch.cuda.synchronize()
+    assert ctx.poll() == tq.TQ_OK
+    b_mse = b - 1 if prod else b
+    cb = oracle_codebook(d, b_mse)
+    s = cs.norm[first:first + N].cpu().numpy().astype(np.float64)
+    if prod:
+        idx, bits = tq.tq_unpack_indices(cs, first, N, with_bits=True)
+        gam = cs.rnorm[first:first + N].cpu().numpy().astype(np.float64)
+        ref = oatt.prod_scores(Q.astype(np.float64), idx, s, bits, gam, Pi, S, cb["centroids"], math.sqrt(d))
+    else:
+        idx = tq.tq_unpack_indices(cs, first, N)
+        ref = oatt.mse_scores(Q.astype(np.float64), idx, s, Pi, cb["centroids"], math.sqrt(d))
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()  # every (query, key) written, nothing outside
+    Xs = X[first:first + N].astype(np.float64)
+    bound = 1e-4 * np.linalg.norm(Q, axis=1)[:, None] * np.linalg.norm(Xs, axis=1)[None, :]
+    assert (np.abs(got - ref) <= bound).all()
+
+
 def test_scores_prod_config3_sample():
     ctx, Pi, S = make_pair(0, 128, 3, tq.TQ_PROD)
     X = synth.unit_rows(0, 8192, 128)
