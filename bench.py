@@ -187,6 +187,7 @@ def run_tq(args, world, rank, local):
     import torch
 
     import kv_cache_vector_tq_gb300 as tq
+    from bench_workloads import traffic
     from kv_cache_vector_tq_gb300 import synth
 
     torch.cuda.set_device(local)
@@ -317,7 +318,8 @@ def run_tq(args, world, rank, local):
         },
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None,
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic(os.path.dirname(os.path.abspath(__file__)), f"decode_b{bits}"),
             "kernel": "decode_step_kernel without the append (one launch per call)", "peak_kind": peak_kind,
             "us_per_call": round(attn_us, 3), "bytes_per_call": attn_bytes,
         },

@@ -35,6 +35,29 @@ def _peaks(root):
         return 6800.0, 1900.0, "fallback"
 
 
+def traffic(root, key):
+    """DRAM bytes (read + write) of one launch of the kernel recorded under
+    `key` in profiles/traffic.md, or None when no row matches or the kernel's
+    source file has changed since that capture (its SHA-256 differs)."""
+    import hashlib
+    try:
+        with open(os.path.join(root, "profiles", "traffic.md")) as f:
+            rows = [r.split("|")[1:-1] for r in f.read().splitlines() if r.startswith("| ")]
+    except OSError:
+        return None
+    for r in rows:
+        cells = [c.strip() for c in r]
+        if len(cells) < 5 or cells[0] != key:
+            continue
+        try:
+            with open(os.path.join(root, cells[1]), "rb") as f:
+                digest = hashlib.sha256(f.read()).hexdigest()
+        except OSError:
+            return None
+        return int(cells[3]) + int(cells[4]) if digest == cells[2] else None
+    return None
+
+
 def _timed(fn, steps, warmup, stream, clocks_cls, local, flush=None):
     """W warm-up calls, then K timed calls bracketed by events on `stream`.
     With `flush`, L2 is flushed between calls and only the calls are timed."""
@@ -111,16 +134,21 @@ def run_encode(args, world, rank, local, root, clocks_cls, cpu):
     if rot == "hadamard":
         ach = args.steps * N * bytes_per_vec / sec / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
-                "traffic": None, "kernel": "encode_wht_kernel", "peak_kind": kind,
+                "traffic": traffic(root, f"encode_wht_d{d}_n{N // 1000}k"), "kernel": "encode_wht_kernel",
+                "peak_kind": kind,
                 "bytes_per_vector": bytes_per_vec}
     else:
         ach = args.steps * 2.0 * N * d * d / sec / 1e12  # useful flops of Y = X·Πᵀ
         peak = bf16 / 3.0  # fp32-accurate products: three fp16 tensor passes (hi·hi, lo·hi, hi·lo)
         roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4), "traffic": None, "kernel": "encode_umma_kernel",
+                "frac": round(ach / peak, 4), "traffic": traffic(root, f"encode_dense_d{d}_n{N // 1000}k"),
+                "kernel": "encode_umma_kernel",
                 "peak_kind": f"{kind} bf16 dense / 3 split passes (fp16 hi/lo, same tensor rate as bf16)",
                 "passes": 3, "flops_per_vector": 2 * d * d,
                 "timed": "whole tq_encode call (row_norm_kernel + encode_umma_kernel)"}
+    # kernels per tq_encode call: the Hadamard kernel alone, or the norm pass and
+    # the tensor-core kernel (d > 128, a multiple of 128), or one dense kernel
+    launches = 2 if rot == "dense" and d > 128 and d % 128 == 0 else 1
     # end to end: rows from pinned host memory, codes and norms back, per call
     e2e = None
     if N * d * 4 <= (2 << 30):
@@ -147,7 +175,7 @@ def run_encode(args, world, rank, local, root, clocks_cls, cpu):
                  {"workload": f"bulk indexing encode, TurboQuant_MSE b=4, d={d}, N={N}, {rot} rotation",
                   "d": d, "rows": N, "bits": bits, "rotation": rot,
                   "l2": f"inputs larger than L2: {N * d * 4 / 1e9:.2f} GB of rows per step"},
-                 roof, e2e, args.steps, clk)
+                 roof, e2e, args.steps * launches, clk)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu["encode"](d, bits, rot, rotm)
     return line if rank == 0 else None
@@ -184,7 +212,7 @@ def run_scores(args, world, rank, local, root, clocks_cls, cpu):
     bytes_call = N * (32 + 16 + 4 + 4) + M * N * 4
     ach = args.steps * bytes_call / sec / 1e9
     roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
-            "traffic": None, "kernel": "scores_kernel (Prod)", "peak_kind": kind, "bytes_per_call": bytes_call}
+            "traffic": traffic(root, "scores_prod_b3"), "kernel": "scores_kernel (Prod)", "peak_kind": kind, "bytes_per_call": bytes_call}
     qh = q.cpu().pin_memory()
     oh = torch.empty((M, N), dtype=torch.float32).pin_memory()
     reps = max(3, min(args.steps, 10))
@@ -282,7 +310,8 @@ def run_longctx(args, world, rank, local, root, clocks_cls, cpu):
                   "prefill_encode_gbs": round(enc_vecs * (D * 2 + D * bits // 8 + 4) / (enc_ms * 1e-3) / 1e9, 1),
                   "ms_per_layer": round(total_ms / args.steps / L, 4)},
                  {"bound": "hbm", "achieved": round(gbs / world, 1), "peak": hbm, "unit": "GB/s",
-                  "frac": round(gbs / world / hbm, 4), "traffic": None, "kernel": "decode_step_kernel<3,3,8,8>",
+                  "frac": round(gbs / world / hbm, 4), "traffic": traffic(root, "longctx_b3"),
+                  "kernel": "decode_step_kernel<3,3,8,8>",
                   "peak_kind": kind, "bytes_per_step": step_bytes},
                  None, args.steps * L, clk)
     return line if rank == 0 else None
