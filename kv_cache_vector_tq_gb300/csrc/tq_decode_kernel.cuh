@@ -894,11 +894,11 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     }
     __syncthreads();
     if (tid == 0) {
-      __threadfence();  // releases the CTA's stores above (ordered by the barrier)
-      const int old = atomicAdd(p.counters + grp, 1);
+      // releases the CTA's stores above (ordered by the barrier); the last
+      // arrival acquires everyone else's
+      const int old = atomic_add_acq_rel(p.counters + grp, 1);
       const int last = old == p.S - 1;
       if (last) p.counters[grp] = 0;  // ready for the next call
-      __threadfence();
       *flag = last;
     }
     __syncthreads();

@@ -237,6 +237,14 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 __device__ __forceinline__ void griddep_launch() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
+// Atomic add with acquire-release semantics at GPU scope: the CTA's writes
+// ordered before it (by a barrier) are visible to whoever observes the new
+// count, and writes of earlier arrivals are visible after it.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 // Shared-window address of a lane's copy of table entry `byte k of w`, for
 // tables laid out as 256-byte rows (one row per index, 4-byte entries at
 // lane·4): byte 0 = lane·4, byte 1 = byte k of w, upper bytes zero.
