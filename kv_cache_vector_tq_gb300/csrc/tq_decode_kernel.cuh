@@ -608,6 +608,16 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
   }
+  // this warp's rows of Π_V for the output rotation, copied into its own region
+  // (asynchronous: nothing waits on them before the rotation at the end)
+  auto issue_pv = [&]() {
+    float* prow = reinterpret_cast<float*>(my_stage + pi_off(G));
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) cp_async16(prow + r * 128 + 4 * lane, p.vpi + (warp * RPW + r) * 128 + 4 * lane);
+    cp_async_commit();
+  };
+  // issued in the warp's last tile when it has one (Prod keys: after the loop)
+  const bool pv_in_loop = !Q && warp < ntl;
   for (int j = 0; warp + j * W < ntl; ++j) {
     const int tile = t_begin + warp + j * W;
     cp_async_wait<kStages - 1>();
@@ -646,6 +656,9 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     }
     // every lane's words are in registers: refill this stage
     issue(j + kStages);
+    if constexpr (!Q) {  // (Prod keys still read this stage's γ and signs below)
+      if (warp + (j + 1) * W >= ntl) issue_pv();  // the warp's last tile: its region is free now
+    }
     const int lt0 = tile * kTileTok;
     // K side: S = K̂·Q with two independent MMA chains
     float sa[NT][4], sb[NT][4];
@@ -784,14 +797,11 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
       for (int nt = 0; nt < NT; ++nt) mma16816(o[mt][nt], a0, a1, a2, a3, bw[nt][0], bw[nt][1]);
     }
   }
-  cp_async_wait_all();
-  // this warp's rows of Π_V for the output rotation, copied into its own region
-  // while the warps merge (asynchronous: no registers held, nothing waits on them yet)
-  {
-    float* prow = reinterpret_cast<float*>(my_stage + pi_off(G));
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) cp_async16(prow + r * 128 + 4 * lane, p.vpi + (warp * RPW + r) * 128 + 4 * lane);
-    cp_async_commit();
+  if (pv_in_loop) {
+    cp_async_wait<1>();  // every tile copy is done; the Π_V rows may still be in flight
+  } else {
+    cp_async_wait_all();
+    issue_pv();
   }
 
   // ---- 4. merge the warps and rotate back.  Each warp leaves its state in its
