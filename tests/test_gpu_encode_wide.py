@@ -157,10 +157,12 @@ def test_dense_bulk_indexing_full_size_sampled(d):
     check(cs, Pi, X, 4, rows)
 
 
-def test_dense_wide_encode_grouped_destination():
+@pytest.mark.parametrize("d,b", [(256, 4), (384, 1), (384, 3)])
+def test_dense_wide_encode_grouped_destination(d, b):
     """Rows scattered into a larger code set (group_rows / group_stride /
-    offset), as when appending to (batch, head) blocks of a cache."""
-    d, b, n = 256, 4, 200
+    offset), as when appending to (batch, head) blocks of a cache; tiles of
+    128 (d = 256) and 192 (d = 384) output coordinates."""
+    n = 200
     ctx, Pi = haar_pair(14, d, b)
     X = synth.bulk_rows(14, n, d)
     x = torch.from_numpy(X).cuda()
