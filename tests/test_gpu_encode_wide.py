@@ -54,15 +54,20 @@ def encode(ctx, X, dtype=torch.float32):
 
 def check(cs, Pi, X, b, rows=None):
     """Oracle on the (sampled) rows; rows = None means all."""
-    d = X.shape[1]
     rows = np.arange(X.shape[0]) if rows is None else np.asarray(rows)
-    Xs = X[rows].astype(np.float64)
+    return check_rows(cs, Pi, X[rows], rows, b, all_rows=len(rows) == X.shape[0])
+
+
+def check_rows(cs, Pi, Xs, rows, b, all_rows=False):
+    """Oracle on the rows Xs, which the code set holds at indices `rows`."""
+    d = Xs.shape[1]
+    Xs = Xs.astype(np.float64)
     cb = codebook(d, b)
     idx_ref, s_ref, v = oq.mse_quantize(Xs, Pi, cb["centroids"], math.sqrt(d))
     band = oq.near_threshold(v, cb["centroids"])
     band[s_ref == 0.0] = False
-    idx = np.stack([tq.tq_unpack_indices(cs, int(r), 1)[0] for r in rows]) if len(rows) < X.shape[0] \
-        else tq.tq_unpack_indices(cs, 0, X.shape[0])
+    idx = tq.tq_unpack_indices(cs, 0, len(rows)) if all_rows \
+        else np.stack([tq.tq_unpack_indices(cs, int(r), 1)[0] for r in rows])
     mism = (idx.astype(np.int64) != idx_ref) & ~band
     assert not mism.any(), f"{mism.sum()} mismatches outside the band (rows {rows[np.nonzero(mism.any(1))[0][:8]]})"
     # the band is a rare event: on small samples allow a Poisson fluctuation
@@ -187,3 +192,30 @@ def test_wide_encode_rejects_unsupported():
     with pytest.raises(tq.TqError) as err:
         tq.tq_encode(ctx, x, cs)
     assert err.value.status == tq.TQ_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("rot", ["dense", "hadamard"])
+def test_bulk_indexing_ten_million_rows_sampled(rot):
+    """N = 10M rows of the bulk-indexing workload at d = 3072 (123 GB of fp32
+    rows, generated on the device by torch's seeded generator with the
+    workload's distribution: N(0, 1), a seeded 1 % of the rows x50), encoded in
+    one call; 256 random rows plus the first and last are copied back and
+    checked against the oracle."""
+    d, N = 3072, 10_000_000
+    if torch.cuda.mem_get_info()[0] < 150e9:
+        pytest.skip("needs 150 GB of free device memory")
+    ctx, Pi = haar_pair(0, d, 4) if rot == "dense" else hadamard_pair(0, d, 4)
+    gen = torch.Generator(device="cuda").manual_seed(20)
+    x = torch.randn((N, d), generator=gen, device="cuda")
+    x[torch.randperm(N, generator=gen, device="cuda")[: N // 100]] *= 50.0
+    cs = tq.CodeSet(ctx, N, tq.TQ_LAYOUT_TOKEN)
+    tq.tq_encode(ctx, x, cs)
+    torch.cuda.synchronize()
+    assert ctx.poll() == tq.TQ_OK
+    rows = np.concatenate([[0, N - 1], np.random.default_rng(3).choice(N, size=256, replace=False)])
+    Xs = x[torch.from_numpy(rows).cuda()].cpu().numpy()
+    del x
+    torch.cuda.empty_cache()
+    check_rows(cs, Pi, Xs, rows, 4)
+    del cs
+    torch.cuda.empty_cache()
