@@ -144,6 +144,37 @@ __global__ void __launch_bounds__(256, 1) encode_kernel(const EncParams p) {
       ss += __shfl_xor_sync(kFull, ss, 1);
       ss += __shfl_xor_sync(kFull, ss, 2);
       nrm[h] = sqrtf(ss);
+      // squares near or past the ends of the fp32 range (or a zero row): sum
+      // them again with the row scaled by the power of two that brings its
+      // largest magnitude to [1, 2).  The shuffles run on every lane whenever
+      // any lane needs them (the condition differs between rows).
+      const bool need = !(ss > 1e-30f && ss < 1e36f);
+      if (__any_sync(kFull, need)) {
+        float m = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) m = fmaxf(m, fabsf(xv[s][h][q]));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+        float scale = 1.f;
+        if (m > 0.f) {
+          int e;
+          frexpf(m, &e);
+          scale = ldexpf(1.f, 1 - e);
+        }
+        float s2 = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float v = xv[s][h][q] * scale;
+            s2 = fmaf(v, v, s2);
+          }
+        s2 += __shfl_xor_sync(kFull, s2, 1);
+        s2 += __shfl_xor_sync(kFull, s2, 2);
+        if (need) nrm[h] = sqrtf(s2) / scale;
+      }
     }
     // ---------------- a2: rotation on tensor cores
     float sc[2];

@@ -136,6 +136,31 @@ __global__ void __launch_bounds__(256) row_norm_kernel(const void* x, int64_t N,
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+    if (!(ss > 1e-30 && ss < 1e36)) {
+      // squares near or past the ends of the fp32 range (or a zero row): sum
+      // them again with the row scaled by the power of two that brings its
+      // largest magnitude to [1, 2)
+      float m = 0.f;
+      for (int k = lane; k < d; k += 32)
+        m = fmaxf(m, fabsf(F16 ? __half2float(static_cast<const __half*>(x)[r * d + k]) : static_cast<const float*>(x)[r * d + k]));
+#pragma unroll
+      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      if (m > 0.f) {
+        int e;
+        frexpf(m, &e);
+        const float sc = ldexpf(1.f, 1 - e);
+        double s2 = 0.0;
+        for (int k = lane; k < d; k += 32) {
+          const float v = (F16 ? __half2float(static_cast<const __half*>(x)[r * d + k]) : static_cast<const float*>(x)[r * d + k]) * sc;
+          s2 += (double)(v * v);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) s2 += __shfl_xor_sync(kFull, s2, o);
+        ss = s2 / ((double)sc * (double)sc);
+      } else {
+        ss = 0.0;
+      }
+    }
     if (lane == 0) norm[dest_row(r, offset, group_rows, group_stride)] = (float)sqrt(ss);
   }
 }

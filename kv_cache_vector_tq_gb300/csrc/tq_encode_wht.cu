@@ -98,8 +98,8 @@ __global__ void __launch_bounds__(P == 12 ? 384 : 256) encode_wht_kernel(const W
   constexpr int SLOT = VPC * D * ES;    // a ring slot: the CTA's VPC consecutive rows
   extern __shared__ __align__(16) unsigned char wsm[];
   float* zs = reinterpret_cast<float*>(wsm);                    // [D] Paley exchange (P = 12)
-  float* part = zs + (P == 12 ? D : 0);                        // [12] warp norm partials
-  unsigned char* cbuf = reinterpret_cast<unsigned char*>(part + 16);  // [VPC][D] code bytes
+  float* part = zs + (P == 12 ? D : 0);                        // [12] warp norm partials, [16 + 12] rescaled ones
+  unsigned char* cbuf = reinterpret_cast<unsigned char*>(part + 32);  // [VPC][D] code bytes
   unsigned char* ring = cbuf + ((VPC * D + 15) / 16) * 16;
   __shared__ float thr_s[16];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -160,6 +160,38 @@ __global__ void __launch_bounds__(P == 12 ? 384 : 256) encode_wht_kernel(const W
 #pragma unroll
       for (int k = 0; k < E; ++k) x[k] = fmaf(sgn, x[k], __shfl_xor_sync(kFull, x[k], h));
     }
+    // squares near or past the ends of the fp32 range (or a zero vector): the
+    // sum again with the vector scaled by the power of two that brings its
+    // largest magnitude to [1, 2); this thread's largest magnitude, then its
+    // scaled sum of squares
+    auto reload_max = [&]() {
+      float m = 0.f;
+#pragma unroll
+      for (int k = 0; k < E; ++k) {
+        const int o = a * M + 32 * k + lane;
+        m = fmaxf(m, fabsf(F16 ? __half2float(reinterpret_cast<const __half*>(src)[o]) : reinterpret_cast<const float*>(src)[o]));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+      return m;
+    };
+    auto reload_ss = [&](float scale) {
+      float q = 0.f;
+#pragma unroll
+      for (int k = 0; k < E; ++k) {
+        const int o = a * M + 32 * k + lane;
+        const float v = (F16 ? __half2float(reinterpret_cast<const __half*>(src)[o]) : reinterpret_cast<const float*>(src)[o]) * scale;
+        q = fmaf(v, v, q);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(kFull, q, off);
+      return q;
+    };
+    auto pow2_unit = [](float m) {
+      int e;
+      frexpf(m, &e);
+      return ldexpf(1.f, 1 - e);
+    };
     const int64_t r = base + vloc;
     if constexpr (P == 12) {
       // the Paley stage (z_a = Σ_b H12[a][b]·x_b per column i'), one exchange
@@ -170,7 +202,24 @@ __global__ void __launch_bounds__(P == 12 ? 384 : 256) encode_wht_kernel(const W
       float s2 = 0.f;
 #pragma unroll
       for (int b = 0; b < 12; ++b) s2 += part[b];
-      const float s = sqrtf(s2);
+      float s = sqrtf(s2);
+      if (!(s2 > 1e-30f && s2 < 1e36f)) {  // the same for every thread of the CTA
+        const float m = reload_max();
+        if (lane == 0) part[16 + a] = m;
+        __syncthreads();
+        float mm = 0.f;
+#pragma unroll
+        for (int b = 0; b < 12; ++b) mm = fmaxf(mm, part[16 + b]);
+        const float scale = mm > 0.f ? pow2_unit(mm) : 1.f;
+        const float q = reload_ss(scale);
+        __syncthreads();
+        if (lane == 0) part[16 + a] = q;
+        __syncthreads();
+        float q2 = 0.f;
+#pragma unroll
+        for (int b = 0; b < 12; ++b) q2 += part[16 + b];
+        s = sqrtf(q2) / scale;
+      }
       // the Paley stage: thread T < M takes column i' = T of all twelve blocks
       if (tid < M) {
         float xb[12];
@@ -198,7 +247,12 @@ __global__ void __launch_bounds__(P == 12 ? 384 : 256) encode_wht_kernel(const W
       }
     } else {
       // P = 1: the warp holds the whole vector
-      const float s = sqrtf(ss);
+      float s = sqrtf(ss);
+      if (!(ss > 1e-30f && ss < 1e36f)) {
+        const float m = reload_max();
+        const float scale = m > 0.f ? pow2_unit(m) : 1.f;
+        s = sqrtf(reload_ss(scale)) / scale;
+      }
       const float inv = s > 0.f ? 1.f / s : 0.f;
       unsigned char* cw = cbuf + vloc * D;
 #pragma unroll
@@ -230,7 +284,7 @@ static cudaError_t launch_wht_t(const WhtParams& p, bool f16, cudaStream_t st) {
   constexpr int NW = P == 12 ? 12 : 8, VPC = P == 12 ? 1 : 8, D = P * 32 * E;
   const int64_t ctas = (p.N + VPC - 1) / VPC;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * (P == 12 ? 4 : 8)));
-  const size_t smem = (size_t)(P == 12 ? D : 0) * 4 + 16 * 4 + (size_t)((VPC * D + 15) / 16) * 16 +
+  const size_t smem = (size_t)(P == 12 ? D : 0) * 4 + 32 * 4 + (size_t)((VPC * D + 15) / 16) * 16 +
                       (size_t)kWhtStages * VPC * D * (f16 ? 2 : 4);
   static int attr_done[2] = {0, 0};  // set once, before any stream capture
   if (!attr_done[f16 ? 1 : 0]) {

@@ -102,6 +102,23 @@ def test_hadamard_fast_transform_fp16_rows():
     check(cs, Pi, X.astype(np.float32), 3)
 
 
+@pytest.mark.parametrize("d", [256, 3072])
+def test_hadamard_extreme_magnitudes(d):
+    """Rows scaled by 1e-20, 1e-25 and 1e22 and rows with a single non-zero
+    value, through the fast transform (one block, and twelve)."""
+    ctx, Pi = hadamard_pair(16, d, 4)
+    X = synth.bulk_rows(16, 40, d)
+    X[1] *= 1e-20
+    X[2] *= 1e-25
+    X[3] *= 1e22
+    X[4] = 0.0
+    X[4, d // 3] = 2.5e-30
+    X[5] = 0.0
+    X[5, 0] = -3e30
+    cs = encode(ctx, X)
+    check(cs, Pi, X, 4)
+
+
 @pytest.mark.parametrize("d", [1536, 3072])
 def test_hadamard_bulk_indexing_full_size_sampled(d):
     """N = 100K rows of the bulk-indexing workload, 512 rows checked."""
@@ -141,6 +158,31 @@ def test_dense_wide_encode(d, b):
     words = cs.codes.view(torch.int32).cpu().numpy().view(np.uint32).reshape(n, -1)
     ok = ~band.any(axis=1)
     np.testing.assert_array_equal(words[ok], oq.pack_codes(idx_ref[ok], b))
+
+
+@pytest.mark.parametrize("d", [256, 1536])
+def test_dense_wide_encode_magnitude_edges(d):
+    """Rows whose magnitudes vary along the row or are extreme: zero leading
+    chunks, a small first chunk, a single huge or single non-zero value, rows
+    scaled by 1e-20, 1e-25 and 1e22 (squares below the fp32 normal range,
+    below its range, above it)."""
+    b = 4
+    X = synth.bulk_rows(15, 140, d)
+    X[3, :64] = 0.0          # first chunk zero
+    X[4, :128] = 0.0         # first two chunks zero
+    X[5, :64] *= 1e-2        # small first chunk, later values ~100x larger
+    X[6, :64] *= 1e-6        # later values ~1e6x larger
+    X[7, 64:] = 0.0          # only the first chunk non-zero
+    X[8] *= 1e-20            # a tiny row
+    X[9, :64] *= 1e-35       # a first chunk far below the rest
+    X[10, -1] = 1e6          # one huge last value
+    X[11] = 0.0
+    X[11, d - 1] = -3.0      # a single non-zero value, in the last chunk
+    X[12] *= 1e-25           # squares below the fp32 range
+    X[13] *= 1e22            # squares above the fp32 range
+    ctx, Pi = haar_pair(15, d, b)
+    cs = encode(ctx, X)
+    check(cs, Pi, X, b)
 
 
 def test_dense_wide_encode_fp16_rows():

@@ -117,6 +117,23 @@ def test_encode_ragged_and_zero_rows(N):
     assert not idx.any() and cs.norm[N // 2].item() == 0.0
 
 
+def test_encode_extreme_magnitudes():
+    """Rows scaled by 1e-20, 1e-25 (squares below the fp32 range) and 1e22
+    (above it), and rows with a single non-zero value: the norm and the codes
+    follow the definition at any magnitude."""
+    ctx, Pi, _ = make_pair(6, 128, 3)
+    X = synth.gaussian_rows(6, 64, 128)
+    X[1] *= 1e-20
+    X[2] *= 1e-25
+    X[3] *= 1e22
+    X[4] = 0.0
+    X[4, 77] = 2.5e-30
+    X[5] = 0.0
+    X[5, 0] = -3e30
+    cs = gpu_encode(ctx, X)
+    check_mse_encode(ctx, Pi, X, 3, cs)
+
+
 @pytest.mark.parametrize("b", [2, 3, 4])
 def test_encode_fp16_kv_token_and_pair_layouts(b):
     """fp16 K/V with 4 outlier channels x10 (the KV workloads), both layouts."""
