@@ -150,7 +150,8 @@ def run_encode(args, world, rank, local, root, clocks_cls, cpu):
                 "kernel": "encode_umma_kernel",
                 "peak_kind": f"{kind} bf16 dense / 3 split passes (fp16 hi/lo, same tensor rate as bf16)",
                 "passes": 3, "flops_per_vector": 2 * d * d,
-                "timed": "whole tq_encode call (row_norm_kernel + encode_umma_kernel)"}
+                "timed": "whole tq_encode call (row_norm_kernel + encode_umma_kernel)",
+                "traffic_of": "encode_umma_kernel alone"}
     # kernels per tq_encode call: the Hadamard kernel alone, or the norm pass and
     # the tensor-core kernel (d > 128, a multiple of 128), or one dense kernel
     launches = 2 if rot == "dense" and d > 128 and d % 128 == 0 else 1
