@@ -467,9 +467,10 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeds as the tq arm)",
-        "config": {"workload": f"decode attention, 1 layer, batch 1, 32 q / 8 kv heads, head_dim 128, "
-                               f"seq 16384, K/V TurboQuant_MSE b={bits} (oracle on a bounded sample)",
-                   "bits": bits},
+        "config": {"workload": f"decode attention, 1 layer, batch 1, 32 q / 8 kv heads, head_dim 128, seq 16384, "
+                               f"K/V TurboQuant_MSE b={bits}",
+                   "bits": bits, "seq": SEQ, "heads_q": HQ, "heads_kv": HKV, "head_dim": D,
+                   "sampled": sample},
         "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
