@@ -50,6 +50,22 @@ __host__ __device__ constexpr int paley12_sign(int a, int b) {
              : -1;
 }
 
+// The kernel's circulant form of rows 1-11: the +1 entries off the diagonal
+// of row a >= 1 sit at b = (a + o) % 11 + 1 for o in {0, 2, 3, 4, 8}.
+__host__ __device__ constexpr bool paley12_residue_form() {
+  for (int a = 1; a < 12; ++a)
+    for (int b = 1; b < 12; ++b) {
+      if (b == a) continue;
+      const bool listed = b == (a + 0) % 11 + 1 || b == (a + 2) % 11 + 1 || b == (a + 3) % 11 + 1 ||
+                          b == (a + 4) % 11 + 1 || b == (a + 8) % 11 + 1;
+      if (listed != (paley12_sign(a, b) > 0)) return false;
+    }
+  for (int a = 1; a < 12; ++a)
+    if (paley12_sign(a, 0) != -1 || paley12_sign(a, a) != 1 || paley12_sign(0, a) != 1) return false;
+  return paley12_sign(0, 0) == 1;
+}
+static_assert(paley12_residue_form(), "circulant form of the Paley matrix");
+
 constexpr int kWhtStages = 3;  // row groups in flight per CTA (cp.async ring)
 
 __device__ __forceinline__ void wcp16(void* dst, const void* src) {
@@ -226,11 +242,22 @@ __global__ void __launch_bounds__(P == 12 ? 384 : 256) encode_wht_kernel(const W
 #pragma unroll
         for (int b = 0; b < 12; ++b) xb[b] = zs[b * M + tid];
         const float inv = s > 0.f ? 1.f / s : 0.f;
+        // Rows 1-11 of H12 are circulant in the quadratic residues mod 11 (+1
+        // at b - a in {1, 3, 4, 5, 9}, -1 elsewhere, -1 at b = 0, +1 at b = a):
+        // with T = x_1 + ... + x_11 and z_0 = x_0 + T, z_a = 2(p_a + x_a) - z_0,
+        // p_a the sum of x_b over the five residue offsets from a.
+        float T = xb[1];
+#pragma unroll
+        for (int b = 2; b < 12; ++b) T += xb[b];
+        const float z0 = xb[0] + T;
 #pragma unroll
         for (int aa = 0; aa < 12; ++aa) {
-          float acc = 0.f;
-#pragma unroll
-          for (int b = 0; b < 12; ++b) acc = paley12_sign(aa, b) > 0 ? acc + xb[b] : acc - xb[b];
+          float acc = z0;
+          if (aa > 0) {
+            const float pa = ((xb[(aa + 0) % 11 + 1] + xb[(aa + 2) % 11 + 1]) + (xb[(aa + 3) % 11 + 1] + xb[(aa + 4) % 11 + 1])) +
+                             xb[(aa + 8) % 11 + 1];
+            acc = fmaf(2.f, pa + xb[aa], -z0);
+          }
           const float v = acc * inv;  // v = z/s
           int code = 0;
 #pragma unroll
