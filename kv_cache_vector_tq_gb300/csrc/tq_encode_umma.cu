@@ -594,8 +594,17 @@ tq_status launch_encode_umma(const DevCtx& c, const void* x, int x_dtype, int64_
   if (N > INT32_MAX) return TQ_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
   const bool f16 = x_dtype == TQ_F16;
   {
-    // one warp per row, 8 rows per CTA in flight
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((N + 7) / 8, (int64_t)num_sms() * 8));
+    // one warp per row, 8 rows per CTA in flight; as many CTAs as are resident
+    // at once (each warp strides over the rows with an equal share)
+    static int per_sm[2] = {0, 0};  // asked once, before any stream capture
+    if (!per_sm[f16 ? 1 : 0]) {
+      int n = 0;
+      const cudaError_t e = f16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, row_norm_kernel<true>, 256, 0)
+                                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, row_norm_kernel<false>, 256, 0);
+      if (e != cudaSuccess) return set_cuda_error(e);
+      per_sm[f16 ? 1 : 0] = n > 0 ? n : 1;
+    }
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((N + 7) / 8, (int64_t)num_sms() * per_sm[f16 ? 1 : 0]));
     if (f16)
       row_norm_kernel<true><<<grid, 256, 0, stream>>>(x, N, c.d, out->d_norm, offset, group_rows, group_stride);
     else

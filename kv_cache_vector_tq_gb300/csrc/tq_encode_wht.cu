@@ -310,18 +310,25 @@ template <int BM, int P, int E>
 static cudaError_t launch_wht_t(const WhtParams& p, bool f16, cudaStream_t st) {
   constexpr int NW = P == 12 ? 12 : 8, VPC = P == 12 ? 1 : 8, D = P * 32 * E;
   const int64_t ctas = (p.N + VPC - 1) / VPC;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * (P == 12 ? 4 : 8)));
   const size_t smem = (size_t)(P == 12 ? D : 0) * 4 + 32 * 4 + (size_t)((VPC * D + 15) / 16) * 16 +
                       (size_t)kWhtStages * VPC * D * (f16 ? 2 : 4);
-  static int attr_done[2] = {0, 0};  // set once, before any stream capture
-  if (!attr_done[f16 ? 1 : 0]) {
+  // CTAs resident per SM (registers and shared memory decide), asked once
+  // before any stream capture: every CTA of the grid strides over the rows
+  // with an equal share, so the grid must fit in one wave
+  static int per_sm[2] = {0, 0};
+  if (!per_sm[f16 ? 1 : 0]) {
     cudaError_t e = f16 ? cudaFuncSetAttribute(encode_wht_kernel<BM, P, E, true>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024)
                         : cudaFuncSetAttribute(encode_wht_kernel<BM, P, E, false>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
     if (e != cudaSuccess) return e;
-    attr_done[f16 ? 1 : 0] = 1;
+    int n = 0;
+    e = f16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_wht_kernel<BM, P, E, true>, NW * 32, smem)
+            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_wht_kernel<BM, P, E, false>, NW * 32, smem);
+    if (e != cudaSuccess) return e;
+    per_sm[f16 ? 1 : 0] = n > 0 ? n : 1;
   }
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * per_sm[f16 ? 1 : 0]));
   if (f16)
     encode_wht_kernel<BM, P, E, true><<<grid, NW * 32, smem, st>>>(p);
   else
