@@ -2,7 +2,9 @@
 table that fills roofline.traffic only while the captured kernel is unchanged."""
 
 import hashlib
+import json
 import os
+import subprocess
 import sys
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -40,3 +42,24 @@ def test_committed_traffic_rows_are_well_formed():
         assert os.path.exists(os.path.join(ROOT, src)), src
         assert len(digest) == 64 and int(digest, 16) >= 0
         assert int(rd) >= 0 and int(wr) >= 0
+
+
+def test_reference_arm_prints_one_contract_line():
+    """bench.py --impl reference: the oracle on the host cores, one JSON line
+    with the contract's keys and the library arm's metric and workload."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    j = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in j, k
+    assert j["impl"] == "reference" and j["metric"] == "decode-attn HBM GB/s" and j["unit"] == "GB/s"
+    assert j["higher_is_better"] is True and j["steps"] == 1 and j["warmup"] == 3 and j["value"] > 0
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["cpu_baseline"]["value"] == j["value"] and j["e2e"]["value"] == j["value"]
+    assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["d2h_bytes_per_step"] == 0
+    assert j["config"]["workload"].startswith("decode attention, 1 layer, batch 1, 32 q / 8 kv heads, head_dim 128, "
+                                              "seq 16384, K/V TurboQuant_MSE b=4")
