@@ -183,7 +183,12 @@ tq_status tq_codes_layout(const tq_ctx* ctx, int layout, int64_t n, tq_codes* de
  * TQ_ERR_UNSUPPORTED otherwise): two kernels on `stream`, a norm pass and a
  * tensor-core GEMM whose coordinates lying near a threshold are recomputed in
  * float-float arithmetic, so codes match the fp64 definition outside a band
- * of ~1e-6 around each threshold, as on every other path.
+ * of ~1e-6 around each threshold, as on every other path.  A context with the
+ * randomized Hadamard rotation (MSE, d = 2^k or 12·2^k with 2^k in 32..256)
+ * encodes with one kernel that applies the fast transform instead.
+ * Norms: fp32 sums of squares; a vector whose sum leaves (1e-30, 1e36) is
+ * summed again scaled by a power of two, so s is right for any finite
+ * magnitude the input type can hold.
  */
 tq_status tq_encode(const tq_ctx* ctx, const void* d_x, int x_dtype, int64_t N,
                     const tq_codes* out, int64_t offset, int64_t group_rows,
