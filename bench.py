@@ -18,7 +18,11 @@ value    = algorithmic decode bytes / s (codes + norms of K and V for all cached
            tokens, query, output, and the appended token) over the timed steps.
 e2e      = the same metric with the step inputs (query, new K/V token) copied
            from pinned host memory and the output copied back every decode step.
-roofline = the decode-attention call (query prep + split kernel + merge) alone.
+roofline = one decode-attention call alone (the same kernel without the
+           append: query rotation, tiles and merge in one launch) against the
+           measured HBM copy peak; traffic = its DRAM bytes per launch from the
+           ncu capture recorded in profiles/traffic.md, while the kernel's
+           source still matches that capture (else null).
 """
 
 import argparse
