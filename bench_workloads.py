@@ -40,11 +40,36 @@ def _peaks(root, sustained=False):
         return 6800.0, 1700.0 if sustained else 1900.0, "fallback"
 
 
+def code_digest(text):
+    """SHA-256 of C/C++/CUDA source with its comments and whitespace removed,
+    so that an edit of comments alone keeps the digest (string literals kept)."""
+    import hashlib
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":  # a literal, copied up to its closing quote
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return hashlib.sha256(" ".join("".join(out).split()).encode()).hexdigest()
+
+
 def traffic(root, key):
     """DRAM bytes (read + write) of one launch of the kernel recorded under
-    `key` in profiles/traffic.md, or None when no row matches or the kernel's
-    source file has changed since that capture (its SHA-256 differs)."""
-    import hashlib
+    `key` in profiles/traffic.md, or None when no row matches or the code of
+    the kernel's source file has changed since that capture (its digest by
+    code_digest differs)."""
     try:
         with open(os.path.join(root, "profiles", "traffic.md")) as f:
             rows = [r.split("|")[1:-1] for r in f.read().splitlines() if r.startswith("| ")]
@@ -55,8 +80,8 @@ def traffic(root, key):
         if len(cells) < 5 or cells[0] != key:
             continue
         try:
-            with open(os.path.join(root, cells[1]), "rb") as f:
-                digest = hashlib.sha256(f.read()).hexdigest()
+            with open(os.path.join(root, cells[1]), encoding="utf-8") as f:
+                digest = code_digest(f.read())
         except OSError:
             return None
         return int(cells[3]) + int(cells[4]) if digest == cells[2] else None

@@ -19,7 +19,8 @@
 //     codebook thresholds, pack), writes them to the cache and patches them
 //     into its staged tile; it takes half a share of the tiles to make room.
 //  3. Every CTA streams its tiles: each lane copies its own 16-byte chunks
-//     with cp.async into lane-private shared-memory slots, three tiles ahead,
+//     with cp.async into lane-private shared-memory slots, up to four tiles
+//     ahead (a slot is refilled as soon as its tile's words are in registers),
 //     and the warp runs
 //       K side  S[t][n] = Σ_κ K̂[t][κ]·Q[κ][n]   (mma.m16n8k16: A from a pair
 //               table indexed by two codes, B = pre-rotated queries, hi/lo)

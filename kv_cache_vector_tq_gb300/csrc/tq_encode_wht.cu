@@ -14,9 +14,11 @@
 // Work split: one warp per Hadamard block of a vector (the twelve blocks of a
 // d = 12·m vector are the twelve warps of a CTA; for d = m, eight vectors per
 // CTA), lane L holding elements 32k + L of its block.  Rows stream into a
-// shared-memory ring by cp.async, three row groups ahead.  Plain fp32 butterflies: each output sees one
-// rounding per stage, so the error in v stays near √(log2 d)·2^-24 (about
-// 2e-7 at d = 3072), inside the 1e-6 band around the codebook thresholds.
+// three-slot shared-memory ring by cp.async, two row groups ahead of the one
+// being transformed; the grid holds as many CTAs as are resident at once.
+// Plain fp32 butterflies: each output sees one rounding per stage, so the
+// error in v stays near √(log2 d)·2^-24 (about 2e-7 at d = 3072), inside the
+// 1e-6 band around the codebook thresholds.
 #include <algorithm>
 
 #include "tq_device.cuh"

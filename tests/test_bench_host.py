@@ -1,7 +1,6 @@
 """Host-side pieces of the benchmark (no GPU): the per-launch DRAM traffic
 table that fills roofline.traffic only while the captured kernel is unchanged."""
 
-import hashlib
 import json
 import os
 import subprocess
@@ -21,16 +20,26 @@ def _table(tmp_path, src_rel, digest, rd, wr):
         f"| k1 | {src_rel} | {digest} | {rd} | {wr} | test |\n")
 
 
-def test_traffic_follows_the_source_hash(tmp_path):
+def test_traffic_follows_the_code_digest(tmp_path):
     src = tmp_path / "kern.cu"
-    src.write_bytes(b"__global__ void k() {}\n")
-    _table(tmp_path, "kern.cu", hashlib.sha256(src.read_bytes()).hexdigest(), 1000, 24)
+    src.write_text("// kernel\n__global__ void k(int* p) { p[0] = 1; }\n")
+    _table(tmp_path, "kern.cu", bench_workloads.code_digest(src.read_text()), 1000, 24)
     assert bench_workloads.traffic(str(tmp_path), "k1") == 1024
     assert bench_workloads.traffic(str(tmp_path), "missing") is None
-    src.write_bytes(b"__global__ void k() { }\n")  # any edit voids the capture
+    # comments and layout do not change the code
+    src.write_text("/* the kernel, one store */\n__global__ void k(int* p) {\n  p[0] = 1;  // one\n}\n")
+    assert bench_workloads.traffic(str(tmp_path), "k1") == 1024
+    src.write_text("__global__ void k(int* p) { p[0] = 2; }\n")  # a code edit voids the capture
     assert bench_workloads.traffic(str(tmp_path), "k1") is None
     os.remove(src)
     assert bench_workloads.traffic(str(tmp_path), "k1") is None
+
+
+def test_code_digest_keeps_literals():
+    d = bench_workloads.code_digest
+    assert d('asm("a // b");') != d('asm("a");')  # a comment marker inside a literal is code
+    assert d("x = '/'; // c\ny = 1;") == d("x = '/';\ny = 1;")
+    assert d("a /* c */ + b") == d("a + b") and d("a + b") != d("a - b")
 
 
 def test_committed_traffic_rows_are_well_formed():
