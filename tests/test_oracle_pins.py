@@ -445,3 +445,83 @@ def test_hadamard_rotation_is_orthogonal():
     signs = np.where(np.random.default_rng(0).integers(0, 2, d) == 1, 1.0, -1.0)
     P = orot.hadamard_rotation(d, signs)
     assert np.abs(P @ P.T - np.eye(d)).max() < 1e-12
+
+
+# ------------------------------------------------ near-threshold bands
+# The parity tests excuse an index mismatch only inside the band
+# |v - t_k| <= 1e-6 · max(1, |t_k|) around a codebook threshold, and a QJL bit
+# only inside |(S·r)_j| <= 1e-6 · ‖S_j‖₂ · γ.  These values are built by hand so
+# that a band that is absolute instead of relative, relative to plain |t_k|
+# (no band at t = 0), uses column norms of S, drops γ or takes < for <= selects
+# different coordinates.
+def test_near_threshold_band_selects_exactly_the_hand_built_coordinates():
+    c = np.array([-5.0, -3.0, 3.0, 5.0])  # thresholds -4, 0, 4
+    v = np.array([
+        1.0e-6,          # t = 0, on the band edge (1e-6 · max(1, 0)): inside
+        0.5e-6,          # t = 0, inside (a band of 1e-6·|t| would be empty here)
+        -0.99e-6,        # t = 0, inside from below
+        1.01e-6,         # t = 0, outside
+        4.0 + 3.9e-6,    # t = 4: band 4e-6, inside (an absolute 1e-6 band would miss it)
+        4.0 - 3.9e-6,    # inside from below
+        4.0 + 4.1e-6,    # outside
+        -4.0 - 2.0e-6,   # t = -4, inside
+        -4.0 + 4.2e-6,   # outside
+        2.0,             # far from every threshold
+    ])
+    want = [True, True, True, False, True, True, False, True, False, False]
+    assert list(oq.near_threshold(v, c)) == want
+
+
+def test_near_threshold_band_keeps_the_unit_floor_below_one():
+    c = np.array([-0.3, -0.1, 0.1, 0.3])  # thresholds -0.2, 0, 0.2: all |t| < 1
+    v = np.array([0.2 + 0.9e-6, 0.2 + 1.1e-6, -0.2 - 0.95e-6, 0.2 + 0.15e-6])
+    # the band is 1e-6 absolute here (max(1, 0.2) = 1), not 0.2e-6
+    assert list(oq.near_threshold(v, c)) == [True, False, True, True]
+
+
+def test_near_threshold_shape_and_dtype():
+    c = np.array([-1.0, 1.0])
+    v = np.zeros((3, 4))
+    m = oq.near_threshold(v, c)
+    assert m.shape == (3, 4) and m.dtype == bool and m.all()
+
+
+def test_qjl_band_uses_row_norms_of_s_and_gamma():
+    # rows of S with norms 5 and 1; its column norms are 5 and 4, so a
+    # column-norm band differs in the second coordinate
+    S = np.array([[3.0, 4.0], [0.0, 1.0]])
+    assert np.allclose(np.sqrt((S * S).sum(1)), [5.0, 1.0])
+    gamma = np.array([2.0, 2.0, 2.0, 0.5, 1.0])
+    # bands per row: 1e-6·5·γ and 1e-6·1·γ
+    p = np.array([
+        [0.99e-5, 1.99e-6],    # both inside (γ = 2: 1e-5, 2e-6)
+        [1.01e-5, 2.01e-6],    # both outside
+        [-0.99e-5, -2.1e-6],   # first inside from below, second outside
+        [2.4e-6, 0.49e-6],     # γ = 0.5: bands 2.5e-6 and 0.5e-6, both inside
+        [5.1e-6, 1.0e-6],      # γ = 1: first outside; second exactly on its band (<=)
+    ])
+    want = np.array([[True, True], [False, False], [True, False], [True, True], [False, True]])
+    np.testing.assert_array_equal(oq.qjl_near_zero(p, gamma, S), want)
+
+
+def test_qjl_band_is_empty_for_a_zero_residual():
+    # γ = 0 (a zero vector or an exact MSE code) gives a band of width zero:
+    # only an exactly zero projection lies in it
+    S = np.eye(3)
+    m = oq.qjl_near_zero(np.array([[0.0, 1e-30, -1e-30]]), np.array([0.0]), S)
+    assert m.tolist() == [[True, False, False]]
+
+
+def test_band_width_by_uniform_draws_near_each_threshold():
+    # Draws uniform within ±1e-5 of each threshold of the b = 3 codebook fall in
+    # the band with probability 1e-6·max(1,|t_k|) / 1e-5 (binomial count).
+    cb = ocb.build_codebook(128, 3, density="gauss")
+    t = 0.5 * (cb["centroids"][:-1] + cb["centroids"][1:])
+    assert np.diff(t).min() > 1e-3  # no draw reaches a neighbour's band
+    rng = np.random.default_rng(7)
+    width, n = 1e-5, 500_000
+    for tk in t:
+        v = tk + rng.uniform(-width, width, n)
+        hits = int(oq.near_threshold(v, cb["centroids"]).sum())
+        pr = 1e-6 * max(1.0, abs(tk)) / width
+        assert abs(hits - n * pr) <= 6 * math.sqrt(n * pr * (1 - pr)), (tk, hits, n * pr)
