@@ -21,7 +21,7 @@ e2e      = the same metric with the step inputs (query, new K/V token) copied
 roofline = one decode-attention call alone (the same kernel without the
            append: query rotation, tiles and merge in one launch) against the
            measured HBM copy peak; traffic = its DRAM bytes per launch from the
-           ncu capture recorded in profiles/traffic.md, while the kernel's
+           ncu capture recorded in profiles/traffic.json, while the kernel's
            source still matches that capture (else null).
 """
 
@@ -433,9 +433,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     import numpy as np
-    import torch
 
-    import kv_cache_vector_tq_gb300 as tq
     from kv_cache_vector_tq_gb300 import synth
     from oracle import codebook as ocb
     from oracle import quantizer as oq

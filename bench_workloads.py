@@ -66,25 +66,25 @@ def code_digest(text):
 
 
 def traffic(root, key):
-    """DRAM bytes (read + write) of one launch of the kernel recorded under
-    `key` in profiles/traffic.md, or None when no row matches or the code of
+    """DRAM bytes (read + written) of one launch of the kernel recorded under
+    `key` in profiles/traffic.json, or None when no row matches or the code of
     the kernel's source file has changed since that capture (its digest by
     code_digest differs)."""
+    import json
     try:
-        with open(os.path.join(root, "profiles", "traffic.md")) as f:
-            rows = [r.split("|")[1:-1] for r in f.read().splitlines() if r.startswith("| ")]
-    except OSError:
+        with open(os.path.join(root, "profiles", "traffic.json")) as f:
+            rows = json.load(f)["rows"]
+    except (OSError, ValueError, KeyError):
         return None
     for r in rows:
-        cells = [c.strip() for c in r]
-        if len(cells) < 5 or cells[0] != key:
+        if r.get("key") != key:
             continue
         try:
-            with open(os.path.join(root, cells[1]), encoding="utf-8") as f:
+            with open(os.path.join(root, r["source"]), encoding="utf-8") as f:
                 digest = code_digest(f.read())
-        except OSError:
+        except (OSError, KeyError):
             return None
-        return int(cells[3]) + int(cells[4]) if digest == cells[2] else None
+        return int(r["read_bytes"]) + int(r["write_bytes"]) if digest == r.get("code_digest") else None
     return None
 
 

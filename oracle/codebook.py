@@ -15,7 +15,7 @@ Sources
   300 Lloyd-Max iterations, computed once per (d, b) and cached:
   "sub-byte-kv-cache-quantization-turboquant", section "工程实现的关键路径".
 
-Readings where the pages are silent (each one also listed in the design doc):
+Readings where the pages are silent:
 * initial centroids: the (k + 1/2)/2^b quantiles of the grid's weighted
   midpoint CDF, linearly interpolated (the pages only say "guess"/"random");
 * a grid point exactly on a threshold belongs to the upper cell;

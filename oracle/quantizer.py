@@ -18,7 +18,7 @@ Sources
   "内积偏差问题与 QJL 修正器"; "sub-byte-kv-cache-quantization-turboquant",
   section "两阶段量化框架".
 
-Readings (also in DESIGN.md):
+Readings where the pages are silent or ambiguous:
 * Decisions are taken in unit-variance units v = √d · y against centroids in
   the same units; ties at equal distance go to the higher index.
 * A zero vector has s = 0, all indices 0, γ = 0 and all QJL bits 0.

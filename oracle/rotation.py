@@ -13,7 +13,7 @@ Sources
   "TurboQuant 和 RotorQuant 的真相", chapter 3 (WHT, O(d log d)) and
   chapter 7 ("WHT vs Random Rotation").
 
-Readings (also in DESIGN.md):
+Readings where the pages are silent or ambiguous:
 * The QR factor is sign-fixed, Π = Q · diag(sign(diag R)) with sign(0) = +1,
   which makes Π Haar-distributed and makes ΠᵀG upper triangular with a
   positive diagonal.

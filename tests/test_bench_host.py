@@ -14,10 +14,9 @@ import bench_workloads  # noqa: E402
 
 def _table(tmp_path, src_rel, digest, rd, wr):
     (tmp_path / "profiles").mkdir(exist_ok=True)
-    (tmp_path / "profiles" / "traffic.md").write_text(
-        "| key | source | sha256 | read bytes | write bytes | launch captured |\n"
-        "|---|---|---|---|---|---|\n"
-        f"| k1 | {src_rel} | {digest} | {rd} | {wr} | test |\n")
+    row = {"key": "k1", "source": src_rel, "code_digest": digest, "read_bytes": rd, "write_bytes": wr,
+           "launch": "test", "command": "none"}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"about": "test", "rows": [row]}))
 
 
 def test_traffic_follows_the_code_digest(tmp_path):
@@ -43,14 +42,16 @@ def test_code_digest_keeps_literals():
 
 
 def test_committed_traffic_rows_are_well_formed():
-    path = os.path.join(ROOT, "profiles", "traffic.md")
-    rows = [r.split("|")[1:-1] for r in open(path).read().splitlines() if r.startswith("| ")]
-    rows = [[c.strip() for c in r] for r in rows if r[0].strip() not in ("key",)]
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rows = json.load(f)["rows"]
     assert rows
-    for key, src, digest, rd, wr, _ in rows:
-        assert os.path.exists(os.path.join(ROOT, src)), src
-        assert len(digest) == 64 and int(digest, 16) >= 0
-        assert int(rd) >= 0 and int(wr) >= 0
+    keys = [r["key"] for r in rows]
+    assert len(set(keys)) == len(keys)
+    for r in rows:
+        assert os.path.exists(os.path.join(ROOT, r["source"])), r["source"]
+        assert len(r["code_digest"]) == 64 and int(r["code_digest"], 16) >= 0
+        assert int(r["read_bytes"]) >= 0 and int(r["write_bytes"]) >= 0
+        assert r["command"].startswith("ncu ") and "--clock-control none" in r["command"]
 
 
 def test_reference_arm_prints_one_contract_line():
