@@ -284,7 +284,7 @@ tq_status tq_decode_step(const tq_ctx* kctx, const tq_ctx* vctx, const void* d_q
  * and ws_bytes.  Its scratch (the counters and partial softmax states that
  * tq_decode_attention keeps in the workspace) is a 2 MiB array built into the
  * library, which every GPU that loads libtq keeps reserved until the process
- * exits.  It starts zero-filled and every call leaves its counters at zero.
+ * exits.
  *   - Shapes whose scratch (tq_decode_workspace_size) exceeds 2 MiB return
  *     TQ_ERR_UNSUPPORTED before anything is launched.  The need is 4 bytes per
  *     (batch, KV head) plus at most about 80 KB per query head of a KV head
@@ -294,8 +294,10 @@ tq_status tq_decode_step(const tq_ctx* kctx, const tq_ctx* vctx, const void* d_q
  *     capture.
  *   - All calls share the array: two calls that overlap on the GPU (different
  *     streams, no ordering between them) race and corrupt each other's output.
- *     Order them on one stream.  Nothing in the array needs clearing between
- *     calls: each call writes every state it reads and resets its counters.
+ *     Order them on one stream.  Each call first zeroes the array's arrival
+ *     counters on `stream` (a memset, which allocates nothing), so a call that
+ *     failed part-way leaves nothing behind for the next one; every other
+ *     state a call reads it writes itself first.
  * The call itself allocates nothing (no cudaMalloc or allocating library routine).
  */
 tq_status tq_decode_attention_noalloc(const tq_ctx* kctx, const tq_ctx* vctx, const void* d_q,

@@ -104,7 +104,6 @@ size_t decode_noalloc_limit() { return kNoAllocScratchBytes; }
 // symbol is only a stand-in, so the address is asked from the runtime once per
 // device (with that device current) and cached.
 static cudaError_t decode_scratch_address(void** out) {
-  constexpr int kMaxDevices = 64;
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
   int dev = 0;
@@ -130,6 +129,11 @@ tq_status launch_decode_noalloc(const DevCtx& kc, const DevCtx& vc, const void* 
   if (need > kNoAllocScratchBytes) return TQ_ERR_UNSUPPORTED;
   void* ws = nullptr;
   cudaError_t e = decode_scratch_address(&ws);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  // Every call that completes leaves the counters at zero, but a call that
+  // failed part-way could leave them set, and the caller cannot reach this
+  // array to clear it: zero them on the call's stream first (no allocation).
+  e = cudaMemsetAsync(ws, 0, ws_counter_bytes(B * Hkv), stream);
   if (e != cudaSuccess) return set_cuda_error(e);
   return launch_decode(kc, vc, q, q_dtype, K, V, B, Hq, Hkv, seq, cap, scale, out, ws, need, stream);
 }
