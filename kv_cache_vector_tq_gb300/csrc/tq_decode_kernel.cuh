@@ -977,12 +977,9 @@ template <int BK, int BV, int G, bool Q = false>
 static cudaError_t run_step(const StepParams& p, int groups, cudaStream_t st) {
   constexpr int W = G >= 8 ? 8 : 16;
   auto kern = decode_step_kernel<BK, BV, G, W, Q>;
-  static int attr_done = 0;  // set once, before any stream capture
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_done = 1;
-  }
+  static PerDeviceValue smem_attr;  // set once per device, before any stream capture
+  const cudaError_t e = smem_attr_once(smem_attr, (const void*)kern, 227 * 1024);
+  if (e != cudaSuccess) return e;
   const StepSmem L = step_smem(BK, BV, G, W, p.same_lut != 0, Q);
   StepParams pp = p;
   pp.S = choose_splits(p.tiles, groups, W, p.append != 0, L.mw / (G * kPart * 4));

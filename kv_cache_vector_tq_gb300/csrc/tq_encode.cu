@@ -344,24 +344,18 @@ __global__ void __launch_bounds__(256, 1) encode_kernel(const EncParams p) {
 template <int BM, bool PROD>
 static cudaError_t launch_typed(const EncParams& p, bool f16, int grid, size_t smem,
                                 cudaStream_t st) {
-  // kernel attributes are set once (outside any stream capture that follows)
-  static int attr_done[2] = {0, 0};
+  // kernel attributes are set once per device (outside any stream capture that follows)
+  static PerDeviceValue attr[2];
   cudaError_t e;
   if (f16) {
     auto k = encode_kernel<BM, PROD, true>;
-    if (!attr_done[1]) {
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 16 * 16 * 2 * 32 * 8);
-      if (e != cudaSuccess) return e;
-      attr_done[1] = 1;
-    }
+    e = smem_attr_once(attr[1], (const void*)k, 16 * 16 * 2 * 32 * 8);
+    if (e != cudaSuccess) return e;
     k<<<grid, 256, smem, st>>>(p);
   } else {
     auto k = encode_kernel<BM, PROD, false>;
-    if (!attr_done[0]) {
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 16 * 16 * 2 * 32 * 8);
-      if (e != cudaSuccess) return e;
-      attr_done[0] = 1;
-    }
+    e = smem_attr_once(attr[0], (const void*)k, 16 * 16 * 2 * 32 * 8);
+    if (e != cudaSuccess) return e;
     k<<<grid, 256, smem, st>>>(p);
   }
   return cudaGetLastError();

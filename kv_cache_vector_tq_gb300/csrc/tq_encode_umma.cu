@@ -546,12 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1) encode_umma_kernel(const UmmaPara
 template <int BM, bool F16>
 cudaError_t launch_umma_t(const UmmaParams& p, const CUtensorMap& xmap, cudaStream_t st) {
   auto k = encode_umma_kernel<BM, F16>;
-  static bool attr_done = false;  // set once, before any stream capture
-  if (!attr_done) {
-    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, XLayout<F16>::Smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static PerDeviceValue attr;  // set once per device, before any stream capture
+  const cudaError_t e = smem_attr_once(attr, (const void*)k, XLayout<F16>::Smem);
+  if (e != cudaSuccess) return e;
   const int64_t tiles = (p.N + kTM - 1) / kTM * (p.d / kTN);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms()));
   k<<<grid, kThreads, XLayout<F16>::Smem, st>>>(p, xmap);
@@ -596,15 +593,10 @@ tq_status launch_encode_umma(const DevCtx& c, const void* x, int x_dtype, int64_
   {
     // one warp per row, 8 rows per CTA in flight; as many CTAs as are resident
     // at once (each warp strides over the rows with an equal share)
-    static int per_sm[2] = {0, 0};  // asked once, before any stream capture
-    if (!per_sm[f16 ? 1 : 0]) {
-      int n = 0;
-      const cudaError_t e = f16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, row_norm_kernel<true>, 256, 0)
-                                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, row_norm_kernel<false>, 256, 0);
-      if (e != cudaSuccess) return set_cuda_error(e);
-      per_sm[f16 ? 1 : 0] = n > 0 ? n : 1;
-    }
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((N + 7) / 8, (int64_t)num_sms() * per_sm[f16 ? 1 : 0]));
+    static PerDeviceValue per_sm[2];  // asked once per device, before any stream capture
+    const int resident = f16 ? ctas_per_sm_once(per_sm[1], (const void*)row_norm_kernel<true>, 256, 0)
+                             : ctas_per_sm_once(per_sm[0], (const void*)row_norm_kernel<false>, 256, 0);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((N + 7) / 8, (int64_t)num_sms() * resident));
     if (f16)
       row_norm_kernel<true><<<grid, 256, 0, stream>>>(x, N, c.d, out->d_norm, offset, group_rows, group_stride);
     else

@@ -317,20 +317,12 @@ static cudaError_t launch_wht_t(const WhtParams& p, bool f16, cudaStream_t st) {
   // CTAs resident per SM (registers and shared memory decide), asked once
   // before any stream capture: every CTA of the grid strides over the rows
   // with an equal share, so the grid must fit in one wave
-  static int per_sm[2] = {0, 0};
-  if (!per_sm[f16 ? 1 : 0]) {
-    cudaError_t e = f16 ? cudaFuncSetAttribute(encode_wht_kernel<BM, P, E, true>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024)
-                        : cudaFuncSetAttribute(encode_wht_kernel<BM, P, E, false>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-    if (e != cudaSuccess) return e;
-    int n = 0;
-    e = f16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_wht_kernel<BM, P, E, true>, NW * 32, smem)
-            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_wht_kernel<BM, P, E, false>, NW * 32, smem);
-    if (e != cudaSuccess) return e;
-    per_sm[f16 ? 1 : 0] = n > 0 ? n : 1;
-  }
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * per_sm[f16 ? 1 : 0]));
+  static PerDeviceValue attr[2], per_sm[2];  // once per device
+  const void* kf = f16 ? (const void*)encode_wht_kernel<BM, P, E, true> : (const void*)encode_wht_kernel<BM, P, E, false>;
+  const cudaError_t e = smem_attr_once(attr[f16 ? 1 : 0], kf, 160 * 1024);
+  if (e != cudaSuccess) return e;
+  const int resident = ctas_per_sm_once(per_sm[f16 ? 1 : 0], kf, NW * 32, smem);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * resident));
   if (f16)
     encode_wht_kernel<BM, P, E, true><<<grid, NW * 32, smem, st>>>(p);
   else

@@ -21,17 +21,51 @@ tq_status set_cuda_error(cudaError_t e) {
   return TQ_ERR_CUDA;
 }
 
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-      v = 152;
-    n = v;
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
   }
-  return n;
+  return dev;
+}
+
+int num_sms() {
+  static PerDeviceValue cache;
+  const int dev = current_device();
+  const int n = cache.get(dev, [dev] {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return -1;
+    }
+    return v;
+  });
+  return n > 0 ? n : 152;
+}
+
+cudaError_t smem_attr_once(PerDeviceValue& flag, const void* func, int bytes) {
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  cudaError_t err = cudaSuccess;
+  const int r = flag.get(dev, [&] {
+    err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return err == cudaSuccess ? 1 : -1;
+  });
+  return r > 0 ? cudaSuccess : (err != cudaSuccess ? err : cudaErrorInvalidDevice);
+}
+
+int ctas_per_sm_once(PerDeviceValue& cache, const void* func, int threads, size_t smem) {
+  const int dev = current_device();
+  const int n = cache.get(dev, [&] {
+    int v = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, func, threads, smem) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return -1;
+    }
+    return v;
+  });
+  return n > 0 ? n : 1;
 }
 
 // Sum with Neumaier compensation, so the result does not depend on the order

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "tq.h"
+#include "tq_once.h"
 
 namespace tq {
 
@@ -86,6 +87,16 @@ tq_status launch_encode_umma(const DevCtx& c, const void* x, int x_dtype, int64_
                              int64_t offset, int64_t group_rows, int64_t group_stride, cudaStream_t stream);
 tq_status launch_encode_wht(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
                             int64_t offset, int64_t group_rows, int64_t group_stride, cudaStream_t stream);
+// SM count of the current device (cached per device).
 int num_sms();
+// Current device, or -1 if the runtime cannot tell.
+int current_device();
+// cudaFuncAttributeMaxDynamicSharedMemorySize = bytes for `func` on the current
+// device, set once per device (`flag` is the kernel's own per-device record).
+cudaError_t smem_attr_once(PerDeviceValue& flag, const void* func, int bytes);
+// CTAs of `func` resident per SM with `threads` threads and `smem` bytes of
+// dynamic shared memory, on the current device (cached per device in `cache`;
+// 1 if the runtime cannot tell).
+int ctas_per_sm_once(PerDeviceValue& cache, const void* func, int threads, size_t smem);
 
 }  // namespace tq

@@ -309,12 +309,9 @@ cudaError_t run_scores(const ScoreParams& p, cudaStream_t st) {
   constexpr int E = 1 << (2 * BM);
   constexpr size_t smem = 2 * kAStage + kBBytes + E * 32 * 4 + 256;
   auto k = scores_kernel<BM, PROD>;
-  static bool attr_done = false;  // set once, outside any later stream capture
-  if (!attr_done) {
-    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static PerDeviceValue attr;  // set once per device, outside any later stream capture
+  const cudaError_t e = smem_attr_once(attr, (const void*)k, (int)smem);
+  if (e != cudaSuccess) return e;
   const int64_t tiles = (p.N + kKeyTile - 1) / kKeyTile;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms()));
   k<<<grid, kThreads, smem, st>>>(p);

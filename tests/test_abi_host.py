@@ -108,3 +108,21 @@ def test_words_per_vector_rule():
     assert [words_per_vector(128, b) for b in (1, 2, 3, 4)] == [4, 8, 12, 16]
     assert words_per_vector(32, 3) == 4 and words_per_vector(3072, 4) == 384
     assert math.ceil(4 * 1536 / 32) == 192
+
+
+def test_per_device_cache_logic(tmp_path):
+    """Kernel attributes, SM counts and occupancy answers are kept per device
+    (tq_once.h): compile the header's host test with g++ and run it."""
+    import shutil
+    import subprocess
+    cxx = shutil.which("g++")
+    if cxx is None:
+        pytest.skip("no g++")
+    exe = tmp_path / "per_device_value_test"
+    src = os.path.join(ROOT, "tests", "native", "per_device_value_test.cpp")
+    inc = os.path.join(ROOT, "kv_cache_vector_tq_gb300", "csrc")
+    r = subprocess.run([cxx, "-std=c++17", "-O1", "-pthread", "-I", inc, src, "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
