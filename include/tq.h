@@ -314,6 +314,18 @@ tq_status tq_decode_attention_noalloc(const tq_ctx* kctx, const tq_ctx* vctx, co
 tq_status tq_unpack_indices(const tq_codes* codes, int64_t first, int64_t count, uint8_t* h_idx,
                             uint8_t* h_bits);
 
+/* Bound of the pipeline waits (mbarrier phases) of the tensor-memory kernels
+ * launched with this context afterwards (the encoders for d = 128 and
+ * d > 128 with the dense rotation, and the scorer): a wait that has polled `polls` times without success gives up; the
+ * kernel then stops its pipeline, waits (with the default bound) for its own
+ * copies and tensor-core operations in flight, frees its tensor memory and
+ * returns, leaving its outputs unspecified, and tq_status_poll reports
+ * TQ_ERR_TIMEOUT once.  Default 2^22 polls (seconds); 0 makes every such wait
+ * give up before its first poll, which exercises that path on demand.  A
+ * failure-handling and testing aid: not synchronised with launches in flight,
+ * so set it between calls.  Errors: INVALID_ARG (NULL ctx). */
+tq_status tq_ctx_set_wait_limit(tq_ctx* ctx, uint32_t polls);
+
 /* Reads and clears the context's device status word (synchronises `stream`).
  * Returns TQ_OK; TQ_ERR_UNSUPPORTED if a decode kernel launched with this
  * context (as kctx) found dynamic shared memory at another shared-window

@@ -25,6 +25,7 @@ EXPORTS = (
     "tq_rotation_haar", "tq_ctx_create", "tq_ctx_destroy", "tq_codes_layout", "tq_encode",
     "tq_scores_workspace_size", "tq_scores", "tq_decode_workspace_size",
     "tq_decode_attention", "tq_decode_step", "tq_decode_attention_noalloc", "tq_unpack_indices", "tq_status_poll",
+    "tq_ctx_set_wait_limit",
 )
 
 
@@ -90,6 +91,7 @@ def lib():
                                          _i64, _f, _vp, _vp], _i),
         "tq_unpack_indices": ([P(Codes), _i64, _i64, _vp, _vp], _i),
         "tq_status_poll": ([_vp, _vp], _i),
+        "tq_ctx_set_wait_limit": ([_vp, ctypes.c_uint32], _i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -162,6 +164,10 @@ class Context:
             self.close()
         except Exception:
             pass
+
+    def set_wait_limit(self, polls):
+        """Bound of the context's pipeline waits (tq_ctx_set_wait_limit)."""
+        _check("tq_ctx_set_wait_limit", lib().tq_ctx_set_wait_limit(self.handle, int(polls)))
 
     def poll(self, stream=None):
         st = lib().tq_status_poll(self.handle, _stream(stream))

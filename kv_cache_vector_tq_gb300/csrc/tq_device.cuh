@@ -65,6 +65,30 @@ __device__ __forceinline__ float pow2_scale_16_32(float s) {
   return ldexpf(1.f, 5 - e);
 }
 
+// ------------------------------------------------------------------ encoder helpers
+// code = #{k : v >= t_k} by binary search over thr (2^BM - 1 thresholds,
+// padded with +inf to 16); near = v lies within m of a neighbouring threshold.
+template <int BM>
+__device__ __forceinline__ uint32_t bucketize(float v, const float* thr, float m, bool& near) {
+  int c = 0;
+#pragma unroll
+  for (int st = (1 << BM) >> 1; st > 0; st >>= 1)
+    if (v >= thr[c + st - 1]) c += st;
+  const float below = c > 0 ? thr[c - 1] : -INFINITY;
+  near = (v - below < m) || (thr[c] - v < m);
+  return (uint32_t)c;
+}
+
+// sh + sl += a·b, float-float (the product split exactly by an FMA)
+__device__ __forceinline__ void ff_fma(float a, float b, float& sh, float& sl) {
+  const float p = a * b;
+  const float e = fmaf(a, b, -p);
+  const float s = sh + p;
+  const float bb = s - sh;
+  sl += ((sh - (s - bb)) + (p - bb)) + e;
+  sh = s;
+}
+
 // ------------------------------------------------------------------ PTX helpers
 // mbarrier, bulk asynchronous copy (global -> shared), programmatic dependent launch
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -92,19 +116,19 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
 // Bounded wait on an mbarrier phase of a warp-specialized kernel: gives up
-// (false) when another thread of the CTA set the abort flag, or after the spin
-// limit, when it sets the abort flag and bit 0 of the status word itself.
-__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
+// (false) when another thread of the CTA set the abort flag, or once it has
+// polled `limit` times without success, when it sets the abort flag and bit 0
+// of the status word itself (limit 0: gives up before the first poll).
+__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                         uint32_t limit) {
   for (uint32_t n = 0;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63u) == 63u) {
-      if (*abort_flag) return false;
-      if (n > kSpinLimitDev) {
-        *abort_flag = 1;
-        atomicOr(status, 1);
-        return false;
-      }
+    if (n >= limit) {
+      *abort_flag = 1;
+      atomicOr(status, 1);
+      return false;
     }
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63u) == 63u && *abort_flag) return false;
   }
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -148,6 +172,14 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+// Shared-memory matrix descriptor for a K-major operand stored in the 128-byte
+// swizzle (as a 2-D TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes it): rows
+// of 128 bytes, 8-row groups 1024 bytes apart; the group base must be 1024-byte
+// aligned.  A K step inside the 128-byte row advances saddr by its byte offset.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 // Instruction descriptor, kind::f16 with fp16 A and B, fp32 accumulator, both K-major.
 __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {

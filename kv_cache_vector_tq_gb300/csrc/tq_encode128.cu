@@ -1,0 +1,706 @@
+// TurboQuant encoder for d = 128 (MSE and Prod, fp32 or fp16 rows, TOKEN or
+// PAIR layout) on the fifth-generation tensor cores.
+//
+// "TurboQuant 详解", section 一个具体例子：KV Cache 在 prefill 和 decode 里怎么量化
+// steps 1-6 (s = ‖x‖, y = Π·x/s, idx_i = nearest centroid of √d·y_i, pack the
+// indices, store s) and section TurboQuant_prod (a (b-1)-bit MSE stage, the
+// residual r = u − Πᵀŷ, γ = ‖r‖ and the 1-bit code sign(S·r), sign(0) = +1);
+// the rotation is the encoder's one dense matrix product ("turboquant-first-
+// principles-walkthrough", section 通用码本设计).
+//
+// A persistent CTA per SM walks tiles of 128 rows.  Per tile the rotation is
+// Y = X·(pi_scale·Π)ᵀ as tcgen05.mma of M = N = 128 and K = 16, eight K steps
+// per pass, into one fp32 accumulator in tensor memory:
+//   fp16 rows: A is the x tile itself, loaded by TMA in the 128-byte swizzle
+//              and read by the MMA from shared memory (x is exact in fp16);
+//              two passes, x·Πlo then x·Πhi.
+//   fp32 rows: A is x·2^e split into fp16 hi + lo (2^e puts s·2^e in [16, 32)),
+//              written to tensor memory by the prep warps; three passes,
+//              xl·Πhi, xh·Πlo, then xh·Πhi.
+// The low-order passes go first so that their small products are not
+// truncated against a large accumulator.  The tensor cores' fp32 accumulation
+// still truncates (measured on GB300 about 7e-9·L in v units over an
+// accumulated K range L, ~1e-6 at L = 128), so every coordinate within 8e-6 of
+// a threshold is recomputed by one warp as a float-float dot product of the
+// input row with the fp32 Π (error ~3e-8) and decided again: codes match the
+// fp64 definition outside the 1e-6 band, as on every other path.
+// Prod: the epilogue forms r_rot = (v − c[idx])/√d per coordinate (γ = ‖r_rot‖
+// = ‖r‖, Π being orthogonal), writes it scaled by 2^e (γ·2^e in [16, 32)) as
+// fp16 hi + lo into tensor memory, and a second three-pass product with
+// (m_scale·S·Πᵀ) gives p = S·r up to a positive factor; bit_j = [p_j >= 0].
+//
+// Warp roles (10 warps):
+//   0     producer: the B operand tables once (bulk copy), then per tile one
+//         2-D TMA load per 128-byte column box of the x tile.
+//   1     MMA issuer (one thread).
+//   2-5   prep: thread = row = TMEM lane (warp w owns lanes 32·(w % 4)..+31):
+//         s = ‖x‖ from the staged tile (fp32 sums; a row whose sum leaves
+//         (1e-30, 1e36) is summed again scaled by a power of two); fp32 rows:
+//         the split A operand into tensor memory.
+//   6-9   epilogue: thread = row: v = acc·√d/(s·scales), bucketize (binary
+//         search over the thresholds) with a near-threshold flag, pack in
+//         registers, recompute flagged coordinates, (Prod: residual, second
+//         product, sign bits), store codes, norm (γ, sign words).
+// All waits are bounded (tq_ctx_set_wait_limit); a wait that gives up sets the
+// abort flag, which every role polls, and bit 0 of the status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+namespace {
+
+constexpr int kRows = 128;                   // rows per tile = TMEM lanes = MMA M
+constexpr int kDim = 128;                    // d = MMA N = K
+constexpr int kBox = kRows * 128;            // one 128-byte column box of the x tile: 16 KB
+constexpr int kTab = 4 * kUmmaPlaneBytes;    // B operand of one 128 x 128 matrix: (hi, lo) x 2 K chunks
+constexpr int kThreads = 10 * 32;
+constexpr float kMargin = 8e-6f;             // recomputation band around each threshold (v units)
+
+template <bool F16, bool PROD>
+struct Lay {
+  static constexpr int ES = F16 ? 2 : 4;
+  static constexpr int Boxes = kDim * ES / 128;  // 2 (fp16) or 4 (fp32)
+  static constexpr int Stage = Boxes * kBox;     // 32 or 64 KB
+  static constexpr int XStages = F16 ? (PROD ? 2 : 3) : (PROD ? 1 : 2);
+  static constexpr int AStages = F16 ? 0 : (PROD ? 1 : 2);  // fp32: split A in tensor memory
+  static constexpr int AccBufs = (PROD && !F16) ? 1 : 2;
+  // tensor memory columns: A stages (hi 64 | lo 64), accumulators, then (Prod)
+  // the residual operand (hi 64 | lo 64) and the QJL accumulator
+  static constexpr uint32_t ColAcc = AStages * 128;
+  static constexpr uint32_t ColA2 = ColAcc + AccBufs * 128;
+  static constexpr uint32_t ColAcc2 = ColA2 + 128;
+  static constexpr uint32_t Cols = PROD ? ColAcc2 + 128 : ColA2;
+  static constexpr uint32_t TmemCols = Cols <= 256 ? 256 : 512;
+  static constexpr int OffX = kTab * (PROD ? 2 : 1);
+  static constexpr int OffNorm = OffX + XStages * Stage;
+  static constexpr int OffThr = OffNorm + AccBufs * kRows * 4;
+  static constexpr int OffCen = OffThr + 16 * 4;
+  static constexpr int OffBar = OffCen + 16 * 4;
+  static constexpr int NBar = 24;
+  static constexpr int Smem = OffBar + NBar * 8 + 16;
+  static constexpr int SmemAlloc = Smem + 1024;  // slack to align the base to 1024 bytes
+  static_assert(Cols <= 512, "tensor memory");
+  static_assert(SmemAlloc <= 227 * 1024, "shared memory");
+};
+
+struct Enc128Params {
+  const void* x;
+  int64_t N;
+  uint32_t* codes;
+  float* norm;
+  uint32_t* qjl;
+  float* rnorm;
+  const unsigned char* tab_pi;  // pi_scale·Π as B tiles (hi, lo planes per 64-wide K chunk)
+  const unsigned char* tab_m;   // Prod: m_scale·S·Πᵀ in the same layout
+  const float* pi;              // Π, fp32 row-major (recomputation)
+  float pi_scale;
+  double sqrt_d;
+  float thr[15];
+  float cen[16];
+  int layout, W, QW, pair_aligned;
+  int64_t offset, group_rows, group_stride;
+  int* status;
+  uint32_t wait_limit;
+};
+
+__device__ __forceinline__ int64_t dest_row(const Enc128Params& p, int64_t r) {
+  return (r / p.group_rows) * p.group_stride + p.offset + (r % p.group_rows);
+}
+
+// Code of coordinate `col` (a run-time index) in a row's packed words, and its replacement.
+template <int BM>
+__device__ __forceinline__ uint32_t code_at(const uint32_t (&wd)[4 * BM], int col) {
+  const int pos = col * BM;
+  uint32_t v = 0;
+#pragma unroll
+  for (int w = 0; w < 4 * BM; ++w) {
+    const int sh = pos - 32 * w;
+    if (sh >= 0 && sh < 32) v |= wd[w] >> sh;
+    if (sh < 0 && sh > -BM) v |= wd[w] << (-sh);
+  }
+  return v & ((1u << BM) - 1u);
+}
+template <int BM>
+__device__ __forceinline__ void set_code(uint32_t (&wd)[4 * BM], int col, uint32_t code) {
+  const int pos = col * BM;
+  const uint32_t m = (1u << BM) - 1u;
+#pragma unroll
+  for (int w = 0; w < 4 * BM; ++w) {
+    const int sh = pos - 32 * w;
+    if (sh >= 0 && sh < 32) wd[w] = (wd[w] & ~(m << sh)) | (code << sh);
+    if (sh < 0 && sh > -BM) wd[w] = (wd[w] & ~(m >> (-sh))) | (code >> (-sh));
+  }
+}
+
+// The three-pass product of a tensor-memory A operand (hi at a0, lo at a0 + 64
+// columns, K = 128) with a B table (hi, lo planes per 64-wide K chunk) into acc:
+// lo·Bhi, hi·Blo, then hi·Bhi.
+__device__ __forceinline__ void mma3_ts(uint32_t acc, uint32_t a0, uint32_t btab, uint32_t idesc) {
+#pragma unroll
+  for (int pass = 0; pass < 3; ++pass)
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t a = a0 + (pass == 0 ? 64u : 0u) + 8u * ks;
+      const uint32_t plane = pass == 1 ? 1u : 0u;
+      const uint64_t bd = umma_desc(btab + ((ks >> 2) * 2 + plane) * kUmmaPlaneBytes + (ks & 3) * 256, 128, 1024);
+      umma_f16_ts(acc, a, bd, idesc, (pass | ks) != 0 ? 1u : 0u);
+    }
+}
+
+template <int BM, bool PROD, bool F16>
+__global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Params p,
+                                                                 const __grid_constant__ CUtensorMap xmap) {
+  using L = Lay<F16, PROD>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte aligned base: the swizzled stages and their descriptors need it
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  unsigned char* sPi = smem;
+  unsigned char* sM = smem + kTab;
+  unsigned char* sX = smem + L::OffX;
+  float* norm_s = reinterpret_cast<float*>(smem + L::OffNorm);  // [AccBufs][128]
+  float* thr_s = reinterpret_cast<float*>(smem + L::OffThr);    // thresholds, +inf padded to 16
+  float* cen_s = reinterpret_cast<float*>(smem + L::OffCen);    // centroids
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OffBar);
+  uint64_t* x_full = bars;         // [3] TMA bytes
+  uint64_t* x_empty = bars + 3;    // [3] prep warps (+ the MMA commit for fp16 rows)
+  uint64_t* a_full = bars + 6;     // [2] prep warps
+  uint64_t* a_empty = bars + 8;    // [2] MMA commit
+  uint64_t* acc_full = bars + 10;  // [2] MMA commit
+  uint64_t* acc_empty = bars + 12; // [2] epilogue warps
+  uint64_t* nb_full = bars + 14;   // [2] prep warps: the tile's norms are in norm_s
+  uint64_t* nb_empty = bars + 16;  // [2] epilogue warps
+  uint64_t* a2_full = bars + 18;   // Prod: epilogue warps wrote the residual operand
+  uint64_t* a2_empty = bars + 19;  // MMA commit
+  uint64_t* acc2_full = bars + 20; // MMA commit
+  uint64_t* acc2_empty = bars + 21;// epilogue warps
+  uint64_t* tab_full = bars + 22;  // the B tables
+  uint64_t* drain = bars + 23;     // every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t ntiles = (p.N + kRows - 1) / kRows;
+  const int nloc = ntiles > (int64_t)blockIdx.x ? (int)((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+  const uint32_t lim = p.wait_limit;
+
+  if (tid == 0) {
+    for (int s = 0; s < L::XStages; ++s) {
+      mbar_init(&x_full[s], 1);
+      mbar_init(&x_empty[s], F16 ? 5 : 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&a_full[s], 4);
+      mbar_init(&a_empty[s], 1);
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 4);
+      mbar_init(&nb_full[s], 4);
+      mbar_init(&nb_empty[s], 4);
+    }
+    mbar_init(a2_full, 4);
+    mbar_init(a2_empty, 1);
+    mbar_init(acc2_full, 1);
+    mbar_init(acc2_empty, 4);
+    mbar_init(tab_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (tid < 16) {
+    thr_s[tid] = tid < (1 << BM) - 1 ? p.thr[tid] : INFINITY;
+    cen_s[tid] = tid < (1 << BM) ? p.cen[tid] : 0.f;
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, L::TmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- producer
+    uint32_t i = 0;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(tab_full, (uint32_t)(kTab * (PROD ? 2 : 1)));
+      bulk_g2s(sPi, p.tab_pi, kTab, tab_full);
+      if (PROD) bulk_g2s(sM, p.tab_m, kTab, tab_full);
+    }
+    for (; (int)i < nloc; ++i) {
+      const int64_t t = blockIdx.x + (int64_t)i * gridDim.x;
+      const uint32_t s = i % L::XStages;
+      if (!__all_sync(kFull, bar_wait(&x_empty[s], ((i / L::XStages) & 1u) ^ 1u, abort_flag, p.status, lim))) break;
+      if (lane == 0) {
+        // rows past N read as zeros and still count toward the box's bytes
+        mbar_arrive_expect_tx(&x_full[s], (uint32_t)L::Stage);
+#pragma unroll
+        for (int bx = 0; bx < L::Boxes; ++bx)
+          tma_load_2d(sX + s * L::Stage + bx * kBox, &xmap, bx * (128 / L::ES), (int)(t * kRows), &x_full[s]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      // every copy this CTA issued lands before it may exit (bounded)
+      const uint32_t first = i >= (uint32_t)L::XStages ? i - L::XStages : 0u;
+      for (uint32_t j = first; j < i; ++j)
+        for (uint32_t n = 0; n < kSpinLimitDev && !mbar_try_wait(&x_full[j % L::XStages], (j / L::XStages) & 1u); ++n) {
+        }
+      for (uint32_t n = 0; n < kSpinLimitDev && !mbar_try_wait(tab_full, 0u); ++n) {
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_f16(kRows, kDim);
+      const uint32_t bpi = smem_u32(sPi), bm = smem_u32(sM);
+      bool ok = bar_wait(tab_full, 0u, abort_flag, p.status, lim);
+      for (int i = 0; ok && i <= nloc; ++i) {
+        if (i < nloc) {
+          const uint32_t ab = i % L::AccBufs;
+          if (!bar_wait(&acc_empty[ab], ((i / L::AccBufs) & 1u) ^ 1u, abort_flag, p.status, lim)) break;
+          const uint32_t acc = tmem + L::ColAcc + ab * 128;
+          if constexpr (F16) {
+            const uint32_t s = i % L::XStages;
+            if (!bar_wait(&x_full[s], (i / L::XStages) & 1u, abort_flag, p.status, lim)) break;
+            tc_fence_after();
+            const uint32_t xa = smem_u32(sX + s * L::Stage);
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass)  // x·Πlo, then x·Πhi
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t ad = umma_desc_sw128(xa + (ks >> 2) * kBox + (ks & 3) * 32);
+                const uint64_t bd = umma_desc(
+                    bpi + ((ks >> 2) * 2 + (pass == 0 ? 1 : 0)) * kUmmaPlaneBytes + (ks & 3) * 256, 128, 1024);
+                umma_f16(acc, ad, bd, idesc, (pass | ks) != 0 ? 1u : 0u);
+              }
+            umma_commit(&x_empty[s]);
+          } else {
+            const uint32_t as = i % L::AStages;
+            if (!bar_wait(&a_full[as], (i / L::AStages) & 1u, abort_flag, p.status, lim)) break;
+            tc_fence_after();
+            mma3_ts(acc, tmem + as * 128, bpi, idesc);
+            umma_commit(&a_empty[as]);
+          }
+          umma_commit(&acc_full[ab]);
+        }
+        if (PROD && i >= 1) {  // the QJL product of the previous tile
+          const uint32_t ph = (uint32_t)(i - 1) & 1u;
+          if (!bar_wait(a2_full, ph, abort_flag, p.status, lim) ||
+              !bar_wait(acc2_empty, ph ^ 1u, abort_flag, p.status, lim))
+            break;
+          tc_fence_after();
+          mma3_ts(tmem + L::ColAcc2, tmem + L::ColA2, bm, idesc);
+          umma_commit(a2_empty);
+          umma_commit(acc2_full);
+        }
+      }
+      // every MMA issued completes before tensor memory is released (bounded)
+      umma_commit(drain);
+      for (uint32_t n = 0; n < kSpinLimitDev && !mbar_try_wait(drain, 0u); ++n) {
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------- prep: norms (and the split A operand of fp32 rows)
+    const int q = warp & 3, r = 32 * q + lane, sw = r & 7;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    for (int i = 0; i < nloc; ++i) {
+      const uint32_t s = i % L::XStages;
+      if (!__all_sync(kFull, bar_wait(&x_full[s], (i / L::XStages) & 1u, abort_flag, p.status, lim))) break;
+      // 16-byte chunk c of row r of a box sits at chunk c ^ (r % 8) of its 128-byte row
+      const unsigned char* row = sX + s * L::Stage + r * 128;
+      float ss = 0.f;
+      if constexpr (F16) {
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 u = *reinterpret_cast<const uint4*>(row + bx * kBox + 16 * (c ^ sw));
+            const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f2 = __half22float2(h[e]);
+              ss = fmaf(f2.x, f2.x, fmaf(f2.y, f2.y, ss));
+            }
+          }
+      } else {
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float4 f4 = *reinterpret_cast<const float4*>(row + bx * kBox + 16 * (c ^ sw));
+            ss = fmaf(f4.x, f4.x, fmaf(f4.y, f4.y, fmaf(f4.z, f4.z, fmaf(f4.w, f4.w, ss))));
+          }
+      }
+      float nrm = sqrtf(ss);
+      if (!(ss > 1e-30f && ss < 1e36f)) {
+        // squares near or past the ends of the fp32 range (or a zero row): sum
+        // again with the row scaled by the power of two that brings its
+        // largest magnitude to [1, 2)
+        float m = 0.f;
+#pragma unroll 1
+        for (int k = 0; k < kDim; ++k) {
+          const unsigned char* at = row + (k * L::ES / 128) * kBox + 16 * (((k * L::ES % 128) / 16) ^ sw) + (k * L::ES % 16);
+          const float xv = F16 ? __half2float(*reinterpret_cast<const __half*>(at)) : *reinterpret_cast<const float*>(at);
+          m = fmaxf(m, fabsf(xv));
+        }
+        nrm = 0.f;
+        if (m > 0.f) {
+          int e;
+          frexpf(m, &e);
+          const float scl = ldexpf(1.f, 1 - e);
+          float s2 = 0.f;
+#pragma unroll 1
+          for (int k = 0; k < kDim; ++k) {
+            const unsigned char* at = row + (k * L::ES / 128) * kBox + 16 * (((k * L::ES % 128) / 16) ^ sw) + (k * L::ES % 16);
+            const float xv = (F16 ? __half2float(*reinterpret_cast<const __half*>(at)) : *reinterpret_cast<const float*>(at)) * scl;
+            s2 = fmaf(xv, xv, s2);
+          }
+          nrm = sqrtf(s2) / scl;
+        }
+      }
+      if constexpr (F16) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&x_empty[s]);
+      }
+      // the tile's norms to the epilogue
+      const uint32_t ab = i % L::AccBufs;
+      if (!__all_sync(kFull, bar_wait(&nb_empty[ab], ((i / L::AccBufs) & 1u) ^ 1u, abort_flag, p.status, lim))) break;
+      norm_s[ab * kRows + r] = nrm;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&nb_full[ab]);
+      if constexpr (!F16) {
+        // A = x·2^e as fp16 hi + lo: hi plane columns [0, 64), lo plane [64, 128)
+        // of the stage, column c holding coordinates 2c and 2c + 1
+        const float sc = pow2_scale_16_32(nrm);
+        const uint32_t as = i % L::AStages;
+        if (!__all_sync(kFull, bar_wait(&a_empty[as], ((i / L::AStages) & 1u) ^ 1u, abort_flag, p.status, lim))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx) {  // 32 coordinates per box
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float4 f4 = *reinterpret_cast<const float4*>(row + bx * kBox + 16 * (c ^ sw));
+            split2(f4.x * sc, f4.y * sc, hi[2 * c], lo[2 * c]);
+            split2(f4.z * sc, f4.w * sc, hi[2 * c + 1], lo[2 * c + 1]);
+          }
+          tmem_st16(tmem + lane_base + as * 128 + 16 * bx, hi);
+          tmem_st16(tmem + lane_base + as * 128 + 64 + 16 * bx, lo);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&a_full[as]);
+          mbar_arrive(&x_empty[s]);
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue
+    const int q = warp & 3, r = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    constexpr int WW = 4 * BM;  // code words of a row
+    for (int i = 0; i < nloc; ++i) {
+      const int64_t t = blockIdx.x + (int64_t)i * gridDim.x;
+      const int64_t row = t * kRows + r;
+      const bool valid = row < p.N;
+      const uint32_t ab = i % L::AccBufs, par = (i / L::AccBufs) & 1u;
+      if (!__all_sync(kFull, bar_wait(&nb_full[ab], par, abort_flag, p.status, lim))) break;
+      const float s = norm_s[ab * kRows + r];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&nb_empty[ab]);
+      const float sc = F16 ? 1.f : pow2_scale_16_32(s);
+      const float f = s > 0.f ? (float)(p.sqrt_d / ((double)s * sc * p.pi_scale)) : 0.f;
+      const bool live = valid && s > 0.f;
+      if (!__all_sync(kFull, bar_wait(&acc_full[ab], par, abort_flag, p.status, lim))) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + lane_base + L::ColAcc + ab * 128;
+      // a3/a4: bucketize (binary search), flag coordinates near a threshold, pack
+      uint32_t wd[WW];
+#pragma unroll
+      for (int w = 0; w < WW; ++w) wd[w] = 0u;
+      uint32_t fm[4];
+      float g2 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t a[32];
+        tmem_ld32_nw(acc + 32 * c, a);
+        tmem_wait_ld();
+        uint32_t m32 = 0u;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float v = __uint_as_float(a[j]) * f;
+          bool near;
+          const uint32_t code = bucketize<BM>(v, thr_s, kMargin, near);
+          m32 |= (near ? 1u : 0u) << j;
+          put_bits<BM>(wd, (32 * c + j) * BM, code);
+          if constexpr (PROD) {
+            const float rr = v - cen_s[code];
+            g2 = fmaf(rr, rr, g2);
+          }
+        }
+        fm[c] = m32;
+      }
+      if constexpr (!PROD) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      }
+      if (!live) {
+#pragma unroll
+        for (int w = 0; w < WW; ++w) wd[w] = 0u;
+        fm[0] = fm[1] = fm[2] = fm[3] = 0u;
+        g2 = 0.f;
+      }
+      // flagged coordinates: one warp-wide float-float dot product each
+      for (;;) {
+        const uint32_t any = __ballot_sync(kFull, (fm[0] | fm[1] | fm[2] | fm[3]) != 0u);
+        if (!any) break;
+        const int src = __ffs(any) - 1;
+        int col = 0;
+        if (lane == src) {
+#pragma unroll
+          for (int g = 3; g >= 0; --g)
+            if (fm[g]) col = 32 * g + __ffs(fm[g]) - 1;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            if (g == (col >> 5)) fm[g] &= fm[g] - 1u;
+        }
+        col = __shfl_sync(kFull, col, src);
+        const float ssrc = __shfl_sync(kFull, s, src);
+        const int64_t srow = t * kRows + 32 * q + src;
+        float4 xv;
+        if constexpr (F16) {
+          const uint2 h = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.x) + srow * kDim) + lane);
+          const float2 x0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+          const float2 x1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+          xv = make_float4(x0.x, x0.y, x1.x, x1.y);
+        } else {
+          xv = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + srow * kDim) + lane);
+        }
+        const float4 pv = __ldg(reinterpret_cast<const float4*>(p.pi + (int64_t)col * kDim) + lane);
+        float sh = 0.f, sl = 0.f;
+        ff_fma(xv.x, pv.x, sh, sl);
+        ff_fma(xv.y, pv.y, sh, sl);
+        ff_fma(xv.z, pv.z, sh, sl);
+        ff_fma(xv.w, pv.w, sh, sl);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const float oh = __shfl_xor_sync(kFull, sh, o), ol = __shfl_xor_sync(kFull, sl, o);
+          const float s2 = sh + oh, bb = s2 - sh;
+          sl = sl + ol + ((sh - (s2 - bb)) + (oh - bb));
+          sh = s2;
+        }
+        if (lane == src) {
+          const float vv = (float)(((double)sh + (double)sl) * (p.sqrt_d / (double)ssrc));
+          bool nr;
+          const uint32_t code = bucketize<BM>(vv, thr_s, 0.f, nr);
+          if constexpr (PROD) {
+            const uint32_t old = code_at<BM>(wd, col);
+            const float a0 = vv - cen_s[old], a1 = vv - cen_s[code];
+            g2 += a1 * a1 - a0 * a0;
+          }
+          set_code<BM>(wd, col, code);
+        }
+      }
+      // a5 (Prod): residual operand, second product, sign bits
+      uint32_t sg[4] = {0u, 0u, 0u, 0u};
+      float gam = 0.f;
+      if constexpr (PROD) {
+        gam = live ? sqrtf(fmaxf(g2, 0.f)) / (float)p.sqrt_d : 0.f;
+        const float rsd = live ? pow2_scale_16_32(gam) / (float)p.sqrt_d : 0.f;
+        if (!__all_sync(kFull, bar_wait(a2_empty, ((uint32_t)i & 1u) ^ 1u, abort_flag, p.status, lim))) break;
+        tc_fence_after();
+        const uint32_t a2 = tmem + lane_base + L::ColA2;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t a[32];
+          tmem_ld32_nw(acc + 32 * c, a);
+          tmem_wait_ld();
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float r0 = (__uint_as_float(a[2 * j]) * f - cen_s[get_bits<BM>(wd, (32 * c + 2 * j) * BM)]) * rsd;
+            const float r1 = (__uint_as_float(a[2 * j + 1]) * f - cen_s[get_bits<BM>(wd, (32 * c + 2 * j + 1) * BM)]) * rsd;
+            split2(r0, r1, hi[j], lo[j]);
+          }
+          tmem_st16(a2 + 16 * c, hi);
+          tmem_st16(a2 + 64 + 16 * c, lo);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(a2_full);
+          mbar_arrive(&acc_empty[ab]);
+        }
+        if (!__all_sync(kFull, bar_wait(acc2_full, (uint32_t)i & 1u, abort_flag, p.status, lim))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t a[32];
+          tmem_ld32_nw(tmem + lane_base + L::ColAcc2 + 32 * c, a);
+          tmem_wait_ld();
+          uint32_t bits = 0u;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) bits |= (__uint_as_float(a[j]) >= 0.f ? 1u : 0u) << j;
+          sg[c] = live ? bits : 0u;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc2_empty);
+      }
+      // ---------------- stores
+      const int64_t dv = valid ? dest_row(p, row) : 0;
+      if (valid) {
+        p.norm[dv] = s;
+        if constexpr (PROD) {
+          p.rnorm[dv] = gam;
+          *reinterpret_cast<uint4*>(p.qjl + dv * p.QW) = make_uint4(sg[0], sg[1], sg[2], sg[3]);
+        }
+      }
+      if (p.layout == TQ_LAYOUT_TOKEN) {
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.codes + dv * p.W);
+#pragma unroll
+          for (int w = 0; w < BM; ++w) dst[w] = make_uint4(wd[4 * w], wd[4 * w + 1], wd[4 * w + 2], wd[4 * w + 3]);
+        }
+      } else {
+        // PAIR: vectors 2k and 2k+1 share a block of 2·WW words, coordinate j's
+        // two codes side by side at bits 2j·BM (even vector low).  Rows r and
+        // r+1 of the tile are lanes l and l+1: when the destination pairs them
+        // the even lane writes the block's first WW words (coordinates 0-63),
+        // the odd lane the last WW (64-127), each with its partner's codes of
+        // that half, obtained by one exchange.
+        const bool even = (lane & 1) == 0;
+        uint32_t part[2 * BM];
+#pragma unroll
+        for (int w = 0; w < 2 * BM; ++w) part[w] = __shfl_xor_sync(kFull, even ? wd[2 * BM + w] : wd[w], 1);
+        const int64_t base_row = row - (even ? 0 : 1);
+        const bool whole = p.pair_aligned && base_row + 1 < p.N;  // both rows of the pair are here
+        if (valid && whole) {
+          uint32_t out[WW];
+#pragma unroll
+          for (int w = 0; w < WW; ++w) out[w] = 0u;
+#pragma unroll
+          for (int jj = 0; jj < 64; ++jj) {
+            const uint32_t own = even ? get_bits<BM>(wd, jj * BM) : get_bits<BM>(wd, (64 + jj) * BM);
+            const uint32_t prt = get_bits<BM>(part, jj * BM);
+            put_bits<BM>(out, 2 * jj * BM, even ? own : prt);
+            put_bits<BM>(out, (2 * jj + 1) * BM, even ? prt : own);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.codes + (dv >> 1) * (2 * (int64_t)WW) + (even ? 0 : WW));
+#pragma unroll
+          for (int w = 0; w < BM; ++w) dst[w] = make_uint4(out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
+        } else if (valid) {
+          // the partner is written by another call (or not at all): update this
+          // vector's slot of the block with masked atomics
+          const int slot = (int)(dv & 1);
+          uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)WW);
+#pragma unroll 1
+          for (int w = 0; w < 2 * WW; ++w) {
+            uint32_t m = 0u, bits = 0u;
+#pragma unroll 1
+            for (int b = 0; b < 32; ++b) {
+              const int pos = 32 * w + b;  // block stream bit
+              const int j = pos / (2 * BM), k = pos % (2 * BM);
+              if (k / BM == slot) {
+                m |= 1u << b;
+                bits |= ((code_at<BM>(wd, j) >> (k % BM)) & 1u) << b;
+              }
+            }
+            atomicAnd(blk + w, ~m);
+            atomicOr(blk + w, bits);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TmemCols);
+  }
+}
+
+template <int BM, bool PROD, bool F16>
+cudaError_t launch_t(const Enc128Params& p, const CUtensorMap& xmap, cudaStream_t st) {
+  auto k = encode128_kernel<BM, PROD, F16>;
+  static PerDeviceValue attr;  // set once per device, before any stream capture
+  const cudaError_t e = smem_attr_once(attr, (const void*)k, Lay<F16, PROD>::SmemAlloc);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = (p.N + kRows - 1) / kRows;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms()));
+  k<<<grid, kThreads, Lay<F16, PROD>::SmemAlloc, st>>>(p, xmap);
+  return cudaGetLastError();
+}
+
+template <bool F16>
+cudaError_t launch_mode(const Enc128Params& p, const CUtensorMap& xmap, int bm, bool prod, cudaStream_t st) {
+  if (prod) {
+    switch (bm) {
+      case 1: return launch_t<1, true, F16>(p, xmap, st);
+      case 2: return launch_t<2, true, F16>(p, xmap, st);
+      case 3: return launch_t<3, true, F16>(p, xmap, st);
+    }
+    return cudaErrorInvalidValue;
+  }
+  switch (bm) {
+    case 1: return launch_t<1, false, F16>(p, xmap, st);
+    case 2: return launch_t<2, false, F16>(p, xmap, st);
+    case 3: return launch_t<3, false, F16>(p, xmap, st);
+    case 4: return launch_t<4, false, F16>(p, xmap, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool enc128_supported(const DevCtx& c) {
+  return c.d == kDim && c.enc_tab != nullptr && (c.mode == TQ_MSE || c.enc_tab_m != nullptr) &&
+         c.b_mse >= 1 && c.b_mse <= (c.mode == TQ_PROD ? 3 : 4);
+}
+
+tq_status launch_encode128(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
+                           int64_t offset, int64_t group_rows, int64_t group_stride, cudaStream_t stream) {
+  if (!enc128_supported(c)) return TQ_ERR_UNSUPPORTED;
+  if (N > INT32_MAX) return TQ_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
+  Enc128Params p;
+  p.x = x;
+  p.N = N;
+  p.codes = out->d_codes;
+  p.norm = out->d_norm;
+  p.qjl = out->d_qjl;
+  p.rnorm = out->d_rnorm;
+  p.tab_pi = c.enc_tab;
+  p.tab_m = c.enc_tab_m;
+  p.pi = c.pi;
+  p.pi_scale = c.pi_scale;
+  p.sqrt_d = std::sqrt((double)c.d);
+  for (int k = 0; k < 15; ++k) p.thr[k] = c.thr[k];
+  for (int k = 0; k < 16; ++k) p.cen[k] = c.cen[k];
+  p.layout = out->layout;
+  p.W = c.words_per_vec;
+  p.QW = c.qjl_words_per_vec;
+  p.offset = offset;
+  p.group_rows = group_rows;
+  p.group_stride = group_stride;
+  p.pair_aligned = (offset % 2 == 0) && (group_rows % 2 == 0 || group_rows >= N) && (group_stride % 2 == 0);
+  p.status = c.status;
+  p.wait_limit = c.wait_limit;
+  CUtensorMap xmap;
+  const tq_status ms = rows_tensor_map(&xmap, x, N, c.d, x_dtype == TQ_F16);
+  if (ms != TQ_OK) return ms;
+  const cudaError_t e = x_dtype == TQ_F16 ? launch_mode<true>(p, xmap, c.b_mse, c.mode == TQ_PROD, stream)
+                                          : launch_mode<false>(p, xmap, c.b_mse, c.mode == TQ_PROD, stream);
+  return e == cudaSuccess ? TQ_OK : set_cuda_error(e);
+}
+
+}  // namespace tq

@@ -92,6 +92,7 @@ struct UmmaParams {
   float thr[15];
   int64_t offset, group_rows, group_stride;
   int* status;
+  uint32_t wait_limit;
 };
 
 __device__ __forceinline__ int64_t dest_row(int64_t r, int64_t offset, int64_t group_rows, int64_t group_stride) {
@@ -165,30 +166,6 @@ __global__ void __launch_bounds__(256) row_norm_kernel(const void* x, int64_t N,
   }
 }
 
-// ------------------------------------------------------------------ pass 2 helpers
-// code = #{k : v >= t_k} by binary search over thr (2^BM - 1 thresholds,
-// padded with +inf to 16); near = v lies within m of a neighbouring threshold.
-template <int BM>
-__device__ __forceinline__ uint32_t bucketize(float v, const float* thr, float m, bool& near) {
-  int c = 0;
-#pragma unroll
-  for (int st = (1 << BM) >> 1; st > 0; st >>= 1)
-    if (v >= thr[c + st - 1]) c += st;
-  const float below = c > 0 ? thr[c - 1] : -INFINITY;
-  near = (v - below < m) || (thr[c] - v < m);
-  return (uint32_t)c;
-}
-
-// sh + sl += a·b, float-float (the product split exactly by an FMA)
-__device__ __forceinline__ void ff_fma(float a, float b, float& sh, float& sl) {
-  const float p = a * b;
-  const float e = fmaf(a, b, -p);
-  const float s = sh + p;
-  const float bb = s - sh;
-  sl += ((sh - (s - bb)) + (p - bb)) + e;
-  sh = s;
-}
-
 // ------------------------------------------------------------------ pass 2: GEMM, bucketize, pack
 template <int BM, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) encode_umma_kernel(const UmmaParams p,
@@ -255,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_umma_kernel(const UmmaPara
       const float sc = pow2_scale_16_32(s);
       for (int kc = 0; kc < nkc; ++kc, ++i) {
         const uint32_t xs = i % kStages;
-        if (!__all_sync(kFull, bar_wait(&x_full[xs], (i / kStages) & 1u, abort_flag, p.status))) {
+        if (!__all_sync(kFull, bar_wait(&x_full[xs], (i / kStages) & 1u, abort_flag, p.status, p.wait_limit))) {
           ok = false;
           break;
         }
@@ -297,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_umma_kernel(const UmmaPara
 #pragma unroll
         for (int j = 0; j < 16; ++j) split2(v[2 * j] * sc, v[2 * j + 1] * sc, hi[j], lo[j]);
         const uint32_t as = i % kAStages;
-        if (!__all_sync(kFull, bar_wait(&a_empty[as], ((i / kAStages) & 1u) ^ 1u, abort_flag, p.status))) {
+        if (!__all_sync(kFull, bar_wait(&a_empty[as], ((i / kAStages) & 1u) ^ 1u, abort_flag, p.status, p.wait_limit))) {
           ok = false;
           break;
         }
@@ -321,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_umma_kernel(const UmmaPara
       const int ob = (int)(t % nob);
       const int64_t row = rt * kTM + rl;
       const bool valid = row < p.N;
-      if (!__all_sync(kFull, bar_wait(acc_full, tl & 1u, abort_flag, p.status))) break;
+      if (!__all_sync(kFull, bar_wait(acc_full, tl & 1u, abort_flag, p.status, p.wait_limit))) break;
       tc_fence_after();
       const int64_t dv = valid ? dest_row(row, p.offset, p.group_rows, p.group_stride) : 0;
       const float s = valid ? p.norm[dv] : 0.f;
@@ -465,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode_umma_kernel(const UmmaPara
       const int ob = (int)(t % nob);
       for (int kc = 0; kc < nkc; ++kc, ++i) {
         const uint32_t s = i % kStages, ph = ((i / kStages) & 1u) ^ 1u;
-        if (!__all_sync(kFull, bar_wait(&x_empty[s], ph, abort_flag, p.status) &&
-                                   bar_wait(&b_empty[s], ph, abort_flag, p.status))) {
+        if (!__all_sync(kFull, bar_wait(&x_empty[s], ph, abort_flag, p.status, p.wait_limit) &&
+                                   bar_wait(&b_empty[s], ph, abort_flag, p.status, p.wait_limit))) {
           ok = false;
           break;
         }
@@ -498,16 +475,16 @@ __global__ void __launch_bounds__(kThreads, 1) encode_umma_kernel(const UmmaPara
     uint32_t i = 0, tl = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tl) {
-      if (!bar_wait(acc_empty_a, (tl & 1u) ^ 1u, abort_flag, p.status)) break;
+      if (!bar_wait(acc_empty_a, (tl & 1u) ^ 1u, abort_flag, p.status, p.wait_limit)) break;
       tc_fence_after();
       for (int kc = 0; kc < nkc; ++kc, ++i) {
         const uint32_t s = i % kStages, as = i % kAStages;
-        if (kc == nkc / 2 && !bar_wait(acc_empty_b, (tl & 1u) ^ 1u, abort_flag, p.status)) {
+        if (kc == nkc / 2 && !bar_wait(acc_empty_b, (tl & 1u) ^ 1u, abort_flag, p.status, p.wait_limit)) {
           ok = false;
           break;
         }
-        if (!bar_wait(&b_full[s], (i / kStages) & 1u, abort_flag, p.status) ||
-            !bar_wait(&a_full[as], (i / kAStages) & 1u, abort_flag, p.status)) {
+        if (!bar_wait(&b_full[s], (i / kStages) & 1u, abort_flag, p.status, p.wait_limit) ||
+            !bar_wait(&a_full[as], (i / kAStages) & 1u, abort_flag, p.status, p.wait_limit)) {
           ok = false;
           break;
         }
@@ -581,6 +558,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace
 
+tq_status rows_tensor_map(CUtensorMap* map, const void* x, int64_t N, int d, bool f16) {
+  const int es = f16 ? 2 : 4;
+  const cuuint64_t gdim[2] = {(cuuint64_t)d, (cuuint64_t)N};
+  const cuuint64_t gstride[1] = {(cuuint64_t)d * es};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)kTM};
+  const cuuint32_t estride[2] = {1u, 1u};
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return TQ_ERR_CUDA;
+  const CUresult r = encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                            const_cast<void*>(x), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TQ_OK : TQ_ERR_INVALID_ARG;
+}
+
 bool umma_supported(const DevCtx& c) {
   return c.d > kChunk && c.d % kTN == 0 && c.mode == TQ_MSE && c.b_mse >= 1 && c.b_mse <= 4 && c.umma_tab != nullptr;
 }
@@ -621,22 +613,10 @@ tq_status launch_encode_umma(const DevCtx& c, const void* x, int x_dtype, int64_
   p.group_rows = group_rows;
   p.group_stride = group_stride;
   p.status = c.status;
-  // x as a 2-D tensor [N][d]: boxes of 128 rows x 128 bytes, 128-byte swizzle
+  p.wait_limit = c.wait_limit;
   CUtensorMap xmap;
-  {
-    const int es = f16 ? 2 : 4;
-    const cuuint64_t gdim[2] = {(cuuint64_t)c.d, (cuuint64_t)N};
-    const cuuint64_t gstride[1] = {(cuuint64_t)c.d * es};
-    const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)kTM};
-    const cuuint32_t estride[2] = {1u, 1u};
-    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    if (!encode) return TQ_ERR_CUDA;
-    const CUresult r = encode(
-        &xmap, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(x), gdim,
-        gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return TQ_ERR_INVALID_ARG;
-  }
+  const tq_status ms = rows_tensor_map(&xmap, x, N, c.d, f16);
+  if (ms != TQ_OK) return ms;
   const cudaError_t e =
       f16 ? launch_bm<true>(p, xmap, c.b_mse, stream) : launch_bm<false>(p, xmap, c.b_mse, stream);
   return e == cudaSuccess ? TQ_OK : set_cuda_error(e);

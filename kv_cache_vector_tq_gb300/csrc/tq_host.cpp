@@ -483,6 +483,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   v.b_mse = b_mse;
   v.mode = mode;
   v.rot = rot_kind;
+  v.wait_limit = kWaitLimitDefault;
   v.words_per_vec = words_per_vector(d, b_mse);
   v.qjl_words_per_vec = mode == TQ_PROD ? words_per_vector(d, 1) : 0;
   v.sqrt_d = (float)std::sqrt((double)d);
@@ -521,9 +522,10 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   const bool wht_path = rot_kind == TQ_ROT_HADAMARD && mode == TQ_MSE && v.had_m >= 32 && v.had_m <= 256;
   const bool umma_path = d > kChunk && d % kUmmaTN == 0 && mode == TQ_MSE && !wht_path;
   std::vector<uint2> frag_pi, frag_m;
-  std::vector<uint16_t> umma;
+  std::vector<uint16_t> umma, enc128, enc128m;
   if (d <= kChunk) encoder_fragments(c->h_pi, d, v.pi_scale, frag_pi, false);
   if (umma_path) umma_tiles(c->h_pi, d, v.pi_scale, umma);
+  if (d == kChunk) umma_tiles(c->h_pi, d, v.pi_scale, enc128);  // the tcgen05 encoder at d = 128
   std::vector<double> M;
   if (mode == TQ_PROD) {
     M.assign(dd, 0.0);  // M = S·Πᵀ
@@ -539,6 +541,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
     for (double x : M) mx = std::max(mx, std::fabs(x));
     v.m_scale = (float)pow2_near(4.0 / std::max(mx, 1e-30));
     encoder_fragments(M.data(), d, v.m_scale, frag_m, true);
+    if (d == kChunk) umma_tiles(M.data(), d, v.m_scale, enc128m);
   }
   std::vector<float> pi32(dd), s32, slices, signs32;
   if (rot_kind == TQ_ROT_HADAMARD) {
@@ -583,7 +586,9 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   size_t o_sg = o_sl + al(slices.size() * sizeof(float));
   size_t o_ss = o_sg + al(signs32.size() * sizeof(float));
   size_t o_um = o_ss + al(sslices.size() * sizeof(float));
-  size_t o_lut = o_um + al(umma.size() * sizeof(uint16_t));
+  size_t o_e1 = o_um + al(umma.size() * sizeof(uint16_t));
+  size_t o_e2 = o_e1 + al(enc128.size() * sizeof(uint16_t));
+  size_t o_lut = o_e2 + al(enc128m.size() * sizeof(uint16_t));
   size_t o_st = o_lut + al(lut.size() * sizeof(uint32_t));
   size_t total = o_st + 256;
   void* dmem = nullptr;
@@ -608,6 +613,8 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   if (e == cudaSuccess) e = up(o_sg, signs32.data(), signs32.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_ss, sslices.data(), sslices.size() * sizeof(float));
   if (e == cudaSuccess) e = up(o_um, umma.data(), umma.size() * sizeof(uint16_t));
+  if (e == cudaSuccess) e = up(o_e1, enc128.data(), enc128.size() * sizeof(uint16_t));
+  if (e == cudaSuccess) e = up(o_e2, enc128m.data(), enc128m.size() * sizeof(uint16_t));
   if (e == cudaSuccess) e = up(o_lut, lut.data(), lut.size() * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(base + o_st, 0, 256);
   if (e != cudaSuccess) {
@@ -621,6 +628,8 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   c->d_bytes = total;
   v.enc_pi = d <= kChunk ? (const uint2*)(base + o_pi) : nullptr;
   v.umma_tab = umma_path ? (const unsigned char*)(base + o_um) : nullptr;
+  v.enc_tab = enc128.empty() ? nullptr : (const unsigned char*)(base + o_e1);
+  v.enc_tab_m = enc128m.empty() ? nullptr : (const unsigned char*)(base + o_e2);
   v.s_slices = sslices.empty() ? nullptr : (const float4*)(base + o_ss);
   v.enc_m = mode == TQ_PROD ? (const uint2*)(base + o_m) : nullptr;
   v.pi = (const float*)(base + o_p32);
@@ -630,6 +639,12 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   v.lut = (const uint32_t*)(base + o_lut);
   v.status = (int*)(base + o_st);
   *out = reinterpret_cast<tq_ctx*>(c);
+  return TQ_OK;
+}
+
+tq_status tq_ctx_set_wait_limit(tq_ctx* ctx, uint32_t polls) {
+  if (!ctx) return TQ_ERR_INVALID_ARG;
+  reinterpret_cast<Ctx*>(ctx)->dev.wait_limit = polls;
   return TQ_OK;
 }
 
@@ -705,6 +720,8 @@ tq_status tq_encode(const tq_ctx* ctx, const void* d_x, int x_dtype, int64_t N,
     return launch_encode_wht(v, d_x, x_dtype, N, out, offset, group_rows, group_stride, (cudaStream_t)stream);
   if (wide)
     return launch_encode_umma(v, d_x, x_dtype, N, out, offset, group_rows, group_stride, (cudaStream_t)stream);
+  if (enc128_supported(v))
+    return launch_encode128(v, d_x, x_dtype, N, out, offset, group_rows, group_stride, (cudaStream_t)stream);
   return launch_encode(v, d_x, x_dtype, N, out, offset, group_rows, group_stride,
                        (cudaStream_t)stream);
 }

@@ -1,6 +1,7 @@
 // Internal declarations shared by the host code and the kernels of libtq.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -22,8 +23,12 @@ constexpr int kUmmaTN = 128;
 constexpr int kUmmaKC = 64;
 constexpr int kUmmaPlaneBytes = kUmmaTN * kUmmaKC * 2;
 
+// Polls a bounded pipeline wait makes before it gives up (tq_debug_set_wait_limit).
+constexpr uint32_t kWaitLimitDefault = 1u << 22;
+
 struct DevCtx {
   int d, b, b_mse, mode, rot;
+  uint32_t wait_limit;   // polls of a bounded pipeline wait before it gives up
   int words_per_vec, qjl_words_per_vec;
   float sqrt_d;
   float pi_scale;        // encoder B operand = pi_scale * Π (power of two)
@@ -38,6 +43,8 @@ struct DevCtx {
   const float4* pi_slices;  // d = 128: Π[r][32c + 4j .. +3] at (c·8 + j)·128 + r (decode rotation)
   const float4* s_slices;   // d = 128, Prod: S in the same slices (decode S-rotation of the query)
   const unsigned char* umma_tab;  // d > 128, MSE: pi_scale·Π hi/lo tiles for the tcgen05 encoder (else null)
+  const unsigned char* enc_tab;    // d = 128: pi_scale·Π hi/lo tiles for the tcgen05 encoder (else null)
+  const unsigned char* enc_tab_m;  // d = 128, Prod: m_scale·S·Πᵀ in the same layout (else null)
   const float* signs;    // Hadamard rotation: σ, d entries of ±1 (else null)
   int had_m, had_p;      // Hadamard rotation: H = H12 ⊗ H_m (had_p = 12) or H_m (had_p = 1)
   const uint32_t* lut;   // pair table: 2^(2 b_mse) fp16x2 entries (alpha-scaled)
@@ -82,6 +89,12 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
                       const tq_codes* V, int B, int Hq, int Hkv, int64_t seq, int64_t cap,
                       float scale, float* out, void* ws, cudaStream_t stream);
 bool wht_supported(const DevCtx& c);
+bool enc128_supported(const DevCtx& c);
+tq_status launch_encode128(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
+                           int64_t offset, int64_t group_rows, int64_t group_stride, cudaStream_t stream);
+// 2-D tensor map of N rows of d fp32/fp16 values for TMA loads of boxes of
+// 128 rows x 128 bytes in the 128-byte swizzle.
+tq_status rows_tensor_map(CUtensorMap* map, const void* x, int64_t N, int d, bool f16);
 bool umma_supported(const DevCtx& c);
 tq_status launch_encode_umma(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
                              int64_t offset, int64_t group_rows, int64_t group_stride, cudaStream_t stream);

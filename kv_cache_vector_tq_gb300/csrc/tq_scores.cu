@@ -125,6 +125,7 @@ struct ScoreParams {
   float gscale;                // √(π/2)/√d: γ' = γ·gscale
   float* scores;
   int* status;
+  uint32_t wait_limit;
 };
 
 template <int BM, bool PROD>
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) scores_kernel(const ScoreParams p
       for (int w = 0; w < 4; ++w) sb[w] = sw[w];
       if (t + gridDim.x < ntiles) fetch(t + gridDim.x);  // next tile's words in flight
       const uint32_t s = i & 1u;
-      if (!__all_sync(kFull, bar_wait(&a_empty[s], ((i >> 1) & 1u) ^ 1u, abort_flag, p.status))) break;
+      if (!__all_sync(kFull, bar_wait(&a_empty[s], ((i >> 1) & 1u) ^ 1u, abort_flag, p.status, p.wait_limit))) break;
       unsigned char* A = sA + s * kAStage;
       // 128 coordinates = 16 core rows of 8 fp16 (pairs from the table)
 #pragma unroll
@@ -230,13 +231,13 @@ __global__ void __launch_bounds__(kThreads, 1) scores_kernel(const ScoreParams p
     // ---------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_f16(kKeyTile, kQTile);
-      bool ok = bar_wait(b_full, 0u, abort_flag, p.status);
+      bool ok = bar_wait(b_full, 0u, abort_flag, p.status, p.wait_limit);
       const uint32_t bbase = smem_u32(sB);
       uint32_t i = 0;
       for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++i) {
         const uint32_t s = i & 1u, b = i % kAccBufs;
-        if (!bar_wait(&acc_empty[b], ((i / kAccBufs) & 1u) ^ 1u, abort_flag, p.status) ||
-            !bar_wait(&a_full[s], (i >> 1) & 1u, abort_flag, p.status)) {
+        if (!bar_wait(&acc_empty[b], ((i / kAccBufs) & 1u) ^ 1u, abort_flag, p.status, p.wait_limit) ||
+            !bar_wait(&a_full[s], (i >> 1) & 1u, abort_flag, p.status, p.wait_limit)) {
           ok = false;
           break;
         }
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) scores_kernel(const ScoreParams p
       const bool ok = key < p.N;
       const float sc = ok ? __ldg(p.norm + p.first + key) * p.inv_sd : 0.f;
       const float gq = (PROD && ok) ? __ldg(p.rnorm + p.first + key) * p.gscale : 0.f;
-      if (!__all_sync(kFull, bar_wait(&acc_full[b], (i / kAccBufs) & 1u, abort_flag, p.status))) break;
+      if (!__all_sync(kFull, bar_wait(&acc_full[b], (i / kAccBufs) & 1u, abort_flag, p.status, p.wait_limit))) break;
       tc_fence_after();
       const uint32_t acc = tmem + lane_base + b * kAccCols;
       float* out = p.scores + (int64_t)p.m0 * p.N + key;
@@ -296,6 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1) scores_kernel(const ScoreParams p
     }
   }
 
+  // the B operand's bulk copy lands before the CTA may exit, also when a wait
+  // gave up before the MMA issuer saw it complete (bounded)
+  if (tid == 0)
+    for (uint32_t n = 0; n < kSpinLimitDev && !mbar_try_wait(b_full, 0u); ++n) {
+    }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -348,6 +354,7 @@ tq_status launch_scores(const DevCtx& c, const float* q, int M, const tq_codes* 
   p.gscale = (float)(1.2533141373155002 / std::sqrt((double)c.d));
   p.scores = scores;
   p.status = c.status;
+  p.wait_limit = c.wait_limit;
   const bool prod = c.mode == TQ_PROD;
   for (int m0 = 0; m0 < M; m0 += kQTile) {
     p.m0 = m0;
