@@ -64,10 +64,15 @@ def oracle_codebook(d, b):
     return _cb_cache[(d, b)]
 
 
-def make_pair(seed, d, b, mode=tq.TQ_MSE):
-    """Product context and the oracle's own rotation/QJL matrices for one seed."""
-    G = synth.gaussian_matrix(seed, d)
+def make_pair(seed, d, b, mode=tq.TQ_MSE, rot="dense"):
+    """Product context and the oracle's own rotation/QJL matrices for one seed
+    (rot "dense": Haar rotation from QR; "hadamard": H·diag(σ)/√d)."""
     S = synth.qjl_matrix(seed, d) if mode == tq.TQ_PROD else None
+    if rot == "hadamard":
+        sig = synth.hadamard_signs(seed, d)
+        ctx = tq.Context(d, b, mode, tq.TQ_ROT_HADAMARD, sig, S)
+        return ctx, orot.hadamard_rotation(d, sig), S
+    G = synth.gaussian_matrix(seed, d)
     ctx = tq.Context(d, b, mode, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(G), S)
     return ctx, orot.haar_rotation(G), S
 
@@ -312,14 +317,14 @@ def test_scores_prod_config3_sample():
 
 
 # ------------------------------------------------------------------ decode
-def run_decode(b_k, b_v, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float16):
+def run_decode(b_k, b_v, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float16, rot="dense"):
     d = 128
     cap = cap or (seq + 15) // 16 * 16
-    kctx, Pi_k, _ = make_pair(seed, d, b_k)
+    kctx, Pi_k, _ = make_pair(seed, d, b_k, rot=rot)
     if b_v == b_k:
         vctx, Pi_v = kctx, Pi_k
     else:
-        vctx, Pi_v, _ = make_pair(seed, d, b_v)
+        vctx, Pi_v, _ = make_pair(seed, d, b_v, rot=rot)
     Kh, Vh = synth.kv_layer(seed, 0, B, Hkv, seq, d)
     Kc = tq.CodeSet(kctx, B * Hkv * cap, tq.TQ_LAYOUT_TOKEN)
     Vc = tq.CodeSet(vctx, B * Hkv * cap, tq.TQ_LAYOUT_PAIR)
@@ -370,6 +375,16 @@ def test_decode_gqa_variants(gqa):
 
 def test_decode_asymmetric_bits():
     run_decode(4, 2, 1, 16, 4, 2048)
+
+
+@pytest.mark.parametrize("b", [2, 3, 4])
+def test_decode_hadamard_rotation(b):
+    """Decode attention over K/V caches encoded with the randomized Hadamard
+    rotation Π = H·diag(σ)/√d ("TurboQuant 和 RotorQuant 的真相", chapter 7,
+    WHT vs random rotation): keys by the fast-transform encoder, values (PAIR
+    layout) by the dense encoder with the same Π; the oracle rotates with its
+    own Hadamard matrix."""
+    run_decode(b, b, 1, 32, 8, 3001, seed=5, rot="hadamard")
 
 
 def run_decode_prod(b_k, b_v, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float16):
@@ -489,8 +504,11 @@ def test_prod_full_config3_sampled():
 
 
 def test_decode_config4_layer_subset():
-    """Long-context shape: 64 query / 8 KV heads, seq 131072, b=3 K/V; the
-    oracle checks the query heads of two KV heads on the full sequence."""
+    """Long-context shape: 64 query / 8 KV heads, seq 131072, b=3 K/V.  The
+    prefill encode of the layer (2 x 8 x 131072 fp16 vectors) is checked on a
+    seeded sample of 4096 tokens of every KV head (codes outside the band and
+    norms against the oracle's encoder); the oracle checks the attention of
+    the query heads of two KV heads on the full sequence."""
     d, b, Hq, Hkv, seq = 128, 3, 64, 8, 131072
     cap = seq
     ctx, Pi, _ = make_pair(0, d, b)
@@ -507,6 +525,20 @@ def test_decode_config4_layer_subset():
     torch.cuda.synchronize()
     assert ctx.poll() == tq.TQ_OK
     cb = oracle_codebook(d, b)
+    # prefill encode: sampled tokens of every KV head, K and V
+    rng = np.random.default_rng(44)
+    for arr, cs in ((Kh, Kc), (Vh, Vc)):
+        for kvh in range(Hkv):
+            toks = np.sort(rng.choice(seq, 4096, replace=False))
+            X = arr[0, kvh, toks].astype(np.float64)
+            ref, s_ref, v = oq.mse_quantize(X, Pi, cb["centroids"], math.sqrt(d))
+            band = oq.near_threshold(v, cb["centroids"])
+            allidx = tq.tq_unpack_indices(cs, kvh * cap, seq)
+            got = allidx[toks].astype(np.int64)
+            assert not ((got != ref) & ~band).any(), (kvh, int(((got != ref) & ~band).sum()))
+            assert band_count_ok(band, cb["centroids"])
+            nrm = cs.norm[kvh * cap: kvh * cap + seq].cpu().numpy()[toks].astype(np.float64)
+            np.testing.assert_allclose(nrm, s_ref, rtol=1e-6)
     gqa = Hq // Hkv
     for kvh in (0, 5):
         ki = tq.tq_unpack_indices(Kc, kvh * cap, seq)
@@ -523,15 +555,17 @@ def test_decode_config4_layer_subset():
 
 
 # ------------------------------------------------------------------ fused decode step (append + attend)
-@pytest.mark.parametrize("b,B,Hq,Hkv,seq", [(4, 1, 32, 8, 16384), (2, 1, 32, 8, 16383),
-                                             (3, 2, 16, 2, 1001), (3, 1, 64, 8, 4096), (4, 1, 8, 8, 17)])
-def test_decode_step_appends_then_attends(b, B, Hq, Hkv, seq):
+@pytest.mark.parametrize("b,B,Hq,Hkv,seq,rot", [(4, 1, 32, 8, 16384, "dense"), (2, 1, 32, 8, 16383, "dense"),
+                                                 (3, 2, 16, 2, 1001, "dense"), (3, 1, 64, 8, 4096, "dense"),
+                                                 (4, 1, 8, 8, 17, "dense"), (3, 1, 32, 8, 2047, "hadamard"),
+                                                 (4, 1, 32, 8, 16384, "hadamard")])
+def test_decode_step_appends_then_attends(b, B, Hq, Hkv, seq, rot):
     """The step encodes the new token's K and V into position seq-1 (same codes
     as the oracle's encoder, outside the near-threshold band) and attends over
-    all seq tokens including it."""
+    all seq tokens including it (dense Haar or randomized Hadamard rotation)."""
     d = 128
     cap = (seq + 15) // 16 * 16 + 16
-    ctx, Pi, _ = make_pair(1, d, b)
+    ctx, Pi, _ = make_pair(1, d, b, rot=rot)
     Kh, Vh = synth.kv_layer(1, 0, B, Hkv, seq, d)
     Kc = tq.CodeSet(ctx, B * Hkv * cap, tq.TQ_LAYOUT_TOKEN)
     Vc = tq.CodeSet(ctx, B * Hkv * cap, tq.TQ_LAYOUT_PAIR)
