@@ -49,7 +49,8 @@ def parse_args():
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--bits", type=int, default=4, choices=[1, 2, 3, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="decode", choices=["decode", "encode", "scores", "longctx", "keys"],
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "encode", "scores", "longctx", "keys", "prefill"],
                     help="decode (the headline) or a secondary workload (see bench_workloads.py)")
     ap.add_argument("--dim", type=int, default=3072, help="encode: vector dimension")
     ap.add_argument("--rows", type=int, default=100_000, help="encode: number of vectors")
@@ -489,7 +490,7 @@ def main():
     elif args.workload != "decode":
         import bench_workloads as bw
         run = {"encode": bw.run_encode, "scores": bw.run_scores, "longctx": bw.run_longctx,
-               "keys": bw.run_keys}[args.workload]
+               "keys": bw.run_keys, "prefill": bw.run_prefill}[args.workload]
         line = run(args, world, rank, local, ROOT, Clocks,
                    {"encode": cpu_encode_baseline, "scores": cpu_scores_baseline})
     else:

@@ -212,6 +212,81 @@ def run_encode(args, world, rank, local, root, clocks_cls, cpu):
     return line if rank == 0 else None
 
 
+# ---------------------------------------------------------------- d = 128 encode (prefill, Prod keys)
+def run_prefill(args, world, rank, local, root, clocks_cls, cpu):
+    """The d = 128 encoder on its two large workloads: one layer's prefill at
+    the long-context shape (K and V of 8 KV heads x 131072 tokens, fp16, b = 3,
+    K in TOKEN and V in PAIR layout) and the Prod encode of 1M unit-norm fp32
+    keys (b = 3: 2-bit MSE + 1-bit QJL).  value = the prefill's Mvec/s."""
+    import torch
+
+    import kv_cache_vector_tq_gb300 as tq
+    from kv_cache_vector_tq_gb300 import synth
+    torch.cuda.set_device(local)
+    d, HKV, SEQ = 128, 8, 131072
+    hbm, bf16, kind = _peaks(root)
+    stream = torch.cuda.Stream()
+    gen = torch.Generator(device="cuda").manual_seed(77 + rank)
+    # ---- prefill: K (TOKEN) and V (PAIR), fp16 rows
+    ctx = tq.Context(d, 3, tq.TQ_MSE, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(synth.gaussian_matrix(0, d)))
+    kv = torch.randn((2, HKV * SEQ, d), generator=gen, device="cuda")
+    kv[:, :, :4] *= 10.0
+    kv = kv.half()
+    K = tq.CodeSet(ctx, HKV * SEQ, tq.TQ_LAYOUT_TOKEN)
+    V = tq.CodeSet(ctx, HKV * SEQ, tq.TQ_LAYOUT_PAIR)
+
+    def prefill():
+        tq.tq_encode(ctx, kv[0], K, 0, SEQ, SEQ, stream=stream)
+        tq.tq_encode(ctx, kv[1], V, 0, SEQ, SEQ, stream=stream)
+
+    total_ms, clk = _timed(prefill, args.steps, args.warmup, stream, clocks_cls, local)
+    assert ctx.poll() == tq.TQ_OK
+    nvec = 2 * HKV * SEQ
+    sec = total_ms * 1e-3
+    mvec = world * args.steps * nvec / sec / 1e6
+    bpv = 2 * d + 3 * d // 8 + 4                 # fp16 row in, 3-bit codes and the norm out
+    fpv = 2 * 2 * d * d                          # two fp16 passes (x exact, Π hi + lo)
+    t_hbm, t_tc = bpv / (hbm * 1e9), fpv / (bf16 * 1e12)
+    ach_gbs = args.steps * nvec * bpv / sec / 1e9
+    roof = {"bound": "hbm" if t_hbm >= t_tc else "tensor", "achieved": round(ach_gbs, 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(max(t_hbm, t_tc) * nvec * args.steps / sec, 4),
+            "traffic": traffic(root, "encode128_prefill_b3"), "kernel": "encode128_kernel<3,0,1> (K then V)",
+            "peak_kind": kind, "bytes_per_vector": bpv, "tensor_flops_per_vector": fpv, "passes": 2,
+            "roofline_rule": "max(bytes / HBM peak, issued fp16 flops / bf16 dense peak)"}
+    del kv
+    # ---- Prod encode of 1M unit-norm fp32 keys (the Prod-scores workload's setup)
+    pctx = tq.Context(d, 3, tq.TQ_PROD, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(synth.gaussian_matrix(0, d)),
+                      synth.qjl_matrix(0, d))
+    NK = 1 << 20
+    keys = torch.randn((NK, d), generator=gen, device="cuda")
+    keys /= keys.norm(dim=1, keepdim=True)
+    cs = tq.CodeSet(pctx, NK, tq.TQ_LAYOUT_TOKEN)
+    pms, _ = _timed(lambda: tq.tq_encode(pctx, keys, cs, stream=stream), args.steps, args.warmup, stream,
+                    clocks_cls, local)
+    assert pctx.poll() == tq.TQ_OK
+    psec = pms * 1e-3
+    pbpv = 4 * d + 2 * d // 8 + d // 8 + 8       # fp32 row in; 2-bit codes, sign words, s and γ out
+    pfpv = 6 * 2 * d * d                         # three split passes for Π·u and three for (S·Πᵀ)·r
+    pt_hbm, pt_tc = pbpv / (hbm * 1e9), pfpv / (bf16 * 1e12)
+    prod = {"workload": "TurboQuant_Prod b=3 encode, d=128, 1M unit-norm fp32 keys",
+            "value": round(world * args.steps * NK / psec / 1e6, 2), "unit": "Mvec/s",
+            "ms_per_call": round(pms / args.steps, 4),
+            "roofline": {"bound": "hbm" if pt_hbm >= pt_tc else "tensor",
+                         "frac": round(max(pt_hbm, pt_tc) * NK * args.steps / psec, 4),
+                         "achieved_tflops": round(args.steps * NK * pfpv / psec / 1e12, 1), "peak_tflops": bf16,
+                         "kernel": "encode128_kernel<2,1,0>", "passes": 6, "tensor_flops_per_vector": pfpv,
+                         "bytes_per_vector": pbpv}}
+    line = _line(args, world, "encode Mvec/s", round(mvec, 2), "Mvec/s", total_ms / args.steps,
+                 "f16 in, u3 codes, f16 tensor products (x exact, Π hi + lo), f32 accumulate",
+                 "synthetic (device-generated N(0,1) fp16 K/V, channels 0-3 x10; unit-norm Gaussian keys)",
+                 {"workload": "prefill encode of one long-context layer: K and V of 8 KV heads x 131072 tokens, "
+                              "d=128, TurboQuant_MSE b=3 (K TOKEN, V PAIR layout)",
+                  "vectors": nvec, "l2": f"inputs larger than L2: {nvec * 2 * d / 1e9:.2f} GB of rows per call",
+                  "prod_encode": prod},
+                 roof, None, args.steps * 2, clk)
+    return line if rank == 0 else None
+
+
 # ---------------------------------------------------------------- Prod scores
 def run_scores(args, world, rank, local, root, clocks_cls, cpu):
     import numpy as np

@@ -29,7 +29,7 @@
 // fp16 hi + lo into tensor memory, and a second three-pass product with
 // (m_scale·S·Πᵀ) gives p = S·r up to a positive factor; bit_j = [p_j >= 0].
 //
-// Warp roles (10 warps):
+// Warp roles (14 warps):
 //   0     producer: the B operand tables once (bulk copy), then per tile one
 //         2-D TMA load per 128-byte column box of the x tile.
 //   1     MMA issuer (one thread).
@@ -37,10 +37,13 @@
 //         s = ‖x‖ from the staged tile (fp32 sums; a row whose sum leaves
 //         (1e-30, 1e36) is summed again scaled by a power of two); fp32 rows:
 //         the split A operand into tensor memory.
-//   6-9   epilogue: thread = row: v = acc·√d/(s·scales), bucketize (binary
-//         search over the thresholds) with a near-threshold flag, pack in
-//         registers, recompute flagged coordinates, (Prod: residual, second
-//         product, sign bits), store codes, norm (γ, sign words).
+//   6-13  epilogue: thread = row, two warps per TMEM lane quadrant, each for
+//         64 of the 128 columns, taken as two 32-column chunks (a chunk's
+//         codes are BM whole words of the row's stream): v = acc·√d/(s·scales),
+//         bucketize (a branch-free count over the thresholds, kept as kernel
+//         constants) with a near-threshold flag, pack in registers, recompute
+//         flagged coordinates, store; Prod: γ over both halves, the residual
+//         operand, the second product, sign bits.
 // All waits are bounded (tq_ctx_set_wait_limit); a wait that gives up sets the
 // abort flag, which every role polls, and bit 0 of the status word.
 #include <cuda.h>
@@ -60,7 +63,7 @@ constexpr int kRows = 128;                   // rows per tile = TMEM lanes = MMA
 constexpr int kDim = 128;                    // d = MMA N = K
 constexpr int kBox = kRows * 128;            // one 128-byte column box of the x tile: 16 KB
 constexpr int kTab = 4 * kUmmaPlaneBytes;    // B operand of one 128 x 128 matrix: (hi, lo) x 2 K chunks
-constexpr int kThreads = 10 * 32;
+constexpr int kThreads = 14 * 32;
 constexpr float kMargin = 8e-6f;             // recomputation band around each threshold (v units)
 
 template <bool F16, bool PROD>
@@ -80,10 +83,10 @@ struct Lay {
   static constexpr uint32_t TmemCols = Cols <= 256 ? 256 : 512;
   static constexpr int OffX = kTab * (PROD ? 2 : 1);
   static constexpr int OffNorm = OffX + XStages * Stage;
-  static constexpr int OffThr = OffNorm + AccBufs * kRows * 4;
+  static constexpr int OffThr = OffNorm + (AccBufs + 4) * kRows * 4;  // norms, then (Prod) γ² halves
   static constexpr int OffCen = OffThr + 16 * 4;
   static constexpr int OffBar = OffCen + 16 * 4;
-  static constexpr int NBar = 24;
+  static constexpr int NBar = 26;
   static constexpr int Smem = OffBar + NBar * 8 + 16;
   static constexpr int SmemAlloc = Smem + 1024;  // slack to align the base to 1024 bytes
   static_assert(Cols <= 512, "tensor memory");
@@ -101,26 +104,91 @@ struct Enc128Params {
   const unsigned char* tab_m;   // Prod: m_scale·S·Πᵀ in the same layout
   const float* pi;              // Π, fp32 row-major (recomputation)
   float pi_scale;
-  double sqrt_d;
+  double sqrt_d;   // recomputation (rare) in fp64
+  float sqrt_df;
   float thr[15];
   float cen[16];
+  int sym;  // thresholds symmetric about 0 (thr[H] = 0, thr[H-1-j] = -thr[H+1+j], H = 2^(BM-1) - 1)
   int layout, W, QW, pair_aligned;
   int64_t offset, group_rows, group_stride;
   int* status;
   uint32_t wait_limit;
 };
 
+// Destination vector of row r (< N <= 2^31 - 1): 32-bit division only.
 __device__ __forceinline__ int64_t dest_row(const Enc128Params& p, int64_t r) {
-  return (r / p.group_rows) * p.group_stride + p.offset + (r % p.group_rows);
+  if (p.group_rows >= p.N) return p.offset + r;
+  const uint32_t rr = (uint32_t)r, gr = (uint32_t)p.group_rows, gq = rr / gr;
+  return (int64_t)gq * p.group_stride + p.offset + (int64_t)(rr - gq * gr);
 }
 
-// Code of coordinate `col` (a run-time index) in a row's packed words, and its replacement.
+// Branch-free bucketize against thresholds held as kernel constants (every
+// index is known at compile time, so no shared-memory loads and no dependent
+// chain): code = #{k : v >= t_k}, near = v lies within m of some threshold.
+// Symmetric codebooks (the ones tq_codebook_build makes) compare |v| with the
+// H = 2^(BM-1) - 1 positive thresholds only; a value exactly equal to a
+// negative threshold then counts as below it, which differs from the
+// definition only at exact ties, all inside the band that parity excuses.
+template <int BM, bool SYM>
+__device__ __forceinline__ uint32_t bucketize_c(float v, const float (&thr)[15], float m, bool& near) {
+  constexpr int H = (1 << (BM - 1)) - 1;
+  if constexpr (SYM) {
+    const float a = fabsf(v);
+    float dmin = a;
+    int n = 0;
+#pragma unroll
+    for (int j = 0; j < H; ++j) {
+      const float dj = a - thr[H + 1 + j];
+      dmin = fminf(dmin, fabsf(dj));
+      n += dj >= 0.f ? 1 : 0;
+    }
+    near = dmin < m;
+    return v >= 0.f ? (uint32_t)(H + 1 + n) : (uint32_t)(H - n);
+  } else {
+    float dmin = INFINITY;
+    int n = 0;
+#pragma unroll
+    for (int k = 0; k < 2 * H + 1; ++k) {
+      const float dk = v - thr[k];
+      dmin = fminf(dmin, fabsf(dk));
+      n += dk >= 0.f ? 1 : 0;
+    }
+    near = dmin < m;
+    return (uint32_t)n;
+  }
+}
+
+// One 32-column chunk of a row's accumulator: its BM code words (coordinate j
+// of the chunk at bits j·BM), the near-threshold flags, and (Prod) the sum of
+// squared residuals in v units.
+template <int BM, bool SYM, bool PROD>
+__device__ __forceinline__ uint32_t chunk_codes(const uint32_t (&a)[32], float f, const float (&thr)[15],
+                                                const float* cen_s, uint32_t (&cw)[BM], float& g2) {
+  uint32_t m32 = 0u;
+#pragma unroll
+  for (int w = 0; w < BM; ++w) cw[w] = 0u;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float v = __uint_as_float(a[j]) * f;
+    bool near;
+    const uint32_t code = bucketize_c<BM, SYM>(v, thr, kMargin, near);
+    m32 |= (near ? 1u : 0u) << j;
+    put_bits<BM>(cw, j * BM, code);
+    if constexpr (PROD) {
+      const float rr = v - cen_s[code];
+      g2 = fmaf(rr, rr, g2);
+    }
+  }
+  return m32;
+}
+
+// Code of coordinate `col` (a run-time index) in a chunk's BM packed words, and its replacement.
 template <int BM>
-__device__ __forceinline__ uint32_t code_at(const uint32_t (&wd)[4 * BM], int col) {
+__device__ __forceinline__ uint32_t code_at(const uint32_t (&wd)[BM], int col) {
   const int pos = col * BM;
   uint32_t v = 0;
 #pragma unroll
-  for (int w = 0; w < 4 * BM; ++w) {
+  for (int w = 0; w < BM; ++w) {
     const int sh = pos - 32 * w;
     if (sh >= 0 && sh < 32) v |= wd[w] >> sh;
     if (sh < 0 && sh > -BM) v |= wd[w] << (-sh);
@@ -128,11 +196,11 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t (&wd)[4 * BM], int co
   return v & ((1u << BM) - 1u);
 }
 template <int BM>
-__device__ __forceinline__ void set_code(uint32_t (&wd)[4 * BM], int col, uint32_t code) {
+__device__ __forceinline__ void set_code(uint32_t (&wd)[BM], int col, uint32_t code) {
   const int pos = col * BM;
   const uint32_t m = (1u << BM) - 1u;
 #pragma unroll
-  for (int w = 0; w < 4 * BM; ++w) {
+  for (int w = 0; w < BM; ++w) {
     const int sh = pos - 32 * w;
     if (sh >= 0 && sh < 32) wd[w] = (wd[w] & ~(m << sh)) | (code << sh);
     if (sh < 0 && sh > -BM) wd[w] = (wd[w] & ~(m >> (-sh))) | (code >> (-sh));
@@ -182,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
   uint64_t* acc2_empty = bars + 21;// epilogue warps
   uint64_t* tab_full = bars + 22;  // the B tables
   uint64_t* drain = bars + 23;     // every MMA issued has completed
+  uint64_t* g2_full = bars + 24;   // [2] Prod: both halves of the rows' γ² are in shared memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -199,14 +268,15 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
       mbar_init(&a_full[s], 4);
       mbar_init(&a_empty[s], 1);
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 4);
+      mbar_init(&acc_empty[s], 8);
       mbar_init(&nb_full[s], 4);
-      mbar_init(&nb_empty[s], 4);
+      mbar_init(&nb_empty[s], 8);
+      mbar_init(&g2_full[s], 8);
     }
-    mbar_init(a2_full, 4);
+    mbar_init(a2_full, 8);
     mbar_init(a2_empty, 1);
     mbar_init(acc2_full, 1);
-    mbar_init(acc2_empty, 4);
+    mbar_init(acc2_empty, 8);
     mbar_init(tab_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -401,10 +471,11 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
       }
     }
   } else {
-    // ---------------- epilogue
-    const int q = warp & 3, r = 32 * q + lane;
+    // ---------------- epilogue: warps 6-13; warp w serves TMEM lanes 32·(w % 4)..+31
+    // (rows of the tile) and the column half (w - 6) / 4: chunks 2·half, 2·half + 1
+    const int q = warp & 3, r = 32 * q + lane, half = (warp - 6) >> 2;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    constexpr int WW = 4 * BM;  // code words of a row
+    const bool even = (lane & 1) == 0;
     for (int i = 0; i < nloc; ++i) {
       const int64_t t = blockIdx.x + (int64_t)i * gridDim.x;
       const int64_t row = t * kRows + r;
@@ -415,118 +486,166 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
       __syncwarp();
       if (lane == 0) mbar_arrive(&nb_empty[ab]);
       const float sc = F16 ? 1.f : pow2_scale_16_32(s);
-      const float f = s > 0.f ? (float)(p.sqrt_d / ((double)s * sc * p.pi_scale)) : 0.f;
+      // fp32 on purpose: its rounding (~2e-7 relative) lies far inside the
+      // recomputation band, and fp64 arithmetic is slow on this part
+      const float f = s > 0.f ? p.sqrt_df / (s * sc * p.pi_scale) : 0.f;
       const bool live = valid && s > 0.f;
+      const int64_t dv = valid ? dest_row(p, row) : 0;
       if (!__all_sync(kFull, bar_wait(&acc_full[ab], par, abort_flag, p.status, lim))) break;
       tc_fence_after();
       const uint32_t acc = tmem + lane_base + L::ColAcc + ab * 128;
-      // a3/a4: bucketize (binary search), flag coordinates near a threshold, pack
-      uint32_t wd[WW];
-#pragma unroll
-      for (int w = 0; w < WW; ++w) wd[w] = 0u;
-      uint32_t fm[4];
+      uint32_t a0[32], a1[32];
+      tmem_ld32_nw(acc + 64 * half, a0);
+      tmem_wait_ld();
+      tmem_ld32_nw(acc + 64 * half + 32, a1);  // waited for after the first chunk's codes
+      // a3/a4 per 32-coordinate chunk: bucketize, flag, pack into BM words
+      // (chunk c of a row is words [c·BM, c·BM + BM) of its stream), recompute
+      // flagged coordinates, store
+      uint32_t cw[2][BM];
       float g2 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t a[32];
-        tmem_ld32_nw(acc + 32 * c, a);
-        tmem_wait_ld();
-        uint32_t m32 = 0u;
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
+        if (cc == 1) {
+          tmem_wait_ld();
+          // the accumulator is in registers now: hand it back to the MMA
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[ab]);
+        }
+        uint32_t m32 = p.sym ? chunk_codes<BM, true, PROD>(cc ? a1 : a0, f, p.thr, cen_s, cw[cc], g2)
+                             : chunk_codes<BM, false, PROD>(cc ? a1 : a0, f, p.thr, cen_s, cw[cc], g2);
+        if (!live) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float v = __uint_as_float(a[j]) * f;
-          bool near;
-          const uint32_t code = bucketize<BM>(v, thr_s, kMargin, near);
-          m32 |= (near ? 1u : 0u) << j;
-          put_bits<BM>(wd, (32 * c + j) * BM, code);
-          if constexpr (PROD) {
-            const float rr = v - cen_s[code];
-            g2 = fmaf(rr, rr, g2);
+          for (int w = 0; w < BM; ++w) cw[cc][w] = 0u;
+          m32 = 0u;
+          g2 = 0.f;
+        }
+        // flagged coordinates: one warp-wide float-float dot product each
+        for (;;) {
+          const uint32_t any = __ballot_sync(kFull, m32 != 0u);
+          if (!any) break;
+          const int src = __ffs(any) - 1;
+          int j = 0;
+          if (lane == src) {
+            j = __ffs(m32) - 1;
+            m32 &= m32 - 1u;
+          }
+          j = __shfl_sync(kFull, j, src);
+          const int col = 32 * c + j;
+          const float ssrc = __shfl_sync(kFull, s, src);
+          const int64_t srow = t * kRows + 32 * q + src;
+          float4 xv;
+          if constexpr (F16) {
+            const uint2 h = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.x) + srow * kDim) + lane);
+            const float2 x0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+            const float2 x1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+            xv = make_float4(x0.x, x0.y, x1.x, x1.y);
+          } else {
+            xv = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + srow * kDim) + lane);
+          }
+          const float4 pv = __ldg(reinterpret_cast<const float4*>(p.pi + (int64_t)col * kDim) + lane);
+          float sh = 0.f, sl = 0.f;
+          ff_fma(xv.x, pv.x, sh, sl);
+          ff_fma(xv.y, pv.y, sh, sl);
+          ff_fma(xv.z, pv.z, sh, sl);
+          ff_fma(xv.w, pv.w, sh, sl);
+#pragma unroll
+          for (int o = 16; o; o >>= 1) {
+            const float oh = __shfl_xor_sync(kFull, sh, o), ol = __shfl_xor_sync(kFull, sl, o);
+            const float s2 = sh + oh, bb = s2 - sh;
+            sl = sl + ol + ((sh - (s2 - bb)) + (oh - bb));
+            sh = s2;
+          }
+          if (lane == src) {
+            const float vv = (float)(((double)sh + (double)sl) * (p.sqrt_d / (double)ssrc));
+            bool nr;
+            const uint32_t code = bucketize<BM>(vv, thr_s, 0.f, nr);
+            if constexpr (PROD) {
+              const uint32_t old = code_at<BM>(cw[cc], j);
+              const float e0 = vv - cen_s[old], e1 = vv - cen_s[code];
+              g2 += e1 * e1 - e0 * e0;
+            }
+            set_code<BM>(cw[cc], j, code);
           }
         }
-        fm[c] = m32;
-      }
-      if constexpr (!PROD) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[ab]);
-      }
-      if (!live) {
+        // stores of this chunk's codes
+        if (p.layout == TQ_LAYOUT_TOKEN) {
+          if (valid) {
+            uint32_t* dst = p.codes + dv * p.W + c * BM;
 #pragma unroll
-        for (int w = 0; w < WW; ++w) wd[w] = 0u;
-        fm[0] = fm[1] = fm[2] = fm[3] = 0u;
-        g2 = 0.f;
-      }
-      // flagged coordinates: one warp-wide float-float dot product each
-      for (;;) {
-        const uint32_t any = __ballot_sync(kFull, (fm[0] | fm[1] | fm[2] | fm[3]) != 0u);
-        if (!any) break;
-        const int src = __ffs(any) - 1;
-        int col = 0;
-        if (lane == src) {
-#pragma unroll
-          for (int g = 3; g >= 0; --g)
-            if (fm[g]) col = 32 * g + __ffs(fm[g]) - 1;
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-            if (g == (col >> 5)) fm[g] &= fm[g] - 1u;
-        }
-        col = __shfl_sync(kFull, col, src);
-        const float ssrc = __shfl_sync(kFull, s, src);
-        const int64_t srow = t * kRows + 32 * q + src;
-        float4 xv;
-        if constexpr (F16) {
-          const uint2 h = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.x) + srow * kDim) + lane);
-          const float2 x0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
-          const float2 x1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
-          xv = make_float4(x0.x, x0.y, x1.x, x1.y);
+            for (int w = 0; w < BM; ++w) dst[w] = cw[cc][w];
+          }
         } else {
-          xv = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + srow * kDim) + lane);
-        }
-        const float4 pv = __ldg(reinterpret_cast<const float4*>(p.pi + (int64_t)col * kDim) + lane);
-        float sh = 0.f, sl = 0.f;
-        ff_fma(xv.x, pv.x, sh, sl);
-        ff_fma(xv.y, pv.y, sh, sl);
-        ff_fma(xv.z, pv.z, sh, sl);
-        ff_fma(xv.w, pv.w, sh, sl);
+          // PAIR: vectors 2k and 2k+1 share a block; coordinate j's two codes
+          // sit side by side at block bits 2j·BM (even vector low).  Rows r and
+          // r+1 of the tile are lanes l and l+1; when the destination pairs them,
+          // the even lane writes the block words of coordinates 32c..32c+15 and
+          // the odd lane those of 32c+16..32c+31, after one exchange.
+          uint32_t part[BM];
 #pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          const float oh = __shfl_xor_sync(kFull, sh, o), ol = __shfl_xor_sync(kFull, sl, o);
-          const float s2 = sh + oh, bb = s2 - sh;
-          sl = sl + ol + ((sh - (s2 - bb)) + (oh - bb));
-          sh = s2;
-        }
-        if (lane == src) {
-          const float vv = (float)(((double)sh + (double)sl) * (p.sqrt_d / (double)ssrc));
-          bool nr;
-          const uint32_t code = bucketize<BM>(vv, thr_s, 0.f, nr);
-          if constexpr (PROD) {
-            const uint32_t old = code_at<BM>(wd, col);
-            const float a0 = vv - cen_s[old], a1 = vv - cen_s[code];
-            g2 += a1 * a1 - a0 * a0;
+          for (int w = 0; w < BM; ++w) part[w] = __shfl_xor_sync(kFull, cw[cc][w], 1);
+          const int64_t base_row = row - (even ? 0 : 1);
+          const bool whole = p.pair_aligned && base_row + 1 < p.N;
+          uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)p.W) + 2 * c * BM;
+          if (valid && whole) {
+            uint32_t ow[BM];
+#pragma unroll
+            for (int w = 0; w < BM; ++w) ow[w] = 0u;
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const uint32_t own = even ? get_bits<BM>(cw[cc], jj * BM) : get_bits<BM>(cw[cc], (16 + jj) * BM);
+              const uint32_t prt = even ? get_bits<BM>(part, jj * BM) : get_bits<BM>(part, (16 + jj) * BM);
+              put_bits<BM>(ow, 2 * jj * BM, even ? own : prt);
+              put_bits<BM>(ow, (2 * jj + 1) * BM, even ? prt : own);
+            }
+#pragma unroll
+            for (int w = 0; w < BM; ++w) blk[(even ? 0 : BM) + w] = ow[w];
+          } else if (valid) {
+            // the partner is written by another call (or not at all): update this
+            // vector's slot of the chunk's 2·BM block words with masked atomics
+            const int slot = (int)(dv & 1);
+#pragma unroll 1
+            for (int w = 0; w < 2 * BM; ++w) {
+              uint32_t m = 0u, bits = 0u;
+#pragma unroll 1
+              for (int bt = 0; bt < 32; ++bt) {
+                const int pos = 32 * w + bt;  // bit of the chunk's block stream
+                const int j = pos / (2 * BM), k = pos % (2 * BM);
+                if (k / BM == slot) {
+                  m |= 1u << bt;
+                  bits |= ((code_at<BM>(cw[cc], j) >> (k % BM)) & 1u) << bt;
+                }
+              }
+              atomicAnd(blk + w, ~m);
+              atomicOr(blk + w, bits);
+            }
           }
-          set_code<BM>(wd, col, code);
         }
       }
-      // a5 (Prod): residual operand, second product, sign bits
-      uint32_t sg[4] = {0u, 0u, 0u, 0u};
-      float gam = 0.f;
+      if (valid && half == 0) p.norm[dv] = s;
+      // a5 (Prod): γ over both halves, residual operand, second product, signs
       if constexpr (PROD) {
-        gam = live ? sqrtf(fmaxf(g2, 0.f)) / (float)p.sqrt_d : 0.f;
+        float* g2_s = norm_s + L::AccBufs * kRows;  // [2 tile parities][2 halves][128]
+        g2_s[((i & 1) * 2 + half) * kRows + r] = g2;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&g2_full[i & 1]);
+        if (!__all_sync(kFull, bar_wait(&g2_full[i & 1], ((uint32_t)i >> 1) & 1u, abort_flag, p.status, lim))) break;
+        const float g2t = g2_s[((i & 1) * 2) * kRows + r] + g2_s[((i & 1) * 2 + 1) * kRows + r];
+        const float gam = live ? sqrtf(fmaxf(g2t, 0.f)) / (float)p.sqrt_d : 0.f;
         const float rsd = live ? pow2_scale_16_32(gam) / (float)p.sqrt_d : 0.f;
         if (!__all_sync(kFull, bar_wait(a2_empty, ((uint32_t)i & 1u) ^ 1u, abort_flag, p.status, lim))) break;
         tc_fence_after();
         const uint32_t a2 = tmem + lane_base + L::ColA2;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t a[32];
-          tmem_ld32_nw(acc + 32 * c, a);
-          tmem_wait_ld();
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * half + cc;
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float r0 = (__uint_as_float(a[2 * j]) * f - cen_s[get_bits<BM>(wd, (32 * c + 2 * j) * BM)]) * rsd;
-            const float r1 = (__uint_as_float(a[2 * j + 1]) * f - cen_s[get_bits<BM>(wd, (32 * c + 2 * j + 1) * BM)]) * rsd;
+            const uint32_t* av = cc ? a1 : a0;
+            const float r0 = (__uint_as_float(av[2 * j]) * f - cen_s[get_bits<BM>(cw[cc], 2 * j * BM)]) * rsd;
+            const float r1 = (__uint_as_float(av[2 * j + 1]) * f - cen_s[get_bits<BM>(cw[cc], (2 * j + 1) * BM)]) * rsd;
             split2(r0, r1, hi[j], lo[j]);
           }
           tmem_st16(a2 + 16 * c, hi);
@@ -535,88 +654,26 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(a2_full);
-          mbar_arrive(&acc_empty[ab]);
-        }
+        if (lane == 0) mbar_arrive(a2_full);
         if (!__all_sync(kFull, bar_wait(acc2_full, (uint32_t)i & 1u, abort_flag, p.status, lim))) break;
         tc_fence_after();
+        uint32_t sg[2];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t a[32];
-          tmem_ld32_nw(tmem + lane_base + L::ColAcc2 + 32 * c, a);
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t pa[32];
+          tmem_ld32_nw(tmem + lane_base + L::ColAcc2 + 32 * (2 * half + cc), pa);
           tmem_wait_ld();
           uint32_t bits = 0u;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) bits |= (__uint_as_float(a[j]) >= 0.f ? 1u : 0u) << j;
-          sg[c] = live ? bits : 0u;
+          for (int j = 0; j < 32; ++j) bits |= (__uint_as_float(pa[j]) >= 0.f ? 1u : 0u) << j;
+          sg[cc] = live ? bits : 0u;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc2_empty);
-      }
-      // ---------------- stores
-      const int64_t dv = valid ? dest_row(p, row) : 0;
-      if (valid) {
-        p.norm[dv] = s;
-        if constexpr (PROD) {
-          p.rnorm[dv] = gam;
-          *reinterpret_cast<uint4*>(p.qjl + dv * p.QW) = make_uint4(sg[0], sg[1], sg[2], sg[3]);
-        }
-      }
-      if (p.layout == TQ_LAYOUT_TOKEN) {
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.codes + dv * p.W);
-#pragma unroll
-          for (int w = 0; w < BM; ++w) dst[w] = make_uint4(wd[4 * w], wd[4 * w + 1], wd[4 * w + 2], wd[4 * w + 3]);
-        }
-      } else {
-        // PAIR: vectors 2k and 2k+1 share a block of 2·WW words, coordinate j's
-        // two codes side by side at bits 2j·BM (even vector low).  Rows r and
-        // r+1 of the tile are lanes l and l+1: when the destination pairs them
-        // the even lane writes the block's first WW words (coordinates 0-63),
-        // the odd lane the last WW (64-127), each with its partner's codes of
-        // that half, obtained by one exchange.
-        const bool even = (lane & 1) == 0;
-        uint32_t part[2 * BM];
-#pragma unroll
-        for (int w = 0; w < 2 * BM; ++w) part[w] = __shfl_xor_sync(kFull, even ? wd[2 * BM + w] : wd[w], 1);
-        const int64_t base_row = row - (even ? 0 : 1);
-        const bool whole = p.pair_aligned && base_row + 1 < p.N;  // both rows of the pair are here
-        if (valid && whole) {
-          uint32_t out[WW];
-#pragma unroll
-          for (int w = 0; w < WW; ++w) out[w] = 0u;
-#pragma unroll
-          for (int jj = 0; jj < 64; ++jj) {
-            const uint32_t own = even ? get_bits<BM>(wd, jj * BM) : get_bits<BM>(wd, (64 + jj) * BM);
-            const uint32_t prt = get_bits<BM>(part, jj * BM);
-            put_bits<BM>(out, 2 * jj * BM, even ? own : prt);
-            put_bits<BM>(out, (2 * jj + 1) * BM, even ? prt : own);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(p.codes + (dv >> 1) * (2 * (int64_t)WW) + (even ? 0 : WW));
-#pragma unroll
-          for (int w = 0; w < BM; ++w) dst[w] = make_uint4(out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
-        } else if (valid) {
-          // the partner is written by another call (or not at all): update this
-          // vector's slot of the block with masked atomics
-          const int slot = (int)(dv & 1);
-          uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)WW);
-#pragma unroll 1
-          for (int w = 0; w < 2 * WW; ++w) {
-            uint32_t m = 0u, bits = 0u;
-#pragma unroll 1
-            for (int b = 0; b < 32; ++b) {
-              const int pos = 32 * w + b;  // block stream bit
-              const int j = pos / (2 * BM), k = pos % (2 * BM);
-              if (k / BM == slot) {
-                m |= 1u << b;
-                bits |= ((code_at<BM>(wd, j) >> (k % BM)) & 1u) << b;
-              }
-            }
-            atomicAnd(blk + w, ~m);
-            atomicOr(blk + w, bits);
-          }
+          *reinterpret_cast<uint2*>(p.qjl + dv * p.QW + 2 * half) = make_uint2(sg[0], sg[1]);
+          if (half == 0) p.rnorm[dv] = gam;
         }
       }
     }
@@ -684,8 +741,15 @@ tq_status launch_encode128(const DevCtx& c, const void* x, int x_dtype, int64_t 
   p.pi = c.pi;
   p.pi_scale = c.pi_scale;
   p.sqrt_d = std::sqrt((double)c.d);
+  p.sqrt_df = (float)p.sqrt_d;
   for (int k = 0; k < 15; ++k) p.thr[k] = c.thr[k];
   for (int k = 0; k < 16; ++k) p.cen[k] = c.cen[k];
+  {
+    const int nt = (1 << c.b_mse) - 1, h = nt / 2;
+    bool sym = c.thr[h] == 0.f;
+    for (int j = 0; sym && j < h; ++j) sym = c.thr[h - 1 - j] == -c.thr[h + 1 + j];
+    p.sym = sym ? 1 : 0;
+  }
   p.layout = out->layout;
   p.W = c.words_per_vec;
   p.QW = c.qjl_words_per_vec;
