@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--bits", type=int, default=4, choices=[1, 2, 3, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="decode: skip the other configurations' measurements in the same run")
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "encode", "scores", "longctx", "keys", "prefill"],
                     help="decode (the headline) or a secondary workload (see bench_workloads.py)")
@@ -335,7 +337,64 @@ def run_tq(args, world, rank, local):
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(tq, ctx, reps[0], bits, cap, q)
+    if rank == 0 and not args.no_extras:
+        del reps
+        torch.cuda.empty_cache()
+        line["configs"] = other_configs(args, world, rank, local)
     return line if rank == 0 else None
+
+
+def _summary(sub_line, keep=()):
+    """The figures of a secondary workload's line that the headline line carries."""
+    r = sub_line.get("roofline") or {}
+    out = {"workload": sub_line["config"]["workload"], "metric": sub_line["metric"], "value": sub_line["value"],
+           "unit": sub_line["unit"], "ms_per_step": sub_line["ms_per_step"], "steps": sub_line["steps"],
+           "roofline": {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac", "kernel", "peak_kind")
+                        if k in r},
+           "clocks": sub_line.get("clocks")}
+    for k in keep:
+        if k in sub_line["config"]:
+            out[k] = sub_line["config"][k]
+    return out
+
+
+def other_configs(args, world, rank, local):
+    """Every other configuration of the metric, measured in this run with its own
+    warm-up and timed steps (the same runners as --workload ...): decode at
+    b = 2, the d = 128 encoder (long-context prefill and the Prod keys), Prod
+    scores over 1M keys, the 4096-key encode + score, the 80-layer long-context
+    decode, and bulk encode at N = 100K (d = 1536 / 3072, dense and Hadamard)."""
+    import types
+
+    import torch
+
+    import bench_workloads as bw
+
+    def ns(**kw):
+        base = dict(steps=20, warmup=3, no_cpu_baseline=True, no_extras=True, bits=4, dim=3072, rows=100_000,
+                    rotation="dense", layers=80, gpus=args.gpus)
+        base.update(kw)
+        return types.SimpleNamespace(**base)
+
+    out = {}
+    b2 = run_tq(ns(steps=max(20, min(args.steps, 400)), bits=2), world, rank, local)
+    out["decode_b2"] = _summary(b2, ("bits", "replicas")) | {"us_per_call": b2["roofline"]["us_per_call"]}
+    torch.cuda.empty_cache()
+    pf = bw.run_prefill(ns(steps=10), world, rank, local, ROOT, Clocks, {})
+    out["encode_d128"] = _summary(pf, ("vectors", "prod_encode"))
+    out["scores_prod_1m"] = _summary(bw.run_scores(ns(steps=20), world, rank, local, ROOT, Clocks, {}))
+    out["keys_4096"] = _summary(bw.run_keys(ns(steps=50), world, rank, local, ROOT, Clocks, {}),
+                                ("us_per_encode_plus_score",))
+    torch.cuda.empty_cache()
+    lc = bw.run_longctx(ns(steps=5), world, rank, local, ROOT, Clocks, {})
+    out["longctx_80_layers"] = _summary(lc, ("prefill_encode_mvec_s", "ms_per_layer", "layers"))
+    torch.cuda.empty_cache()
+    for d in (1536, 3072):
+        for rot in ("dense", "hadamard"):
+            ln = bw.run_encode(ns(steps=5, dim=d, rows=100_000, rotation=rot), world, rank, local, ROOT, Clocks, {})
+            out[f"bulk_encode_d{d}_{rot}_100k"] = _summary(ln)
+            torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------- oracle timing
@@ -369,6 +428,29 @@ def cache_for_oracle(tq, reps0, cap):
     return idx_k, idx_v, kn, vn
 
 
+def oracle_band_check(tq, reps0, bits, cap):
+    """The oracle's encoder on a sample of the cache's source rows (first KV
+    head, 4096 tokens): the share of coordinates inside the 1e-6 band around a
+    threshold, and how many GPU codes differ from the oracle's outside it."""
+    import numpy as np
+
+    from kv_cache_vector_tq_gb300 import synth
+    from oracle import codebook as ocb
+    from oracle import quantizer as oq
+    from oracle import rotation as orot
+    Pi = orot.haar_rotation(synth.gaussian_matrix(0, D))
+    cb = ocb.build_codebook(D, bits)
+    Kh, _ = synth.kv_layer(0, 0, B, HKV, SEQ, D)
+    n = 4096
+    X = Kh[0, 0, :n].astype(np.float64)
+    ref, _, v = oq.mse_quantize(X, Pi, cb["centroids"], math.sqrt(D))
+    band = oq.near_threshold(v, cb["centroids"])
+    got = tq.tq_unpack_indices(reps0[0], 0, n).astype(np.int64)
+    return {"band_frac": float(band.mean()), "coordinates": int(band.size),
+            "index_mismatch_outside_band": int(((got != ref) & ~band).sum()),
+            "sample": f"K rows 0-{n - 1} of KV head 0 (fp16 N(0,1), outlier channels), b={bits}"}
+
+
 def cpu_baseline(tq, ctx, reps0, bits, cap, q):
     import numpy as np
     idx_k, idx_v, kn, vn = cache_for_oracle(tq, reps0, cap)
@@ -381,7 +463,8 @@ def cpu_baseline(tq, ctx, reps0, bits, cap, q):
         runs += 1
     return {"value": round(done_bytes / total / 1e9, 6), "unit": "GB/s",
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"{runs} full decode steps (8 KV heads x 16384 tokens, fp64 explicit dequantization)"}
+            "sample": f"{runs} full decode steps (8 KV heads x 16384 tokens, fp64 explicit dequantization)",
+            "parity": oracle_band_check(tq, reps0, bits, cap)}
 
 
 # ---------------------------------------------------------------- oracle timing, secondary workloads

@@ -327,11 +327,9 @@ tq_status tq_unpack_indices(const tq_codes* codes, int64_t first, int64_t count,
 tq_status tq_ctx_set_wait_limit(tq_ctx* ctx, uint32_t polls);
 
 /* Reads and clears the context's device status word (synchronises `stream`).
- * Returns TQ_OK; TQ_ERR_UNSUPPORTED if a decode kernel launched with this
- * context (as kctx) found dynamic shared memory at another shared-window
- * offset than the one its 4-bit table lookups are compiled for, and returned
- * without writing its output; else TQ_ERR_TIMEOUT if a bounded device wait of
- * a kernel launched with this context ran out since the last poll. */
+ * Returns TQ_OK, or TQ_ERR_TIMEOUT if a bounded device wait of a kernel
+ * launched with this context ran out since the last poll (that kernel's
+ * outputs are then unspecified). */
 tq_status tq_status_poll(const tq_ctx* ctx, tq_stream stream);
 
 #ifdef __cplusplus

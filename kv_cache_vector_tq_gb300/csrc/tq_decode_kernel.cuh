@@ -59,10 +59,6 @@ __host__ __device__ constexpr int stage_bytes(bool q) { return q ? kStageBytesQ 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.f;  // rescale only when the running max grows by > 2^8
 constexpr int kPart = 132;    // floats per head in a published partial: m, l, 2 pad, acc[128]
-// Shared-window offset of dynamic shared memory in a kernel without static
-// shared memory (the runtime reserves the window's first KB).  The 4-bit
-// decode addresses its tables from it at compile time and checks it at run time.
-constexpr uint32_t kSmemWindow = 0x400;
 
 // Workspace: one arrival counter per (batch, KV head), then the partial state
 // (m, l, Πᵀ·acc[128]) of every CTA when a (batch, KV head) is split over more
@@ -253,10 +249,6 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
   static_assert(!Q || (G <= 4 && BK <= 3), "Prod keys: up to 4 query heads per KV head, (b-1)-bit codes");
   constexpr int SB = stage_bytes(Q);
   extern __shared__ __align__(128) unsigned char smem[];
-  if (kByte && smem_u32(smem) != kSmemWindow) {  // the table addresses below assume it
-    if (threadIdx.x == 0) atomicOr(p.status, 2);
-    return;
-  }
   const StepSmem L = step_smem(BK, BV, G, W, p.same_lut != 0, Q);
   uint32_t* klut = reinterpret_cast<uint32_t*>(smem);
   uint32_t* qlut = reinterpret_cast<uint32_t*>(smem + L.qlut);  // Prod keys
@@ -600,6 +592,7 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
   const uint32_t* mykl = klut + lane;
   const uint32_t* myvl = vlut + lane;
   const uint32_t lane4 = lane * 4;
+  const uint32_t tbase = smem_u32(smem);  // shared-window address of the byte-row tables
   float m_run[NT], l_run[NT];
   float o[8][NT][4];
 #pragma unroll
@@ -671,10 +664,10 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     for (int s = 0; s < 8; ++s) {
       uint32_t a0, a1, a2, a3;
       if constexpr (kByte) {  // a0/a2: bytes 2(s&1), 2(s&1)+1 of word s/2 (a1/a3 likewise from k1)
-        a0 = lds_at<kSmemWindow>(byte_row_addr(k0[s >> 1], lane4, 2 * (s & 1)));
-        a1 = lds_at<kSmemWindow>(byte_row_addr(k1[s >> 1], lane4, 2 * (s & 1)));
-        a2 = lds_at<kSmemWindow>(byte_row_addr(k0[s >> 1], lane4, 2 * (s & 1) + 1));
-        a3 = lds_at<kSmemWindow>(byte_row_addr(k1[s >> 1], lane4, 2 * (s & 1) + 1));
+        a0 = lds_at<0>(tbase + byte_row_addr(k0[s >> 1], lane4, 2 * (s & 1)));
+        a1 = lds_at<0>(tbase + byte_row_addr(k1[s >> 1], lane4, 2 * (s & 1)));
+        a2 = lds_at<0>(tbase + byte_row_addr(k0[s >> 1], lane4, 2 * (s & 1) + 1));
+        a3 = lds_at<0>(tbase + byte_row_addr(k1[s >> 1], lane4, 2 * (s & 1) + 1));
       } else {
         a0 = mykl[get_bits<2 * BK>(k0, 4 * s * BK) << 5];
         a1 = mykl[get_bits<2 * BK>(k1, 4 * s * BK) << 5];
@@ -784,10 +777,10 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
       // rows g / g+8 <-> coordinates 16g + 2mt / 16g + 2mt + 1
       uint32_t a0, a1, a2, a3;
       if constexpr (kByte) {  // bytes 2(mt&1), 2(mt&1)+1 of word mt/2
-        a0 = lds_at<kSmemWindow + 128>(byte_row_addr(v0w[mt >> 1], lane4, 2 * (mt & 1)));
-        a1 = lds_at<kSmemWindow + 128>(byte_row_addr(v0w[mt >> 1], lane4, 2 * (mt & 1) + 1));
-        a2 = lds_at<kSmemWindow + 128>(byte_row_addr(v1w[mt >> 1], lane4, 2 * (mt & 1)));
-        a3 = lds_at<kSmemWindow + 128>(byte_row_addr(v1w[mt >> 1], lane4, 2 * (mt & 1) + 1));
+        a0 = lds_at<128>(tbase + byte_row_addr(v0w[mt >> 1], lane4, 2 * (mt & 1)));
+        a1 = lds_at<128>(tbase + byte_row_addr(v0w[mt >> 1], lane4, 2 * (mt & 1) + 1));
+        a2 = lds_at<128>(tbase + byte_row_addr(v1w[mt >> 1], lane4, 2 * (mt & 1)));
+        a3 = lds_at<128>(tbase + byte_row_addr(v1w[mt >> 1], lane4, 2 * (mt & 1) + 1));
       } else {
         a0 = myvl[get_bits<2 * BV>(v0w, (2 * mt) * 2 * BV) << 5];
         a1 = myvl[get_bits<2 * BV>(v0w, (2 * mt + 1) * 2 * BV) << 5];

@@ -901,7 +901,6 @@ tq_status tq_status_poll(const tq_ctx* ctx, tq_stream stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e == cudaSuccess && h != 0) e = cudaMemsetAsync(v.status, 0, sizeof(int), (cudaStream_t)stream);
   if (e != cudaSuccess) return set_cuda_error(e);
-  if (h & 2) return TQ_ERR_UNSUPPORTED;  // a decode kernel found another shared-memory layout
   return h == 0 ? TQ_OK : TQ_ERR_TIMEOUT;
 }
 
