@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     cp_async_commit();
   };
   // issued in the warp's last tile when it has one (Prod keys: after the loop)
-  const bool pv_in_loop = !Q && warp < ntl;
+  const bool pv_in_loop = warp < ntl;
   for (int j = 0; warp + j * W < ntl; ++j) {
     const int tile = t_begin + warp + j * W;
     cp_async_wait<kStages - 1>();
@@ -623,6 +623,18 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     read_words<BV>(v1w, st + 3 * kFieldBytes + lane * 16);
     const float* ns = reinterpret_cast<const float*>(st + 4 * kFieldBytes);
     float4 nrm = make_float4(ns[g], ns[g + 8], ns[16 + g], ns[16 + g + 8]);
+    // Prod keys: this tile's sign words (bits j = 32t + 4s + {0..3} of tokens g,
+    // g+8) and γ, read before the stage is refilled below
+    uint32_t qw0 = 0u, qw1 = 0u;
+    float gam0 = 0.f, gam1 = 0.f;
+    if constexpr (Q) {
+      const uint32_t* sw = reinterpret_cast<const uint32_t*>(st + kQSigns);
+      qw0 = sw[g * 4 + t];
+      qw1 = sw[(g + 8) * 4 + t];
+      const float* gm = reinterpret_cast<const float*>(st + kQGamma);
+      gam0 = gm[g];
+      gam1 = gm[g + 8];
+    }
     if (owner && tile == new_tile) {  // the appended token: use the codes just made
       if (new_row == g) {
 #pragma unroll
@@ -650,9 +662,7 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     }
     // every lane's words are in registers: refill this stage
     issue(j + kStages);
-    if constexpr (!Q) {  // (Prod keys still read this stage's γ and signs below)
-      if (warp + (j + 1) * W >= ntl) issue_pv();  // the warp's last tile: its region is free now
-    }
+    if (warp + (j + 1) * W >= ntl) issue_pv();  // the warp's last tile: its region is free now
     const int lt0 = tile * kTileTok;
     // K side: S = K̂·Q with two independent MMA chains
     float sa[NT][4], sb[NT][4];
@@ -684,13 +694,8 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     }
     // Prod keys: Σ_j (S·q)_j·(2·bit_j − 1) for tokens g, g+8, sign bits j = 32t + 4s + {0..3}
     float qa[NT][4], qb[NT][4];
-    float gam0 = 0.f, gam1 = 0.f;
     if constexpr (Q) {
-      const uint32_t* sw = reinterpret_cast<const uint32_t*>(st + kQSigns);
-      const uint32_t w0 = sw[g * 4 + t], w1 = sw[(g + 8) * 4 + t];
-      const float* gm = reinterpret_cast<const float*>(st + kQGamma);
-      gam0 = gm[g];
-      gam1 = gm[g + 8];
+      const uint32_t w0 = qw0, w1 = qw1;
       const uint32_t* myql = qlut + lane;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
