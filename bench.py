@@ -363,7 +363,8 @@ def other_configs(args, world, rank, local):
     warm-up and timed steps (the same runners as --workload ...): decode at
     b = 2, the d = 128 encoder (long-context prefill and the Prod keys), Prod
     scores over 1M keys, the 4096-key encode + score, the 80-layer long-context
-    decode, and bulk encode at N = 100K (d = 1536 / 3072, dense and Hadamard)."""
+    decode, and bulk encode of fp32 rows (d = 128 at N = 1M, d = 1536 / 3072 at
+    N = 100K; dense and Hadamard rotations)."""
     import types
 
     import torch
@@ -389,6 +390,10 @@ def other_configs(args, world, rank, local):
     lc = bw.run_longctx(ns(steps=5), world, rank, local, ROOT, Clocks, {})
     out["longctx_80_layers"] = _summary(lc, ("prefill_encode_mvec_s", "ms_per_layer", "layers"))
     torch.cuda.empty_cache()
+    for rot in ("dense", "hadamard"):
+        ln = bw.run_encode(ns(steps=5, dim=128, rows=1_000_000, rotation=rot), world, rank, local, ROOT, Clocks, {})
+        out[f"bulk_encode_d128_{rot}_1m"] = _summary(ln)
+        torch.cuda.empty_cache()
     for d in (1536, 3072):
         for rot in ("dense", "hadamard"):
             ln = bw.run_encode(ns(steps=5, dim=d, rows=100_000, rotation=rot), world, rank, local, ROOT, Clocks, {})

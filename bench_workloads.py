@@ -161,11 +161,14 @@ def run_encode(args, world, rank, local, root, clocks_cls, cpu):
     mvec = world * args.steps * N / sec / 1e6
     hbm, bf16, kind = _peaks(root, sustained=total_ms > 1000.0)  # a timed region of seconds runs at the power cap
     bytes_per_vec = 4 * d + d * bits // 8 + 4
-    if rot == "hadamard":
+    if rot == "hadamard" or d == 128:
+        # the Hadamard kernel, and the d = 128 tensor-memory kernel on fp32 rows
+        # (three 32.8 KFLOP products per 580 B: the bytes bind first), are HBM-bound
+        kern = "encode_wht_kernel" if rot == "hadamard" else "encode128_kernel"
+        key = f"encode_wht_d{d}_n{N // 1000}k" if rot == "hadamard" else f"encode128_f32_n{N // 1000}k"
         ach = args.steps * N * bytes_per_vec / sec / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
-                "traffic": traffic(root, f"encode_wht_d{d}_n{N // 1000}k"), "kernel": "encode_wht_kernel",
-                "peak_kind": kind,
+                "traffic": traffic(root, key), "kernel": kern, "peak_kind": kind,
                 "bytes_per_vector": bytes_per_vec}
     else:
         ach = args.steps * 2.0 * N * d * d / sec / 1e12  # useful flops of Y = X·Πᵀ
