@@ -30,6 +30,16 @@ Readings where the pages are silent or ambiguous:
   stream bit p is bit p mod 32 of little-endian uint32 word p // 32; each
   vector is padded with zero bits to a whole number of 16-byte units.
   The QJL bit of row j of S is stream bit j of its own padded stream.
+* b + 1/2 bits per coordinate ("TurboQuant 详解", section "论文给出的关键数据点":
+  3.5 and 2.5 bit/channel; section "decode 阶段到底怎么“用”这些压缩后的 KV":
+  672 B per token per layer = 16 vectors x (40 B of codes + a 2 B norm), i.e.
+  one rotation and one norm per vector and 320 code bits at d = 128): half of
+  the rotated coordinates take b + 1 bits, the other half b, each with the
+  Lloyd-Max codebook of its own width for the same coordinate density.  Which
+  half is immaterial to the quantizer (the coordinates of Π·u are exchangeable
+  under a Haar Π); the reading fixes coordinates j with j mod 16 < 8 at b + 1
+  bits.  Packing stays canonical with a width per coordinate: the code of
+  coordinate j occupies stream bits [P_j, P_j + w_j), P_j = Σ_{i<j} w_i.
 * Near-threshold band: a coordinate is excluded from bit-exact comparison iff
   |v - t_k| <= 1e-6 · max(1, |t_k|) for some threshold t_k (unit-variance
   units).  A QJL bit is excluded iff |(S·r)_j| <= 1e-6 · ‖S_j‖₂ · γ, i.e.
@@ -197,3 +207,90 @@ def prod_dequantize(idx, s, bits, gamma, Pi, S, centroids_mse, scale):
     c = np.asarray(centroids_mse, dtype=np.float64)
     base = (c[np.asarray(idx)] / scale) @ np.asarray(Pi, dtype=np.float64)
     return np.asarray(s, dtype=np.float64)[:, None] * (base + qjl_correction(bits, gamma, S))
+
+
+# ------------------------------------------------------------ b + 1/2 bits
+def mixed_widths(d, b):
+    """Bits of rotated coordinate j at b + 1/2 bits per coordinate: b + 1 where
+    j mod 16 < 8, b elsewhere."""
+    j = np.arange(d)
+    return np.where(j % 16 < 8, b + 1, b).astype(np.int64)
+
+
+def mixed_words_per_vector(d, b):
+    """uint32 words per packed vector: the Σ w_j bits, rounded up to whole words."""
+    return (int(mixed_widths(d, b).sum()) + 31) // 32
+
+
+def pack_varwidth(idx, widths):
+    """Canonical LSB-first packing of [N, n] indices with a width per position:
+    position j occupies stream bits [P_j, P_j + w_j), P_j = Σ_{i<j} w_i."""
+    idx = np.asarray(idx, dtype=np.int64)
+    widths = [int(w) for w in widths]
+    n = idx.shape[0]
+    W = (sum(widths) + 31) // 32
+    words = np.zeros((n, W), dtype=np.uint64)
+    p = 0
+    for j, w in enumerate(widths):
+        for k in range(w):
+            bit = (idx[:, j] >> k) & 1
+            words[:, p // 32] |= bit.astype(np.uint64) << np.uint64(p % 32)
+            p += 1
+    return words.astype(np.uint32)
+
+
+def unpack_varwidth(words, widths):
+    """Inverse of ``pack_varwidth``."""
+    words = np.asarray(words, dtype=np.uint64)
+    widths = [int(w) for w in widths]
+    idx = np.zeros((words.shape[0], len(widths)), dtype=np.int64)
+    p = 0
+    for j, w in enumerate(widths):
+        for k in range(w):
+            bit = (words[:, p // 32] >> np.uint64(p % 32)) & np.uint64(1)
+            idx[:, j] |= bit.astype(np.int64) << k
+            p += 1
+    return idx
+
+
+def pack_mixed_pairs(idx, b):
+    """Pair blocks of a b + 1/2-bit V cache: vectors 2i and 2i+1 share one stream
+    in which coordinate j holds the even vector's code then the odd vector's,
+    w_j bits each ([N, d] indices, N even -> [N/2, 2W] words)."""
+    idx = np.asarray(idx, dtype=np.int64)
+    d = idx.shape[1]
+    inter = np.zeros((idx.shape[0] // 2, 2 * d), dtype=np.int64)
+    inter[:, 0::2] = idx[0::2]
+    inter[:, 1::2] = idx[1::2]
+    return pack_varwidth(inter, np.repeat(mixed_widths(d, b), 2))
+
+
+def mixed_quantize(X, Pi, centroids_lo, centroids_hi, b, scale):
+    """TurboQuant_MSE at b + 1/2 bits: as ``mse_quantize``, but coordinate j is
+    quantized with the (b+1)-bit codebook where w_j = b + 1 and with the b-bit
+    codebook elsewhere.  Returns (idx [N, d], s [N], v [N, d])."""
+    U, s = _unit_rows(X)
+    Pi = np.asarray(Pi, dtype=np.float64)
+    v = scale * (U @ Pi.T)
+    hi = mixed_widths(v.shape[1], b) == b + 1
+    idx = np.where(hi[None, :], nearest_centroid(v, centroids_hi), nearest_centroid(v, centroids_lo))
+    idx[s == 0.0] = 0
+    return idx, s, v
+
+
+def mixed_dequantize(idx, s, Pi, centroids_lo, centroids_hi, b, scale):
+    """x̂ = s · Πᵀ · (c_j[idx_j] / scale), c_j the codebook of coordinate j's width."""
+    idx = np.asarray(idx, dtype=np.int64)
+    hi = mixed_widths(idx.shape[1], b) == b + 1
+    c_lo = np.asarray(centroids_lo, dtype=np.float64)
+    c_hi = np.asarray(centroids_hi, dtype=np.float64)
+    yhat = np.where(hi[None, :], c_hi[np.minimum(idx, len(c_hi) - 1)], c_lo[np.minimum(idx, len(c_lo) - 1)])
+    yhat = yhat / scale
+    return np.asarray(s, dtype=np.float64)[:, None] * (yhat @ np.asarray(Pi, dtype=np.float64))
+
+
+def mixed_near_threshold(v, centroids_lo, centroids_hi, b):
+    """The near-threshold band of each coordinate against its own codebook."""
+    v = np.asarray(v, dtype=np.float64)
+    hi = mixed_widths(v.shape[-1], b) == b + 1
+    return np.where(hi, near_threshold(v, centroids_hi), near_threshold(v, centroids_lo))

@@ -525,3 +525,109 @@ def test_band_width_by_uniform_draws_near_each_threshold():
         hits = int(oq.near_threshold(v, cb["centroids"]).sum())
         pr = 1e-6 * max(1.0, abs(tk)) / width
         assert abs(hits - n * pr) <= 6 * math.sqrt(n * pr * (1 - pr)), (tk, hits, n * pr)
+
+
+# ------------------------------------------------ b + 1/2 bits per coordinate
+def test_half_bit_widths_give_the_pages_bytes_per_token():
+    """The pages' 672 B per token and layer against 4 KB uncompressed: 16 vectors
+    of 42 B, i.e. 40 B of codes (2.5 bits x 128) and a 2-byte norm."""
+    g = golden("kv_bytes_per_token.json")
+    vectors = g["uncompressed_bytes"] // (g["head_dim"] * g["uncompressed_bytes_per_value"])
+    assert vectors == 16
+    per_vec = g["compressed_bytes"] / vectors
+    w = oq.mixed_widths(128, 2)
+    assert int(w.sum()) == 320 and oq.mixed_words_per_vector(128, 2) * 4 == 40
+    assert per_vec == 40 + 2
+    assert int(oq.mixed_widths(128, 1).sum()) == 192 and int(oq.mixed_widths(128, 3).sum()) == 448
+    # exactly half of every block of 16 coordinates carries the extra bit, the first eight
+    assert ((w == 3).reshape(-1, 16).sum(axis=1) == 8).all() and (w.reshape(-1, 16)[:, :8] == 3).all()
+
+
+def test_varwidth_packing_hand_example():
+    """d = 16, b = 1: coordinates 0-7 take two bits, 8-15 one bit.  Stream bits
+    0-15 are 11 00 10 01 00 00 00 00 (codes 3, 0, 1, 2, 0, 0, 0, 0, LSB first),
+    bits 16-23 are 1 0 1 0 0 0 0 1."""
+    idx = np.array([[3, 0, 1, 2, 0, 0, 0, 0, 1, 0, 1, 0, 0, 0, 0, 1]])
+    expect = (1 << 0) | (1 << 1) | (1 << 4) | (1 << 7) | (1 << 16) | (1 << 18) | (1 << 23)
+    words = oq.pack_varwidth(idx, oq.mixed_widths(16, 1))
+    assert words.shape == (1, 1) and int(words[0, 0]) == expect
+    np.testing.assert_array_equal(oq.unpack_varwidth(words, oq.mixed_widths(16, 1)), idx)
+
+
+@pytest.mark.parametrize("b", [1, 2, 3, 4])
+def test_varwidth_packing_with_one_width_is_the_canonical_packing(b):
+    rng = np.random.default_rng(40 + b)
+    idx = rng.integers(0, 1 << b, size=(50, 128))
+    a = oq.pack_varwidth(idx, [b] * 128)
+    c = oq.pack_codes(idx, b)
+    np.testing.assert_array_equal(a, c[:, :a.shape[1]])
+    assert not c[:, a.shape[1]:].any()
+
+
+def test_half_bit_pair_blocks_interleave_the_two_vectors():
+    """b = 2: coordinate 0 (3 bits) holds the even vector's code in block bits
+    0-2 and the odd vector's in 3-5; coordinate 8 (2 bits) starts at block bit
+    2·(8·3) = 48, i.e. word 1 bit 16."""
+    idx = np.zeros((2, 128), dtype=np.int64)
+    idx[0, 0], idx[1, 0], idx[0, 8], idx[1, 8] = 5, 2, 1, 3
+    words = oq.pack_mixed_pairs(idx, 2)
+    assert words.shape == (1, 20)
+    assert int(words[0, 0]) == 5 | (2 << 3)
+    assert int(words[0, 1]) == (1 << 16) | (3 << 18)
+    assert not words[0, 2:].any()
+
+
+def test_half_bit_quantize_is_a_brute_force_nearest_search_per_width():
+    d, b = 16, 1
+    rng = np.random.default_rng(7)
+    X = rng.standard_normal((40, d))
+    Pi = orot.haar_rotation(rng.standard_normal((d, d)))
+    lo, hi = ocb.build_codebook(d, b)["centroids"], ocb.build_codebook(d, b + 1)["centroids"]
+    idx, s, v = oq.mixed_quantize(X, Pi, lo, hi, b, math.sqrt(d))
+    for n in range(X.shape[0]):
+        for j in range(d):
+            cb = hi if j % 16 < 8 else lo
+            best = min(range(len(cb)), key=lambda k: abs(v[n, j] - cb[k]))
+            assert idx[n, j] == best
+    # and the rotated coordinates are √d·Π·x/‖x‖
+    np.testing.assert_allclose(v, math.sqrt(d) * (X / np.linalg.norm(X, axis=1, keepdims=True)) @ Pi.T,
+                               rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("b", [1, 2, 3])
+def test_half_bit_distortion_is_the_mean_of_the_two_codebooks(b):
+    """Per-coordinate errors add, and each half of the (exchangeable) rotated
+    coordinates carries its own codebook's distortion: E‖u - û‖² =
+    (D_b + D_(b+1)) / 2, with D_(b+1)/2 on the (b+1)-bit half."""
+    d, n = 128, 3000
+    rng = np.random.default_rng(300 + b)
+    Pi = orot.haar_rotation(rng.standard_normal((d, d)))
+    X = rng.standard_normal((n, d)) * np.exp(rng.standard_normal((n, 1)))
+    cl, ch = ocb.build_codebook(d, b), ocb.build_codebook(d, b + 1)
+    idx, s, _ = oq.mixed_quantize(X, Pi, cl["centroids"], ch["centroids"], b, math.sqrt(d))
+    Xh = oq.mixed_dequantize(idx, s, Pi, cl["centroids"], ch["centroids"], b, math.sqrt(d))
+    err = ((X - Xh) ** 2).sum(axis=1) / s ** 2
+    want = 0.5 * (cl["distortion"] + ch["distortion"])
+    assert abs(err.mean() - want) < 5 * err.std() / math.sqrt(n)
+    assert ch["distortion"] < err.mean() < cl["distortion"]
+    # the (b+1)-bit half alone, in the rotated domain
+    y = (X / s[:, None]) @ Pi.T
+    yh = (Xh / s[:, None]) @ Pi.T
+    hi = oq.mixed_widths(d, b) == b + 1
+    e_hi = ((y - yh)[:, hi] ** 2).sum(axis=1)
+    assert abs(e_hi.mean() - ch["distortion"] / 2) < 5 * e_hi.std() / math.sqrt(n)
+
+
+def test_half_bit_band_uses_each_coordinates_own_codebook():
+    d, b = 16, 2
+    lo, hi = ocb.build_codebook(d, b)["centroids"], ocb.build_codebook(d, b + 1)["centroids"]
+    t_lo, t_hi = 0.5 * (lo[1:] + lo[:-1]), 0.5 * (hi[1:] + hi[:-1])
+    v = np.full((1, d), 5.0)        # far from every threshold
+    v[0, 0] = t_hi[2]               # a (b+1)-bit coordinate on its own threshold
+    v[0, 8] = t_lo[0]               # a b-bit coordinate on its own threshold
+    v[0, 9] = t_hi[0]               # a b-bit coordinate on a threshold of the other codebook
+    v[0, 1] = t_lo[0]               # and the reverse
+    band = oq.mixed_near_threshold(v, lo, hi, b)
+    assert band[0, 0] and band[0, 8]
+    assert not band[0, 9] and not band[0, 1]
+    assert band.sum() == 2
