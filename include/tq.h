@@ -48,7 +48,7 @@ typedef enum {
   TQ_ERR_TIMEOUT = -5
 } tq_status;
 
-typedef enum { TQ_MSE = 0, TQ_PROD = 1 } tq_mode;
+typedef enum { TQ_MSE = 0, TQ_PROD = 1, TQ_MIXED = 2 } tq_mode;
 typedef enum { TQ_ROT_DENSE = 0, TQ_ROT_HADAMARD = 1 } tq_rot_kind;
 typedef enum { TQ_DENS_BETA = 0, TQ_DENS_GAUSS = 1 } tq_density;
 typedef enum { TQ_F32 = 0, TQ_F16 = 1 } tq_dtype;
@@ -107,6 +107,14 @@ tq_status tq_rotation_haar(int d, const double* h_G, double* h_Pi);
  * d, b      dimension and TOTAL bits per coordinate.  TQ_MSE quantizes with
  *           the b-bit codebook; TQ_PROD ([P1] section "TurboQuant_prod"; [P4]
  *           section "两阶段量化框架") uses a (b-1)-bit MSE stage plus 1 QJL bit.
+ *           TQ_MIXED is TurboQuant_mse at b + 1/2 bits per coordinate ([P1]
+ *           section "论文给出的关键数据点": 3.5 and 2.5 bit/channel; section
+ *           "decode 阶段：写入少，但每步都要读取历史 cache": 672 B per token and
+ *           layer = 16 vectors of 40 B of codes and a 2-byte norm): coordinate
+ *           j of Π·u takes b + 1 bits where j mod 16 < 8 and b bits elsewhere,
+ *           each half with the Lloyd-Max codebook of its own width (which half
+ *           is immaterial: the coordinates of Π·u are exchangeable); b = 1..3
+ *           (1.5, 2.5 or 3.5 bits), d = 128, TQ_ROT_DENSE only.
  * rot_kind  TQ_ROT_DENSE: h_rot is Π, d×d row-major fp64 (e.g. from
  *           tq_rotation_haar).  TQ_ROT_HADAMARD: h_rot is the sign vector σ
  *           (d entries ±1) and Π = H·diag(σ)/√d, H the Sylvester Hadamard
@@ -115,7 +123,9 @@ tq_status tq_rotation_haar(int d, const double* h_G, double* h_Pi);
  * h_S       Prod only: the QJL matrix S, d×d row-major fp64 (i.i.d. N(0,1)),
  *           m = d rows.  NULL for TQ_MSE.
  * cb        codebook of the MSE stage: cb->d == d and cb->b == b (MSE) or
- *           b - 1 (Prod).  Copied; the caller may free it afterwards.
+ *           b - 1 (Prod).  TQ_MIXED: an array of two codebooks, cb[0] with b
+ *           bits and cb[1] with b + 1 bits, both for dimension d.  Copied; the
+ *           caller may free it afterwards.
  * Synchronous.  Errors: INVALID_ARG, UNSUPPORTED (d or rot_kind), ALLOC, CUDA.
  */
 typedef struct tq_ctx tq_ctx;
@@ -138,6 +148,13 @@ tq_status tq_ctx_destroy(tq_ctx* ctx);
  *            [2*j*b_mse, 2*(j+1)*b_mse) of the block's stream, the even
  *            vector's code in the low b_mse bits.  (Used for V caches so that
  *            decode reads pairs of tokens per coordinate.)
+ *            TQ_MIXED (b_mse = b): coordinate j's code has w_j bits (b + 1
+ *            where j mod 16 < 8, else b) and occupies stream bits
+ *            [P_j, P_j + w_j), P_j = w_0 + ... + w_(j-1); words_per_vec =
+ *            d·(2b+1)/64 exactly (24, 40 or 56 bytes at d = 128, so vectors
+ *            are 8-byte, not 16-byte, multiples).  PAIR: coordinate j holds a
+ *            field of 2·w_j bits at block bit 2·P_j, the even vector's code
+ *            in its low w_j bits.
  *   d_norm   fp32 ‖x‖ per vector.
  *   d_qjl    Prod only: d/32 words of sign bits per vector (bit j = [(S·r)_j >= 0]),
  *            padded to qjl_words_per_vec; NULL for MSE.

@@ -13,7 +13,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libtq.so")
 
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_ALLOC, TQ_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
-TQ_MSE, TQ_PROD = 0, 1
+TQ_MSE, TQ_PROD, TQ_MIXED = 0, 1, 2
 TQ_ROT_DENSE, TQ_ROT_HADAMARD = 0, 1
 TQ_DENS_BETA, TQ_DENS_GAUSS = 0, 1
 TQ_F32, TQ_F16 = 0, 1
@@ -139,7 +139,8 @@ def tq_rotation_haar(G):
 
 
 class Context:
-    """Owns a tq_ctx (device tables for one (d, b, mode, rotation))."""
+    """Owns a tq_ctx (device tables for one (d, b, mode, rotation)).  TQ_MIXED
+    (b + 1/2 bits per coordinate) passes the b-bit and (b+1)-bit codebooks."""
 
     def __init__(self, d, b, mode, rot_kind, rot, S=None, codebook=None):
         import numpy as np
@@ -147,11 +148,18 @@ class Context:
         S = None if S is None else np.ascontiguousarray(S, dtype=np.float64)
         self.d, self.b, self.mode, self.rot_kind = d, b, mode, rot_kind
         self.b_mse = b - 1 if mode == TQ_PROD else b
-        self.codebook = codebook if codebook is not None else tq_codebook_build(d, self.b_mse)
+        if mode == TQ_MIXED:
+            pair = (Codebook * 2)()
+            pair[0] = tq_codebook_build(d, b) if codebook is None else codebook[0]
+            pair[1] = tq_codebook_build(d, b + 1) if codebook is None else codebook[1]
+            self.codebook = pair
+        else:
+            self.codebook = codebook if codebook is not None else tq_codebook_build(d, self.b_mse)
         h = ctypes.c_void_p()
+        cbp = (ctypes.cast(self.codebook, ctypes.POINTER(Codebook)) if mode == TQ_MIXED
+               else ctypes.byref(self.codebook))
         _check("tq_ctx_create", lib().tq_ctx_create(
-            d, b, mode, rot_kind, _ptr(rot), _ptr(S) if S is not None else None,
-            ctypes.byref(self.codebook), ctypes.byref(h)))
+            d, b, mode, rot_kind, _ptr(rot), _ptr(S) if S is not None else None, cbp, ctypes.byref(h)))
         self.handle = h
 
     def close(self):

@@ -20,6 +20,7 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
                       const tq_codes* V, int B, int Hq, int Hkv, int64_t seq, int64_t cap,
                       float scale, float* out, void* ws, cudaStream_t stream) {
   if (cap % 16 != 0) return TQ_ERR_UNSUPPORTED;
+  if (kc.mode == TQ_MIXED || vc.mode == TQ_MIXED) return TQ_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
   const bool prod = kc.mode == TQ_PROD;
   if (prod && (knew != nullptr || G > 4 || kc.b_mse > 3 || !kc.s_slices || !K->d_qjl || !K->d_rnorm ||

@@ -108,6 +108,7 @@ struct Enc128Params {
   float sqrt_df;
   float thr[15];
   float cen[16];
+  float thr_hi[15];  // b + 1/2 bits: the (BM+1)-bit codebook's thresholds
   int sym;  // thresholds symmetric about 0 (thr[H] = 0, thr[H-1-j] = -thr[H+1+j], H = 2^(BM-1) - 1)
   int layout, W, QW, pair_aligned;
   int64_t offset, group_rows, group_stride;
@@ -182,6 +183,55 @@ __device__ __forceinline__ uint32_t chunk_codes(const uint32_t (&a)[32], float f
   return m32;
 }
 
+// b + 1/2 bits per coordinate: coordinate k (0..63) of a column half has BM + 1
+// bits where k mod 16 < 8 and BM bits elsewhere; its code starts at bit
+// mixed_pos(k, BM) of the half's 2·BM + 1 words (every 16 coordinates span
+// 8·(2·BM + 1) bits, so a half is whole words of the row's stream).
+// One 32-column chunk CC (0 or 1) of a half at b + 1/2 bits: codes into the
+// half's words hw (compile-time positions), near-threshold flags returned.
+template <int BM, bool SYM, int CC>
+__device__ __forceinline__ uint32_t mix_chunk_codes(const uint32_t (&a)[32], float f, const float (&tlo)[15],
+                                                    const float (&thi)[15], uint32_t (&hw)[2 * BM + 1]) {
+  uint32_t m32 = 0u;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float v = __uint_as_float(a[j]) * f;
+    bool near;
+    if ((j & 8) == 0) {
+      const uint32_t code = bucketize_c<BM + 1, SYM>(v, thi, kMargin, near);
+      put_bits<BM + 1>(hw, mixed_pos(32 * CC + j, BM), code);
+    } else {
+      const uint32_t code = bucketize_c<BM, SYM>(v, tlo, kMargin, near);
+      put_bits<BM>(hw, mixed_pos(32 * CC + j, BM), code);
+    }
+    m32 |= (near ? 1u : 0u) << j;
+  }
+  return m32;
+}
+
+// Bits [pos, pos + width) of a word array (run-time position and width), and their replacement.
+template <int N>
+__device__ __forceinline__ uint32_t get_bits_rt(const uint32_t (&wd)[N], int pos, int width) {
+  uint32_t v = 0;
+#pragma unroll
+  for (int w = 0; w < N; ++w) {
+    const int sh = pos - 32 * w;
+    if (sh >= 0 && sh < 32) v |= wd[w] >> sh;
+    if (sh < 0 && sh > -width) v |= wd[w] << (-sh);
+  }
+  return v & ((1u << width) - 1u);
+}
+template <int N>
+__device__ __forceinline__ void set_bits_rt(uint32_t (&wd)[N], int pos, int width, uint32_t code) {
+  const uint32_t m = (1u << width) - 1u;
+#pragma unroll
+  for (int w = 0; w < N; ++w) {
+    const int sh = pos - 32 * w;
+    if (sh >= 0 && sh < 32) wd[w] = (wd[w] & ~(m << sh)) | (code << sh);
+    if (sh < 0 && sh > -width) wd[w] = (wd[w] & ~(m >> (-sh))) | (code >> (-sh));
+  }
+}
+
 // Code of coordinate `col` (a run-time index) in a chunk's BM packed words, and its replacement.
 template <int BM>
 __device__ __forceinline__ uint32_t code_at(const uint32_t (&wd)[BM], int col) {
@@ -222,7 +272,7 @@ __device__ __forceinline__ void mma3_ts(uint32_t acc, uint32_t a0, uint32_t btab
     }
 }
 
-template <int BM, bool PROD, bool F16>
+template <int BM, bool PROD, bool F16, bool MIX>
 __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Params p,
                                                                  const __grid_constant__ CUtensorMap xmap) {
   using L = Lay<F16, PROD>;
@@ -234,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
   unsigned char* sX = smem + L::OffX;
   float* norm_s = reinterpret_cast<float*>(smem + L::OffNorm);  // [AccBufs][128]
   float* thr_s = reinterpret_cast<float*>(smem + L::OffThr);    // thresholds, +inf padded to 16
-  float* cen_s = reinterpret_cast<float*>(smem + L::OffCen);    // centroids
+  float* cen_s = reinterpret_cast<float*>(smem + L::OffCen);    // centroids (MIX: the (BM+1)-bit thresholds)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OffBar);
   uint64_t* x_full = bars;         // [3] TMA bytes
   uint64_t* x_empty = bars + 3;    // [3] prep warps (+ the MMA commit for fp16 rows)
@@ -284,7 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
   }
   if (tid < 16) {
     thr_s[tid] = tid < (1 << BM) - 1 ? p.thr[tid] : INFINITY;
-    cen_s[tid] = tid < (1 << BM) ? p.cen[tid] : 0.f;
+    if constexpr (MIX)
+      cen_s[tid] = tid < (2 << BM) - 1 ? p.thr_hi[tid] : INFINITY;
+    else
+      cen_s[tid] = tid < (1 << BM) ? p.cen[tid] : 0.f;
   }
   if (warp == 0) tmem_alloc(tmem_slot, L::TmemCols);
   tc_fence_before();
@@ -502,6 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
       // (chunk c of a row is words [c·BM, c·BM + BM) of its stream), recompute
       // flagged coordinates, store
       uint32_t cw[2][BM];
+      uint32_t hw[MIX ? 2 * BM + 1 : 1];  // b + 1/2 bits: the half's codes (mix_pos)
+#pragma unroll
+      for (int w = 0; w < (MIX ? 2 * BM + 1 : 1); ++w) hw[w] = 0u;
       float g2 = 0.f;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -513,11 +569,23 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[ab]);
         }
-        uint32_t m32 = p.sym ? chunk_codes<BM, true, PROD>(cc ? a1 : a0, f, p.thr, cen_s, cw[cc], g2)
-                             : chunk_codes<BM, false, PROD>(cc ? a1 : a0, f, p.thr, cen_s, cw[cc], g2);
+        uint32_t m32;
+        if constexpr (MIX) {
+          if (cc == 0)
+            m32 = p.sym ? mix_chunk_codes<BM, true, 0>(a0, f, p.thr, p.thr_hi, hw)
+                        : mix_chunk_codes<BM, false, 0>(a0, f, p.thr, p.thr_hi, hw);
+          else
+            m32 = p.sym ? mix_chunk_codes<BM, true, 1>(a1, f, p.thr, p.thr_hi, hw)
+                        : mix_chunk_codes<BM, false, 1>(a1, f, p.thr, p.thr_hi, hw);
+        } else {
+          m32 = p.sym ? chunk_codes<BM, true, PROD>(cc ? a1 : a0, f, p.thr, cen_s, cw[cc], g2)
+                      : chunk_codes<BM, false, PROD>(cc ? a1 : a0, f, p.thr, cen_s, cw[cc], g2);
+        }
         if (!live) {
 #pragma unroll
           for (int w = 0; w < BM; ++w) cw[cc][w] = 0u;
+#pragma unroll
+          for (int w = 0; w < (MIX ? 2 * BM + 1 : 1); ++w) hw[w] = 0u;
           m32 = 0u;
           g2 = 0.f;
         }
@@ -560,17 +628,24 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
           if (lane == src) {
             const float vv = (float)(((double)sh + (double)sl) * (p.sqrt_d / (double)ssrc));
             bool nr;
-            const uint32_t code = bucketize<BM>(vv, thr_s, 0.f, nr);
-            if constexpr (PROD) {
-              const uint32_t old = code_at<BM>(cw[cc], j);
-              const float e0 = vv - cen_s[old], e1 = vv - cen_s[code];
-              g2 += e1 * e1 - e0 * e0;
+            if constexpr (MIX) {
+              const bool hi = (j & 8) == 0;
+              const uint32_t code = hi ? bucketize<BM + 1>(vv, cen_s, 0.f, nr) : bucketize<BM>(vv, thr_s, 0.f, nr);
+              set_bits_rt(hw, mixed_pos(32 * cc + j, BM), hi ? BM + 1 : BM, code);
+            } else {
+              const uint32_t code = bucketize<BM>(vv, thr_s, 0.f, nr);
+              if constexpr (PROD) {
+                const uint32_t old = code_at<BM>(cw[cc], j);
+                const float e0 = vv - cen_s[old], e1 = vv - cen_s[code];
+                g2 += e1 * e1 - e0 * e0;
+              }
+              set_code<BM>(cw[cc], j, code);
             }
-            set_code<BM>(cw[cc], j, code);
           }
         }
-        // stores of this chunk's codes
-        if (p.layout == TQ_LAYOUT_TOKEN) {
+        // stores of this chunk's codes (b + 1/2 bits: of both chunks, below)
+        if (MIX) {
+        } else if (p.layout == TQ_LAYOUT_TOKEN) {
           if (valid) {
             uint32_t* dst = p.codes + dv * p.W + c * BM;
 #pragma unroll
@@ -615,6 +690,67 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
                 if (k / BM == slot) {
                   m |= 1u << bt;
                   bits |= ((code_at<BM>(cw[cc], j) >> (k % BM)) & 1u) << bt;
+                }
+              }
+              atomicAnd(blk + w, ~m);
+              atomicOr(blk + w, bits);
+            }
+          }
+        }
+      }
+      if constexpr (MIX) {
+        // the half's 2·BM + 1 words: coordinates 64·half .. 64·half + 63
+        constexpr int HW = 2 * BM + 1;
+        if (p.layout == TQ_LAYOUT_TOKEN) {
+          if (valid) {
+            uint32_t* dst = p.codes + dv * p.W + half * HW;
+#pragma unroll
+            for (int w = 0; w < HW; ++w) dst[w] = hw[w];
+          }
+        } else {
+          // PAIR: coordinate k's field of 2·w_k bits at block bit 2·P_k.  The
+          // half's block words are 2·HW: the even lane of a row pair writes the
+          // first HW (coordinates 0-31 of the half), the odd lane the rest
+          // (32-63, whose fields sit at the same offsets within its words).
+          uint32_t part[HW];
+#pragma unroll
+          for (int w = 0; w < HW; ++w) part[w] = __shfl_xor_sync(kFull, hw[w], 1);
+          const int64_t base_row = row - (even ? 0 : 1);
+          const bool whole = p.pair_aligned && base_row + 1 < p.N;
+          uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)p.W) + half * 2 * HW;
+          if (valid && whole) {
+            uint32_t ow[HW];
+#pragma unroll
+            for (int w = 0; w < HW; ++w) ow[w] = 0u;
+#pragma unroll
+            for (int kk = 0; kk < 32; ++kk) {
+              const int wk = (kk & 8) ? BM : BM + 1, pk = mixed_pos(kk, BM);
+              const uint32_t own = even ? get_bits_rt(hw, pk, wk) : get_bits_rt(hw, pk + 16 * HW, wk);
+              const uint32_t prt = even ? get_bits_rt(part, pk, wk) : get_bits_rt(part, pk + 16 * HW, wk);
+              set_bits_rt(ow, 2 * pk, wk, even ? own : prt);
+              set_bits_rt(ow, 2 * pk + wk, wk, even ? prt : own);
+            }
+#pragma unroll
+            for (int w = 0; w < HW; ++w) blk[(even ? 0 : HW) + w] = ow[w];
+          } else if (valid) {
+            // the partner is written by another call (or not at all): this
+            // vector's fields of the half's 2·HW block words by masked atomics
+            const int slot = (int)(dv & 1);
+#pragma unroll 1
+            for (int w = 0; w < 2 * HW; ++w) {
+              uint32_t m = 0u, bits = 0u;
+#pragma unroll 1
+              for (int k = 0; k < 64; ++k) {
+                const int wk = (k & 8) ? BM : BM + 1;
+                const int pos = 2 * mixed_pos(k, BM) + slot * wk - 32 * w;  // relative to word w
+                if (pos >= 32 || pos + wk <= 0) continue;
+                const uint32_t code = get_bits_rt(hw, mixed_pos(k, BM), wk), fm = (1u << wk) - 1u;
+                if (pos >= 0) {
+                  m |= fm << pos;
+                  bits |= code << pos;
+                } else {
+                  m |= fm >> (-pos);
+                  bits |= code >> (-pos);
                 }
               }
               atomicAnd(blk + w, ~m);
@@ -687,9 +823,9 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
   }
 }
 
-template <int BM, bool PROD, bool F16>
+template <int BM, bool PROD, bool F16, bool MIX = false>
 cudaError_t launch_t(const Enc128Params& p, const CUtensorMap& xmap, cudaStream_t st) {
-  auto k = encode128_kernel<BM, PROD, F16>;
+  auto k = encode128_kernel<BM, PROD, F16, MIX>;
   static PerDeviceValue attr;  // set once per device, before any stream capture
   const cudaError_t e = smem_attr_once(attr, (const void*)k, Lay<F16, PROD>::SmemAlloc);
   if (e != cudaSuccess) return e;
@@ -700,7 +836,16 @@ cudaError_t launch_t(const Enc128Params& p, const CUtensorMap& xmap, cudaStream_
 }
 
 template <bool F16>
-cudaError_t launch_mode(const Enc128Params& p, const CUtensorMap& xmap, int bm, bool prod, cudaStream_t st) {
+cudaError_t launch_mode(const Enc128Params& p, const CUtensorMap& xmap, int bm, bool prod, bool mix,
+                        cudaStream_t st) {
+  if (mix) {
+    switch (bm) {
+      case 1: return launch_t<1, false, F16, true>(p, xmap, st);
+      case 2: return launch_t<2, false, F16, true>(p, xmap, st);
+      case 3: return launch_t<3, false, F16, true>(p, xmap, st);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (prod) {
     switch (bm) {
       case 1: return launch_t<1, true, F16>(p, xmap, st);
@@ -721,8 +866,8 @@ cudaError_t launch_mode(const Enc128Params& p, const CUtensorMap& xmap, int bm, 
 }  // namespace
 
 bool enc128_supported(const DevCtx& c) {
-  return c.d == kDim && c.enc_tab != nullptr && (c.mode == TQ_MSE || c.enc_tab_m != nullptr) &&
-         c.b_mse >= 1 && c.b_mse <= (c.mode == TQ_PROD ? 3 : 4);
+  return c.d == kDim && c.enc_tab != nullptr && (c.mode != TQ_PROD || c.enc_tab_m != nullptr) &&
+         c.b_mse >= 1 && c.b_mse <= (c.mode == TQ_MSE ? 4 : 3);
 }
 
 tq_status launch_encode128(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
@@ -744,11 +889,16 @@ tq_status launch_encode128(const DevCtx& c, const void* x, int x_dtype, int64_t 
   p.sqrt_df = (float)p.sqrt_d;
   for (int k = 0; k < 15; ++k) p.thr[k] = c.thr[k];
   for (int k = 0; k < 16; ++k) p.cen[k] = c.cen[k];
+  for (int k = 0; k < 15; ++k) p.thr_hi[k] = c.thr_hi[k];
+  const bool mix = c.mode == TQ_MIXED;
   {
-    const int nt = (1 << c.b_mse) - 1, h = nt / 2;
-    bool sym = c.thr[h] == 0.f;
-    for (int j = 0; sym && j < h; ++j) sym = c.thr[h - 1 - j] == -c.thr[h + 1 + j];
-    p.sym = sym ? 1 : 0;
+    auto symmetric = [](const float* thr, int bits) {
+      const int nt = (1 << bits) - 1, h = nt / 2;
+      bool sym = thr[h] == 0.f;
+      for (int j = 0; sym && j < h; ++j) sym = thr[h - 1 - j] == -thr[h + 1 + j];
+      return sym;
+    };
+    p.sym = symmetric(c.thr, c.b_mse) && (!mix || symmetric(c.thr_hi, c.b_mse + 1)) ? 1 : 0;
   }
   p.layout = out->layout;
   p.W = c.words_per_vec;
@@ -762,8 +912,8 @@ tq_status launch_encode128(const DevCtx& c, const void* x, int x_dtype, int64_t 
   CUtensorMap xmap;
   const tq_status ms = rows_tensor_map(&xmap, x, N, c.d, x_dtype == TQ_F16);
   if (ms != TQ_OK) return ms;
-  const cudaError_t e = x_dtype == TQ_F16 ? launch_mode<true>(p, xmap, c.b_mse, c.mode == TQ_PROD, stream)
-                                          : launch_mode<false>(p, xmap, c.b_mse, c.mode == TQ_PROD, stream);
+  const cudaError_t e = x_dtype == TQ_F16 ? launch_mode<true>(p, xmap, c.b_mse, c.mode == TQ_PROD, mix, stream)
+                                          : launch_mode<false>(p, xmap, c.b_mse, c.mode == TQ_PROD, mix, stream);
   return e == cudaSuccess ? TQ_OK : set_cuda_error(e);
 }
 

@@ -431,13 +431,17 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
                         const double* h_S, const tq_codebook* cb, tq_ctx** out) {
   if (!out || !h_rot || !cb) return TQ_ERR_INVALID_ARG;
   *out = nullptr;
-  if (mode != TQ_MSE && mode != TQ_PROD) return TQ_ERR_INVALID_ARG;
+  if (mode != TQ_MSE && mode != TQ_PROD && mode != TQ_MIXED) return TQ_ERR_INVALID_ARG;
   if (rot_kind != TQ_ROT_DENSE && rot_kind != TQ_ROT_HADAMARD) return TQ_ERR_INVALID_ARG;
-  if (b < 1 || b > 4 || (mode == TQ_PROD && b < 2)) return TQ_ERR_INVALID_ARG;
+  if (b < 1 || b > 4 || (mode == TQ_PROD && b < 2) || (mode == TQ_MIXED && b > 3)) return TQ_ERR_INVALID_ARG;
   if (d % 32 != 0 || d < 32 || d > kMaxD) return TQ_ERR_INVALID_ARG;
   if (!d_supported(d)) return TQ_ERR_UNSUPPORTED;
   const int b_mse = mode == TQ_PROD ? b - 1 : b;
   if (cb->d != d || cb->b != b_mse) return TQ_ERR_INVALID_ARG;
+  const bool mixed = mode == TQ_MIXED;
+  if (mixed && (cb[1].d != d || cb[1].b != b + 1)) return TQ_ERR_INVALID_ARG;
+  // b + 1/2 bits: the tensor-memory encoder, the scorer and decode at d = 128
+  if (mixed && (d != kChunk || rot_kind != TQ_ROT_DENSE)) return TQ_ERR_UNSUPPORTED;
   if (mode == TQ_PROD && !h_S) return TQ_ERR_INVALID_ARG;
   if (mode == TQ_PROD && d > kChunk) return TQ_ERR_UNSUPPORTED;
   int hm = 0;
@@ -447,6 +451,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   Ctx* c = new (std::nothrow) Ctx();
   if (!c) return TQ_ERR_ALLOC;
   c->cb = *cb;
+  if (mixed) c->cb_hi = cb[1];
   const size_t dd = (size_t)d * d;
   c->h_pi = new (std::nothrow) double[dd];
   if (!c->h_pi) {
@@ -484,21 +489,26 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   v.mode = mode;
   v.rot = rot_kind;
   v.wait_limit = kWaitLimitDefault;
-  v.words_per_vec = words_per_vector(d, b_mse);
+  v.words_per_vec = mixed ? mixed_words_per_vector(d, b) : words_per_vector(d, b_mse);
   v.qjl_words_per_vec = mode == TQ_PROD ? words_per_vector(d, 1) : 0;
   v.sqrt_d = (float)std::sqrt((double)d);
   v.pi_scale = (float)pow2_near(std::sqrt((double)d));
   const int K = 1 << b_mse;
   for (int k = 0; k < K; ++k) v.cen[k] = (float)cb->centroid[k];
   for (int k = 0; k + 1 < K; ++k) v.thr[k] = (float)cb->threshold[k];
+  const int KH = mixed ? 2 * K : 0;  // TQ_MIXED: the (b+1)-bit codebook
+  for (int k = 0; k < KH; ++k) v.cen_hi[k] = (float)cb[1].centroid[k];
+  for (int k = 0; k + 1 < KH; ++k) v.thr_hi[k] = (float)cb[1].threshold[k];
 
-  // alpha: scale that makes alpha·c_k closest to fp16 values (max relative error)
+  // alpha: scale that makes alpha·c_k closest to fp16 values (max relative
+  // error); one alpha for both codebooks of TQ_MIXED, whose tables share the
+  // logit and output scales
   {
     double best = 1e30, best_a = 1.0;
     for (int j = 0; j < 65536; ++j) {
       double a = 1.0 + j / 65536.0, worst = 0.0;
-      for (int k = K / 2; k < K; ++k) {
-        double x = a * cb->centroid[k];
+      for (int k = K / 2; k < K + KH; ++k) {
+        double x = a * (k < K ? cb->centroid[k] : cb[1].centroid[k - K]);
         if (x == 0.0) continue;
         double r = std::fabs((double)h_val(h_bits((float)x)) - x) / std::fabs(x);
         worst = std::max(worst, r);
@@ -576,6 +586,11 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
     int k0 = p & (K - 1), k1 = p >> b_mse;
     lut[p] = pack_h2((float)(v.alpha * cb->centroid[k0]), (float)(v.alpha * cb->centroid[k1]));
   }
+  std::vector<uint32_t> lut_hi(mixed ? (size_t)1 << (2 * (b + 1)) : 0);
+  for (size_t p = 0; p < lut_hi.size(); ++p) {
+    const int k0 = (int)(p & (size_t)(KH - 1)), k1 = (int)(p >> (b + 1));
+    lut_hi[p] = pack_h2((float)(v.alpha * cb[1].centroid[k0]), (float)(v.alpha * cb[1].centroid[k1]));
+  }
 
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
   size_t o_pi = 0;
@@ -589,7 +604,8 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   size_t o_e1 = o_um + al(umma.size() * sizeof(uint16_t));
   size_t o_e2 = o_e1 + al(enc128.size() * sizeof(uint16_t));
   size_t o_lut = o_e2 + al(enc128m.size() * sizeof(uint16_t));
-  size_t o_st = o_lut + al(lut.size() * sizeof(uint32_t));
+  size_t o_lh = o_lut + al(lut.size() * sizeof(uint32_t));
+  size_t o_st = o_lh + al(lut_hi.size() * sizeof(uint32_t));
   size_t total = o_st + 256;
   void* dmem = nullptr;
   cudaError_t e = cudaMalloc(&dmem, total);
@@ -616,6 +632,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   if (e == cudaSuccess) e = up(o_e1, enc128.data(), enc128.size() * sizeof(uint16_t));
   if (e == cudaSuccess) e = up(o_e2, enc128m.data(), enc128m.size() * sizeof(uint16_t));
   if (e == cudaSuccess) e = up(o_lut, lut.data(), lut.size() * sizeof(uint32_t));
+  if (e == cudaSuccess) e = up(o_lh, lut_hi.data(), lut_hi.size() * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(base + o_st, 0, 256);
   if (e != cudaSuccess) {
     cudaFree(dmem);
@@ -637,6 +654,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   v.pi_slices = d == kChunk ? (const float4*)(base + o_sl) : nullptr;
   v.signs = rot_kind == TQ_ROT_HADAMARD ? (const float*)(base + o_sg) : nullptr;
   v.lut = (const uint32_t*)(base + o_lut);
+  v.lut_hi = mixed ? (const uint32_t*)(base + o_lh) : nullptr;
   v.status = (int*)(base + o_st);
   *out = reinterpret_cast<tq_ctx*>(c);
   return TQ_OK;
@@ -851,7 +869,7 @@ tq_status tq_unpack_indices(const tq_codes* codes, int64_t first, int64_t count,
     return TQ_ERR_INVALID_ARG;
   if (count == 0) return TQ_OK;
   const int d = codes->d, b = codes->b_mse, W = codes->words_per_vec;
-  const bool pair = codes->layout == TQ_LAYOUT_PAIR;
+  const bool pair = codes->layout == TQ_LAYOUT_PAIR, mixed = codes->mode == TQ_MIXED;
   // copy the covering range of words
   int64_t v0 = pair ? first / 2 * 2 : first;
   int64_t v1 = pair ? (first + count + 1) / 2 * 2 : first + count;
@@ -864,15 +882,17 @@ tq_status tq_unpack_indices(const tq_codes* codes, int64_t first, int64_t count,
     for (int j = 0; j < d; ++j) {
       int64_t bitpos;
       const uint32_t* base;
+      const int wj = mixed ? mixed_width(j, b) : b;
+      const int64_t pj = mixed ? mixed_pos(j, b) : (int64_t)j * b;
       if (!pair) {
         base = &w[(size_t)(vi - v0) * W];
-        bitpos = (int64_t)j * b;
+        bitpos = pj;
       } else {
         base = &w[(size_t)(vi / 2 * 2 - v0) * W];
-        bitpos = (int64_t)2 * j * b + (vi & 1) * b;
+        bitpos = 2 * pj + (vi & 1) * wj;
       }
       int code = 0;
-      for (int k = 0; k < b; ++k) {
+      for (int k = 0; k < wj; ++k) {
         int64_t p = bitpos + k;
         code |= ((base[p / 32] >> (p % 32)) & 1u) << k;
       }

@@ -36,6 +36,8 @@ struct DevCtx {
   float alpha;           // LUT values are fp16(alpha * centroid)
   float thr[15];         // thresholds, unit-variance units (fp32)
   float cen[16];         // centroids, unit-variance units (fp32)
+  float thr_hi[15];      // TQ_MIXED: the (b+1)-bit codebook's thresholds
+  float cen_hi[16];      // TQ_MIXED: the (b+1)-bit codebook's centroids
   const uint2* enc_pi;   // encoder B fragments of Π (hi/lo)
   const uint2* enc_m;    // encoder B fragments of S·Πᵀ (hi/lo), Prod only
   const float* pi;       // Π, d×d row-major fp32
@@ -48,12 +50,14 @@ struct DevCtx {
   const float* signs;    // Hadamard rotation: σ, d entries of ±1 (else null)
   int had_m, had_p;      // Hadamard rotation: H = H12 ⊗ H_m (had_p = 12) or H_m (had_p = 1)
   const uint32_t* lut;   // pair table: 2^(2 b_mse) fp16x2 entries (alpha-scaled)
+  const uint32_t* lut_hi;  // TQ_MIXED: pair table of the (b+1)-bit codebook, same alpha
   int* status;           // device status word
 };
 
 struct Ctx {
   DevCtx dev;
   tq_codebook cb;
+  tq_codebook cb_hi;        // TQ_MIXED: the (b+1)-bit codebook
   double* h_pi = nullptr;   // d×d fp64
   double* h_s = nullptr;    // d×d fp64 (Prod)
   void* d_alloc = nullptr;  // single device allocation holding every table
@@ -66,6 +70,15 @@ inline int words_per_vector(int d, int bits) {
   int w = (bits * d + 31) / 32;
   return (w + 3) / 4 * 4;
 }
+
+// b + 1/2 bits per coordinate: coordinate j has b + 1 bits where j mod 16 < 8,
+// b elsewhere; its code starts at stream bit mixed_pos(j, b).  Every block of 16
+// coordinates spans 8·(2b+1) bits, so d = 128 needs d·(2b+1)/64 whole words.
+__host__ __device__ constexpr int mixed_width(int j, int b) { return (j & 8) ? b : b + 1; }
+__host__ __device__ constexpr int mixed_pos(int j, int b) {
+  return (j >> 4) * 8 * (2 * b + 1) + ((j & 8) ? 8 * (b + 1) + (j & 7) * b : (j & 7) * (b + 1));
+}
+inline int mixed_words_per_vector(int d, int b) { return d * (2 * b + 1) / 64; }
 
 // kernel launchers (defined in the .cu files)
 tq_status launch_encode(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,

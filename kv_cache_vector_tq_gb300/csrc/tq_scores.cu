@@ -117,6 +117,7 @@ struct ScoreParams {
   const uint32_t* qjl;
   const float* rnorm;
   const uint32_t* lut;  // pair table: 2^(2b) fp16x2 entries α·c_k
+  const uint32_t* lut_hi;  // b + 1/2 bits: the (b+1)-bit codebook's pair table (same α)
   int64_t first, N;
   int W, QW;
   const unsigned char* btile;  // this launch's B operand (kBBytes)
@@ -128,15 +129,17 @@ struct ScoreParams {
   uint32_t wait_limit;
 };
 
-template <int BM, bool PROD>
+template <int BM, bool PROD, bool MIX>
 __global__ void __launch_bounds__(kThreads, 1) scores_kernel(const ScoreParams p) {
   constexpr int E = 1 << (2 * BM);
+  constexpr int EH = MIX ? 4 * E : 0;  // b + 1/2 bits: entries of the (b+1)-bit pair table
   constexpr int KS = PROD ? kK / 16 : 128 / 16;  // MMAs per tile
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* sA = smem;                        // 2 stages
   unsigned char* sB = smem + 2 * kAStage;
   uint32_t* lut = reinterpret_cast<uint32_t*>(sB + kBBytes);  // [E][32] replicated per lane
-  uint64_t* bars = reinterpret_cast<uint64_t*>(lut + E * 32);
+  uint32_t* lut_hi = lut + E * 32;                             // [EH][32] (b + 1/2 bits)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(lut_hi + EH * 32);
   uint64_t* a_full = bars;              // [2] 4 decode warps
   uint64_t* a_empty = bars + 2;         // [2] MMA commit
   uint64_t* acc_full = bars + 4;        // [4] MMA commit
@@ -164,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) scores_kernel(const ScoreParams p
     fence_mbar_init();
   }
   for (int i = tid; i < E * 32; i += kThreads) lut[i] = __ldg(p.lut + (i >> 5));
+  for (int i = tid; i < EH * 32; i += kThreads) lut_hi[i] = __ldg(p.lut_hi + (i >> 5));
   if (warp == 0) tmem_alloc(tmem_slot, kAccBufs * kAccCols);
   tc_fence_before();
   __syncthreads();
@@ -178,7 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1) scores_kernel(const ScoreParams p
     // ---------------- decode: key r = 32·warp + lane of the tile, all 128 coordinates
     const int r = 32 * warp + lane;
     const uint32_t* mylut = lut + lane;
-    constexpr int CW = 4 * BM;  // code words of a key
+    const uint32_t* mylut_hi = lut_hi + lane;
+    constexpr int CW = MIX ? 2 * (2 * BM + 1) : 4 * BM;  // code words of a key
     uint32_t cw[CW], sw[4];
     auto fetch = [&](int64_t tile) {
       const int64_t key = tile * kKeyTile + r;
@@ -209,7 +214,14 @@ __global__ void __launch_bounds__(kThreads, 1) scores_kernel(const ScoreParams p
       for (int k8 = 0; k8 < 16; ++k8) {
         uint32_t v[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = mylut[get_bits<2 * BM>(c, (8 * k8 + 2 * e) * BM) << 5];
+        for (int e = 0; e < 4; ++e) {
+          if constexpr (MIX) {  // coordinates 8·k8.. take BM + 1 bits for even k8, BM for odd
+            const int pos = mixed_pos(8 * k8 + 2 * e, BM);
+            v[e] = (k8 & 1) ? mylut[get_bits<2 * BM>(c, pos) << 5] : mylut_hi[get_bits<2 * BM + 2>(c, pos) << 5];
+          } else {
+            v[e] = mylut[get_bits<2 * BM>(c, (8 * k8 + 2 * e) * BM) << 5];
+          }
+        }
         *reinterpret_cast<uint4*>(A + core_off(r, 8 * k8)) = make_uint4(v[0], v[1], v[2], v[3]);
       }
       if constexpr (PROD) {  // ±1 for 128 sign bits
@@ -310,11 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1) scores_kernel(const ScoreParams p
   }
 }
 
-template <int BM, bool PROD>
+template <int BM, bool PROD, bool MIX = false>
 cudaError_t run_scores(const ScoreParams& p, cudaStream_t st) {
   constexpr int E = 1 << (2 * BM);
-  constexpr size_t smem = 2 * kAStage + kBBytes + E * 32 * 4 + 256;
-  auto k = scores_kernel<BM, PROD>;
+  constexpr size_t smem = 2 * kAStage + kBBytes + (MIX ? 5 : 1) * E * 32 * 4 + 256;
+  auto k = scores_kernel<BM, PROD, MIX>;
   static PerDeviceValue attr;  // set once per device, outside any later stream capture
   const cudaError_t e = smem_attr_once(attr, (const void*)k, (int)smem);
   if (e != cudaSuccess) return e;
@@ -346,6 +358,7 @@ tq_status launch_scores(const DevCtx& c, const float* q, int M, const tq_codes* 
   p.qjl = keys->d_qjl;
   p.rnorm = keys->d_rnorm;
   p.lut = c.lut;
+  p.lut_hi = c.lut_hi;
   p.first = first;
   p.N = N;
   p.W = c.words_per_vec;
@@ -360,6 +373,16 @@ tq_status launch_scores(const DevCtx& c, const float* q, int M, const tq_codes* 
     p.m0 = m0;
     p.mq = std::min(kQTile, M - m0);
     p.btile = bt + (size_t)(m0 / kQTile) * kBBytes;
+    if (c.mode == TQ_MIXED) {
+      switch (c.b_mse) {
+        case 1: e = run_scores<1, false, true>(p, stream); break;
+        case 2: e = run_scores<2, false, true>(p, stream); break;
+        case 3: e = run_scores<3, false, true>(p, stream); break;
+        default: return TQ_ERR_UNSUPPORTED;
+      }
+      if (e != cudaSuccess) return set_cuda_error(e);
+      continue;
+    }
     switch (c.b_mse) {
       case 1: e = prod ? run_scores<1, true>(p, stream) : run_scores<1, false>(p, stream); break;
       case 2: e = prod ? run_scores<2, true>(p, stream) : run_scores<2, false>(p, stream); break;

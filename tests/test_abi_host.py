@@ -97,6 +97,30 @@ def test_ctx_validation_before_device(L):
     assert L.tq_ctx_destroy(None) == tq.TQ_ERR_INVALID_ARG
 
 
+def test_mixed_ctx_validation_before_device(L):
+    """b + 1/2 bits: two codebooks (b and b + 1 bits), b = 1..3, d = 128 and the
+    dense rotation only."""
+    p = tq._ptr
+    out = ctypes.c_void_p()
+
+    def pair(d, b0, b1):
+        arr = (tq.Codebook * 2)()
+        arr[0], arr[1] = tq.tq_codebook_build(d, b0), tq.tq_codebook_build(d, b1)
+        return ctypes.cast(arr, ctypes.POINTER(tq.Codebook)), arr
+
+    cb, keep = pair(128, 2, 3)
+    bad, keep2 = pair(128, 2, 4)  # second codebook not b + 1 bits
+    cb4, keep3 = pair(128, 4, 4)
+    cb256, keep4 = pair(256, 2, 3)
+    I128, I256 = np.eye(128), np.eye(256)
+    assert L.tq_ctx_create(128, 2, tq.TQ_MIXED, 0, p(I128), None, bad, ctypes.byref(out)) == tq.TQ_ERR_INVALID_ARG
+    assert L.tq_ctx_create(128, 4, tq.TQ_MIXED, 0, p(I128), None, cb4, ctypes.byref(out)) == tq.TQ_ERR_INVALID_ARG
+    assert L.tq_ctx_create(256, 2, tq.TQ_MIXED, 0, p(I256), None, cb256, ctypes.byref(out)) == tq.TQ_ERR_UNSUPPORTED
+    assert L.tq_ctx_create(128, 2, tq.TQ_MIXED, 1, p(np.ones(128)), None, cb, ctypes.byref(out)) == tq.TQ_ERR_UNSUPPORTED
+    assert L.tq_ctx_create(128, 2, 3, 0, p(I128), None, cb, ctypes.byref(out)) == tq.TQ_ERR_INVALID_ARG
+    assert not out.value
+
+
 def test_unpack_validation(L):
     c = tq.Codes()
     assert L.tq_unpack_indices(ctypes.byref(c), 0, 1, None, None) == tq.TQ_ERR_INVALID_ARG
