@@ -245,8 +245,11 @@ tq_status tq_scores(const tq_ctx* ctx, const float* d_q, int M, const tq_codes* 
  * γ·√(π/2)/d·⟨S q, 2·bits − 1⟩ with both query rotations done once per call.
  * K then needs its QJL words and γ (qjl, rnorm), and Hq / Hkv <= 4
  * (TQ_ERR_UNSUPPORTED otherwise).
- * kctx, vctx  contexts of the K (TQ_MSE or TQ_PROD) and V (TQ_MSE) codes; may
- *             be the same.
+ * kctx, vctx  contexts of the K (TQ_MSE, TQ_PROD or TQ_MIXED) and V (TQ_MSE
+ *             or TQ_MIXED) codes; may be the same.  b + 1/2 bits ([P1]
+ *             section "论文给出的关键数据点"): K and V both TQ_MIXED with the
+ *             same b and codebooks, any GQA of 1, 2, 4, 8 (TQ_ERR_UNSUPPORTED
+ *             otherwise).
  * d_q       [B, Hq, d], fp32 or fp16 (q_dtype).
  * K         TOKEN layout; V: PAIR layout.  Vector index of token t of
  *           (batch b, kv head h) is (b * Hkv + h) * cap + t; tokens [0, seq)
@@ -279,7 +282,7 @@ tq_status tq_decode_attention(const tq_ctx* kctx, const tq_ctx* vctx, const void
  * rounding) into position seq-1 of every (batch, KV head) block of K and V,
  * then computes tq_decode_attention over tokens [0, seq) including the new
  * one, in one kernel launch.  Keys must be TurboQuant_MSE here
- * (TQ_ERR_UNSUPPORTED for TQ_PROD: append with tq_encode, then call
+ * (TQ_ERR_UNSUPPORTED for TQ_PROD and TQ_MIXED: append with tq_encode, then call
  * tq_decode_attention).  Other arguments, the workspace and errors as
  * tq_decode_attention.  The V pair block of position seq-1 is updated with atomics, so
  * its partner token (seq-2 or seq) may be written by an ordered earlier call.

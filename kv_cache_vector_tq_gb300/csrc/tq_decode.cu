@@ -20,7 +20,15 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
                       const tq_codes* V, int B, int Hq, int Hkv, int64_t seq, int64_t cap,
                       float scale, float* out, void* ws, cudaStream_t stream) {
   if (cap % 16 != 0) return TQ_ERR_UNSUPPORTED;
-  if (kc.mode == TQ_MIXED || vc.mode == TQ_MIXED) return TQ_ERR_UNSUPPORTED;
+  // b + 1/2 bits: K and V both, equal b and identical tables, in the attention
+  // entry (append with tq_encode first)
+  const bool mixed = kc.mode == TQ_MIXED || vc.mode == TQ_MIXED;
+  if (mixed) {
+    bool same = kc.mode == vc.mode && kc.b_mse == vc.b_mse && kc.alpha == vc.alpha && knew == nullptr;
+    for (int k = 0; same && k < (1 << kc.b_mse); ++k) same = kc.cen[k] == vc.cen[k];
+    for (int k = 0; same && k < (2 << kc.b_mse); ++k) same = kc.cen_hi[k] == vc.cen_hi[k];
+    if (!same) return TQ_ERR_UNSUPPORTED;
+  }
   const int G = Hq / Hkv;
   const bool prod = kc.mode == TQ_PROD;
   if (prod && (knew != nullptr || G > 4 || kc.b_mse > 3 || !kc.s_slices || !K->d_qjl || !K->d_rnorm ||
@@ -35,6 +43,7 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
   p.status = kc.status;
   p.klut = kc.lut;
   p.vlut = vc.lut;
+  p.klut_hi = kc.lut_hi;
   p.same_lut = same_lut ? 1 : 0;
   for (int k = 0; k < 15; ++k) {
     p.kthr[k] = kc.thr[k];
@@ -69,7 +78,9 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
   p.counters = static_cast<int*>(ws);
   p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + ws_counter_bytes(groups));
   cudaError_t e;
-  if (prod)
+  if (mixed)
+    e = decode_run_mixed(p, kc.b_mse, G, groups, stream);
+  else if (prod)
     e = decode_run_prod(p, kc.b_mse, vc.b_mse, G, groups, stream);
   else if (kc.b_mse == 1 || kc.b_mse == 2)
     e = decode_run_k12(p, kc.b_mse, vc.b_mse, G, groups, stream);

@@ -128,38 +128,41 @@ __device__ __forceinline__ float4 ldg_early(const float4* p) {
 
 
 // ------------------------------------------------------------------ parameters
+// Field order is part of the tuning: the fields the tile loop reads come first
+// (inserting a pointer among them once cost ~0.3 us per call at b = 4).
 struct StepParams {
-  const float4* kslices;  // Π of the K context in column slices (see the rotation below)
-  const float4* vslices;  // the same for the V context
-  const float* vpi;       // Π of the V context, 128 x 128 row-major fp32 (output rotation)
-  const uint32_t* klut;
-  const uint32_t* vlut;
-  int same_lut;
-  float kthr[15];
-  float vthr[15];
-  float kfold;  // scale·log2(e) / (√d·α_K)
-  float qfold;  // Prod keys: scale·log2(e)·√(π/2) / d (the QJL term)
-  const float4* sslices;  // Prod keys: S in column slices, like kslices
-  const uint32_t* kqjl;   // Prod keys: sign words, 4 per token
-  const float* krn;       // Prod keys: γ per token
-  float vfold;  // 1 / (α_V·√d)
-  float sqrt_d;
   uint32_t* kcodes;
   float* knorm;
   uint32_t* vcodes;
   float* vnorm;
   int64_t seq, cap;
+  const uint32_t* kqjl;   // Prod keys: sign words, 4 per token
+  const float* krn;       // Prod keys: γ per token
+  const float* vpi;       // Π of the V context, 128 x 128 row-major fp32 (output rotation)
+  float vfold;  // 1 / (α_V·√d)
+  float kfold;  // scale·log2(e) / (√d·α_K)
+  float qfold;  // Prod keys: scale·log2(e)·√(π/2) / d (the QJL term)
+  float sqrt_d;
   int B, Hq, Hkv, S, tiles;
+  int same_lut;
+  const float4* kslices;  // Π of the K context in column slices (see the rotation below)
+  const float4* vslices;  // the same for the V context
+  const uint32_t* klut;
+  const uint32_t* vlut;
+  const float4* sslices;  // Prod keys: S in column slices, like kslices
   int* status;    // device status word of the K context
   int* counters;  // [B*Hkv] arrival counters (zero between calls)
   float* part;    // [B*Hkv][S][G][kPart] per-CTA (m, l, Πᵀ·acc) when S > 1
   const void* q;
-  int q_f16;
   const void* knew;
   const void* vnew;
+  float* out;
+  const uint32_t* klut_hi;  // b + 1/2 bits: the (b+1)-bit pair table (K and V share both tables)
+  int q_f16;
   int new_f16;
   int append;
-  float* out;
+  float kthr[15];
+  float vthr[15];
 };
 
 // First tile of CTA u of the U CTAs that share a (batch, KV head).  With an
@@ -187,12 +190,15 @@ __host__ __device__ inline int pi_off(int G) {
   return ((a > b ? a : b) + 127) / 128 * 128;
 }
 
-__host__ __device__ inline StepSmem step_smem(int bk, int bv, int G, int W, bool same_lut, bool q) {
+__host__ __device__ inline StepSmem step_smem(int bk, int bv, int G, int W, bool same_lut, bool q,
+                                             bool mx = false) {
   StepSmem m;
   const int NT = (2 * G + 7) / 8, NCH = W / 4;
   int o = (1 << (2 * bk)) * 32 * 4;
-  m.vlut = o;
-  if (bk == 4 && bv == 4)
+  m.vlut = o;  // b + 1/2 bits: where the (b+1)-bit table starts (V shares both tables)
+  if (mx)
+    o += (4 << (2 * bk)) * 32 * 4;
+  else if (bk == 4 && bv == 4)
     o = 256 * 256;  // byte-indexed rows: K entries at lane·4, V entries at 128 + lane·4
   else if (!same_lut)
     o += (1 << (2 * bv)) * 32 * 4;
@@ -233,7 +239,7 @@ __host__ __device__ inline StepSmem step_smem(int bk, int bv, int G, int W, bool
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int BK, int BV, int G, int W, bool Q>
+template <int BK, int BV, int G, int W, bool Q, bool MX = false>
 __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams p) {
   constexpr int NT = (2 * G + 7) / 8;
   constexpr int WK = 4 * BK, WV = 4 * BV;  // words per vector
@@ -247,12 +253,19 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
   constexpr bool kByte = BK == 4 && BV == 4;      // pair codes are whole bytes
   static_assert(W % 4 == 0 && NTH >= 256, "4 warps per rotation chunk; a thread per new-token element");
   static_assert(!Q || (G <= 4 && BK <= 3), "Prod keys: up to 4 query heads per KV head, (b-1)-bit codes");
+  // b + 1/2 bits per coordinate (MX): K and V both at b + 1/2 with the same
+  // tables; coordinates j mod 16 < 8 take BK + 1 bits.  A vector is
+  // WX = 2·(2·BK + 1) words; a lane's 32 K coordinates (or 16 V coordinate
+  // pairs) are 16·(2·BK + 1) contiguous bits from a word or half-word boundary.
+  static_assert(!MX || (!Q && BK == BV && BK <= 3), "b + 1/2 bits: MSE keys and values of equal b <= 3");
+  constexpr int WX = 2 * (2 * BK + 1);
   constexpr int SB = stage_bytes(Q);
   extern __shared__ __align__(128) unsigned char smem[];
-  const StepSmem L = step_smem(BK, BV, G, W, p.same_lut != 0, Q);
+  const StepSmem L = step_smem(BK, BV, G, W, p.same_lut != 0, Q, MX);
   uint32_t* klut = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* khi = reinterpret_cast<uint32_t*>(smem + L.vlut);  // MX: the (BK+1)-bit table
   uint32_t* qlut = reinterpret_cast<uint32_t*>(smem + L.qlut);  // Prod keys
-  uint32_t* vlut = p.same_lut ? klut : reinterpret_cast<uint32_t*>(smem + L.vlut);
+  uint32_t* vlut = (p.same_lut || MX) ? klut : reinterpret_cast<uint32_t*>(smem + L.vlut);
   unsigned char* stage = smem + L.stage;
   float* qs = reinterpret_cast<float*>(smem + L.qs);      // [G][128]
   float* qhat = reinterpret_cast<float*>(smem + L.qhat);  // [G][128]
@@ -340,7 +353,20 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
       const int i = tid + k * NTH;
       if (i < EK * 8) reinterpret_cast<uint4*>(klut)[i] = make_uint4(v[k], v[k], v[k], v[k]);
     }
-    if (!p.same_lut) {
+    if constexpr (MX) {  // the (BK+1)-bit table, 4·EK entries
+      constexpr int NH = (4 * EK * 8 + NTH - 1) / NTH;
+      uint32_t u[NH];
+#pragma unroll
+      for (int k = 0; k < NH; ++k) {
+        const int i = tid + k * NTH;
+        u[k] = i < 4 * EK * 8 ? __ldg(p.klut_hi + (i >> 3)) : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < NH; ++k) {
+        const int i = tid + k * NTH;
+        if (i < 4 * EK * 8) reinterpret_cast<uint4*>(khi)[i] = make_uint4(u[k], u[k], u[k], u[k]);
+      }
+    } else if (!p.same_lut) {
       constexpr int NV = (EV * 8 + NTH - 1) / NTH;
       uint32_t u[NV];
 #pragma unroll
@@ -381,11 +407,24 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     if (tile < t_end) {
       unsigned char* st = my_stage + (j % kStages) * SB;
       const int64_t vb = gbase + (int64_t)tile * kTileTok;
-      copy_words<BK>(st + 0 * kFieldBytes + lane * 16, p.kcodes + (vb + g) * WK + t * BK);
-      copy_words<BK>(st + 1 * kFieldBytes + lane * 16, p.kcodes + (vb + g + 8) * WK + t * BK);
-      // V pair blocks t and t+4 of the tile; this lane's coordinates 16g..16g+15
-      copy_words<BV>(st + 2 * kFieldBytes + lane * 16, p.vcodes + (vb + 2 * t) * WV + g * BV);
-      copy_words<BV>(st + 3 * kFieldBytes + lane * 16, p.vcodes + (vb + 2 * t + 8) * WV + g * BV);
+      if constexpr (MX) {
+        // BK + 1 words from the word holding the lane's first bit (bit
+        // 16·(2·BK + 1)·t of a K row, ·g of a V pair block)
+        const int ko = (t * (2 * BK + 1)) >> 1, vo = (g * (2 * BK + 1)) >> 1;
+#pragma unroll
+        for (int w = 0; w <= BK; ++w) {
+          cp_async4(st + 0 * kFieldBytes + lane * 16 + 4 * w, p.kcodes + (vb + g) * WX + ko + w);
+          cp_async4(st + 1 * kFieldBytes + lane * 16 + 4 * w, p.kcodes + (vb + g + 8) * WX + ko + w);
+          cp_async4(st + 2 * kFieldBytes + lane * 16 + 4 * w, p.vcodes + (vb + 2 * t) * WX + vo + w);
+          cp_async4(st + 3 * kFieldBytes + lane * 16 + 4 * w, p.vcodes + (vb + 2 * t + 8) * WX + vo + w);
+        }
+      } else {
+        copy_words<BK>(st + 0 * kFieldBytes + lane * 16, p.kcodes + (vb + g) * WK + t * BK);
+        copy_words<BK>(st + 1 * kFieldBytes + lane * 16, p.kcodes + (vb + g + 8) * WK + t * BK);
+        // V pair blocks t and t+4 of the tile; this lane's coordinates 16g..16g+15
+        copy_words<BV>(st + 2 * kFieldBytes + lane * 16, p.vcodes + (vb + 2 * t) * WV + g * BV);
+        copy_words<BV>(st + 3 * kFieldBytes + lane * 16, p.vcodes + (vb + 2 * t + 8) * WV + g * BV);
+      }
       if (lane < 8)  // lanes 0-3: the 16 K norms, lanes 4-7: the 16 V norms
         cp_async16(st + 4 * kFieldBytes + lane * 16, (lane < 4 ? p.knorm : p.vnorm) + vb + 4 * (lane & 3));
       if constexpr (Q) {  // lanes 8-11: the 16 γ; lanes 12-27: the 16 tokens' sign words
@@ -590,6 +629,7 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
 
   // ---- 3. stream the tiles
   const uint32_t* mykl = klut + lane;
+  const uint32_t* mykh = khi + lane;  // MX: the (BK+1)-bit table
   const uint32_t* myvl = vlut + lane;
   const uint32_t lane4 = lane * 4;
   const uint32_t tbase = smem_u32(smem);  // shared-window address of the byte-row tables
@@ -616,11 +656,26 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     const int tile = t_begin + warp + j * W;
     cp_async_wait<kStages - 1>();
     const unsigned char* st = my_stage + (j % kStages) * SB;
-    uint32_t k0[BK], k1[BK], v0w[BV], v1w[BV];
-    read_words<BK>(k0, st + 0 * kFieldBytes + lane * 16);
-    read_words<BK>(k1, st + 1 * kFieldBytes + lane * 16);
-    read_words<BV>(v0w, st + 2 * kFieldBytes + lane * 16);
-    read_words<BV>(v1w, st + 3 * kFieldBytes + lane * 16);
+    constexpr int KN = MX ? BK + 1 : BK, VN = MX ? BV + 1 : BV;
+    uint32_t k0[KN], k1[KN], v0w[VN], v1w[VN];
+    read_words<KN>(k0, st + 0 * kFieldBytes + lane * 16);
+    read_words<KN>(k1, st + 1 * kFieldBytes + lane * 16);
+    read_words<VN>(v0w, st + 2 * kFieldBytes + lane * 16);
+    read_words<VN>(v1w, st + 3 * kFieldBytes + lane * 16);
+    if constexpr (MX) {  // bring the lane's first bit to bit 0 (odd t for K, odd g for V)
+      const uint32_t ks = (uint32_t)(t & 1) * 16u, vs = (uint32_t)(g & 1) * 16u;
+#pragma unroll
+      for (int w = 0; w + 1 < KN; ++w) {
+        k0[w] = __funnelshift_r(k0[w], k0[w + 1], ks);
+        k1[w] = __funnelshift_r(k1[w], k1[w + 1], ks);
+        v0w[w] = __funnelshift_r(v0w[w], v0w[w + 1], vs);
+        v1w[w] = __funnelshift_r(v1w[w], v1w[w + 1], vs);
+      }
+      k0[KN - 1] >>= ks;
+      k1[KN - 1] >>= ks;
+      v0w[VN - 1] >>= vs;
+      v1w[VN - 1] >>= vs;
+    }
     const float* ns = reinterpret_cast<const float*>(st + 4 * kFieldBytes);
     float4 nrm = make_float4(ns[g], ns[g + 8], ns[16 + g], ns[16 + g + 8]);
     // Prod keys: this tile's sign words (bits j = 32t + 4s + {0..3} of tokens g,
@@ -635,7 +690,7 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
       gam0 = gm[g];
       gam1 = gm[g + 8];
     }
-    if (owner && tile == new_tile) {  // the appended token: use the codes just made
+    if (!MX && owner && tile == new_tile) {  // the appended token: use the codes just made
       if (new_row == g) {
 #pragma unroll
         for (int w = 0; w < BK; ++w) k0[w] = nk_words[t * BK + w];
@@ -678,6 +733,19 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
         a1 = lds_at<0>(tbase + byte_row_addr(k1[s >> 1], lane4, 2 * (s & 1)));
         a2 = lds_at<0>(tbase + byte_row_addr(k0[s >> 1], lane4, 2 * (s & 1) + 1));
         a3 = lds_at<0>(tbase + byte_row_addr(k1[s >> 1], lane4, 2 * (s & 1) + 1));
+      } else if constexpr (MX) {  // coordinates 4s..4s+3 of the lane's 32: BK + 1 bits for s mod 4 < 2
+        const int p0 = mixed_pos(4 * s, BK), p2 = mixed_pos(4 * s + 2, BK);
+        if ((s & 2) == 0) {
+          a0 = mykh[get_bits<2 * BK + 2>(k0, p0) << 5];
+          a1 = mykh[get_bits<2 * BK + 2>(k1, p0) << 5];
+          a2 = mykh[get_bits<2 * BK + 2>(k0, p2) << 5];
+          a3 = mykh[get_bits<2 * BK + 2>(k1, p2) << 5];
+        } else {
+          a0 = mykl[get_bits<2 * BK>(k0, p0) << 5];
+          a1 = mykl[get_bits<2 * BK>(k1, p0) << 5];
+          a2 = mykl[get_bits<2 * BK>(k0, p2) << 5];
+          a3 = mykl[get_bits<2 * BK>(k1, p2) << 5];
+        }
       } else {
         a0 = mykl[get_bits<2 * BK>(k0, 4 * s * BK) << 5];
         a1 = mykl[get_bits<2 * BK>(k1, 4 * s * BK) << 5];
@@ -786,6 +854,19 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
         a1 = lds_at<128>(tbase + byte_row_addr(v0w[mt >> 1], lane4, 2 * (mt & 1) + 1));
         a2 = lds_at<128>(tbase + byte_row_addr(v1w[mt >> 1], lane4, 2 * (mt & 1)));
         a3 = lds_at<128>(tbase + byte_row_addr(v1w[mt >> 1], lane4, 2 * (mt & 1) + 1));
+      } else if constexpr (MX) {  // pair fields of coordinates 2mt, 2mt+1: BV + 1 bits each for mt < 4
+        const int q0 = 2 * mixed_pos(2 * mt, BV), q1 = 2 * mixed_pos(2 * mt + 1, BV);
+        if (mt < 4) {
+          a0 = mykh[get_bits<2 * BV + 2>(v0w, q0) << 5];
+          a1 = mykh[get_bits<2 * BV + 2>(v0w, q1) << 5];
+          a2 = mykh[get_bits<2 * BV + 2>(v1w, q0) << 5];
+          a3 = mykh[get_bits<2 * BV + 2>(v1w, q1) << 5];
+        } else {
+          a0 = myvl[get_bits<2 * BV>(v0w, q0) << 5];
+          a1 = myvl[get_bits<2 * BV>(v0w, q1) << 5];
+          a2 = myvl[get_bits<2 * BV>(v1w, q0) << 5];
+          a3 = myvl[get_bits<2 * BV>(v1w, q1) << 5];
+        }
       } else {
         a0 = myvl[get_bits<2 * BV>(v0w, (2 * mt) * 2 * BV) << 5];
         a1 = myvl[get_bits<2 * BV>(v0w, (2 * mt + 1) * 2 * BV) << 5];
@@ -971,14 +1052,14 @@ static int choose_splits(int tiles, int groups, int W, bool append, int merge_ca
   return bestS;
 }
 
-template <int BK, int BV, int G, bool Q = false>
+template <int BK, int BV, int G, bool Q = false, bool MX = false>
 static cudaError_t run_step(const StepParams& p, int groups, cudaStream_t st) {
   constexpr int W = G >= 8 ? 8 : 16;
-  auto kern = decode_step_kernel<BK, BV, G, W, Q>;
+  auto kern = decode_step_kernel<BK, BV, G, W, Q, MX>;
   static PerDeviceValue smem_attr;  // set once per device, before any stream capture
   const cudaError_t e = smem_attr_once(smem_attr, (const void*)kern, 227 * 1024);
   if (e != cudaSuccess) return e;
-  const StepSmem L = step_smem(BK, BV, G, W, p.same_lut != 0, Q);
+  const StepSmem L = step_smem(BK, BV, G, W, p.same_lut != 0, Q, MX);
   StepParams pp = p;
   pp.S = choose_splits(p.tiles, groups, W, p.append != 0, L.mw / (G * kPart * 4));
   cudaLaunchConfig_t cfg = {};
@@ -1022,5 +1103,7 @@ cudaError_t decode_run_k12(const StepParams& p, int bk, int bv, int G, int group
 cudaError_t decode_run_k34(const StepParams& p, int bk, int bv, int G, int groups, cudaStream_t st);
 // Prod keys ((b−1)-bit codes bk in 1..3), G in {1, 2, 4}
 cudaError_t decode_run_prod(const StepParams& p, int bk, int bv, int G, int groups, cudaStream_t st);
+// K and V at b + 1/2 bits per coordinate (b in 1..3), G in {1, 2, 4, 8}
+cudaError_t decode_run_mixed(const StepParams& p, int b, int G, int groups, cudaStream_t st);
 
 }  // namespace tq

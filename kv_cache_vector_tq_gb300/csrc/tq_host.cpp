@@ -780,7 +780,7 @@ tq_status tq_decode_attention(const tq_ctx* kctx, const tq_ctx* vctx, const void
   if (!kctx || !vctx || !K || !V) return TQ_ERR_INVALID_ARG;
   const DevCtx& kc = reinterpret_cast<const Ctx*>(kctx)->dev;
   const DevCtx& vc = reinterpret_cast<const Ctx*>(vctx)->dev;
-  if (vc.mode != TQ_MSE || kc.d != vc.d) return TQ_ERR_INVALID_ARG;  // keys MSE or Prod, values MSE
+  if ((vc.mode != TQ_MSE && vc.mode != TQ_MIXED) || kc.d != vc.d) return TQ_ERR_INVALID_ARG;  // values MSE or b + 1/2 bits
   tq_status st = check_codes(kc, K);
   if (st != TQ_OK) return st;
   st = check_codes(vc, V);
@@ -809,7 +809,7 @@ tq_status tq_decode_step(const tq_ctx* kctx, const tq_ctx* vctx, const void* d_q
   if (!kctx || !vctx || !K || !V) return TQ_ERR_INVALID_ARG;
   const DevCtx& kc = reinterpret_cast<const Ctx*>(kctx)->dev;
   const DevCtx& vc = reinterpret_cast<const Ctx*>(vctx)->dev;
-  if (vc.mode != TQ_MSE || kc.d != vc.d) return TQ_ERR_INVALID_ARG;
+  if ((vc.mode != TQ_MSE && vc.mode != TQ_MIXED) || kc.d != vc.d) return TQ_ERR_INVALID_ARG;
   if (kc.mode != TQ_MSE) return TQ_ERR_UNSUPPORTED;  // the fused append encodes MSE keys only
   tq_status st = check_codes(kc, K);
   if (st != TQ_OK) return st;
@@ -842,7 +842,7 @@ tq_status tq_decode_attention_noalloc(const tq_ctx* kctx, const tq_ctx* vctx, co
   if (!kctx || !vctx || !K || !V) return TQ_ERR_INVALID_ARG;
   const DevCtx& kc = reinterpret_cast<const Ctx*>(kctx)->dev;
   const DevCtx& vc = reinterpret_cast<const Ctx*>(vctx)->dev;
-  if (vc.mode != TQ_MSE || kc.d != vc.d) return TQ_ERR_INVALID_ARG;  // keys MSE or Prod, values MSE
+  if ((vc.mode != TQ_MSE && vc.mode != TQ_MIXED) || kc.d != vc.d) return TQ_ERR_INVALID_ARG;  // values MSE or b + 1/2 bits
   tq_status st = check_codes(kc, K);
   if (st != TQ_OK) return st;
   st = check_codes(vc, V);

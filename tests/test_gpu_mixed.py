@@ -164,3 +164,80 @@ def test_mixed_scores(b, N, M):
     got = out.cpu().numpy().astype(np.float64)
     bound = 1e-4 * np.linalg.norm(Q, axis=1)[:, None] * np.linalg.norm(X.astype(np.float64), axis=1)[None, :]
     assert (np.abs(got - ref) <= bound).all(), f"max err/bound {np.max(np.abs(got - ref) / bound)}"
+
+
+def run_decode_mixed(b, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float16):
+    """Decode attention over b + 1/2-bit K (TOKEN) and V (PAIR) caches, each with
+    its own Haar rotation, against fp64 attention over the oracle's
+    dequantization of the GPU's own codes (2e-3·‖out‖ per head)."""
+    cap = cap or (seq + 15) // 16 * 16
+    kctx, Pk = mixed_pair(seed, b)
+    vctx, Pv = mixed_pair(seed + 1000, b)
+    Kh, Vh = synth.kv_layer(seed, 0, B, Hkv, seq, D)
+    Kc = tq.CodeSet(kctx, B * Hkv * cap, tq.TQ_LAYOUT_TOKEN)
+    Vc = tq.CodeSet(vctx, B * Hkv * cap, tq.TQ_LAYOUT_PAIR)
+    tq.tq_encode(kctx, torch.from_numpy(np.ascontiguousarray(Kh.reshape(-1, D))).cuda(), Kc, offset=0,
+                 group_rows=seq, group_stride=cap)
+    tq.tq_encode(vctx, torch.from_numpy(np.ascontiguousarray(Vh.reshape(-1, D))).cuda(), Vc, offset=0,
+                 group_rows=seq, group_stride=cap)
+    q_np = synth.queries(seed, B * Hq, D).reshape(B, Hq, D)
+    q = torch.from_numpy(q_np).cuda().to(q_dtype)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(tq.tq_decode_workspace_size(kctx, B, Hq, Hkv, seq) // 4 + 4, dtype=torch.float32, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    tq.tq_decode_attention(kctx, vctx, q, Kc, Vc, B, Hq, Hkv, seq, cap, scale, out, ws)
+    torch.cuda.synchronize()
+    assert kctx.poll() == tq.TQ_OK and vctx.poll() == tq.TQ_OK
+    lo, hi = codebooks(b)
+
+    def rebuild(cs, Pi):
+        idx = np.concatenate([tq.tq_unpack_indices(cs, blk * cap, seq) for blk in range(B * Hkv)]).astype(np.int64)
+        nrm = cs.norm.cpu().numpy().reshape(B * Hkv, cap)[:, :seq].reshape(-1).astype(np.float64)
+        return oq.mixed_dequantize(idx, nrm, Pi, lo, hi, b, math.sqrt(D)).reshape(B, Hkv, seq, D)
+
+    from oracle import attention as oatt
+    ref = oatt.decode_attention(q.float().cpu().numpy().astype(np.float64), rebuild(Kc, Pk), rebuild(Vc, Pv), scale)
+    got = out.cpu().numpy().astype(np.float64)
+    rel = np.linalg.norm(got - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
+    assert rel.max() <= 2e-3, f"max per-head relative error {rel.max()}"
+    return rel.max()
+
+
+@pytest.mark.parametrize("b", [1, 2, 3])
+def test_mixed_decode_one_layer(b):
+    """One layer, B = 1, 32 query / 8 KV heads, seq 16384: the decode workload at
+    1.5, 2.5 and 3.5 bits per coordinate."""
+    run_decode_mixed(b, 1, 32, 8, 16384)
+
+
+@pytest.mark.parametrize("seq", [1, 15, 17, 33, 1000])
+def test_mixed_decode_ragged_seq(seq):
+    run_decode_mixed(2, 2, 8, 2, seq, cap=((seq + 15) // 16 + 1) * 16)
+
+
+@pytest.mark.parametrize("gqa", [1, 2, 4, 8])
+def test_mixed_decode_gqa(gqa):
+    run_decode_mixed(3, 1, 4 * gqa, 4, 777, q_dtype=torch.float32)
+
+
+def test_mixed_decode_refusals():
+    """b + 1/2-bit caches decode in the attention entry with K and V at the same
+    b; the fused append and mixed/uniform pairs are refused."""
+    kctx, _ = mixed_pair(0, 2)
+    vctx, _ = mixed_pair(1, 3)
+    uctx = tq.Context(D, 2, tq.TQ_MSE, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(synth.gaussian_matrix(2, D)))
+    cap, seq = 32, 20
+    Kc = tq.CodeSet(kctx, 4 * cap, tq.TQ_LAYOUT_TOKEN)
+    q = torch.zeros((1, 8, D), dtype=torch.float16, device="cuda")
+    out = torch.empty((1, 8, D), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(tq.tq_decode_workspace_size(kctx, 1, 8, 4, seq) // 4 + 4, dtype=torch.float32, device="cuda")
+    for vc in (vctx, uctx):
+        Vc = tq.CodeSet(vc, 4 * cap, tq.TQ_LAYOUT_PAIR)
+        with pytest.raises(tq.TqError) as e:
+            tq.tq_decode_attention(kctx, vc, q, Kc, Vc, 1, 8, 4, seq, cap, 0.1, out, ws)
+        assert e.value.status == tq.TQ_ERR_UNSUPPORTED
+    Vc = tq.CodeSet(kctx, 4 * cap, tq.TQ_LAYOUT_PAIR)
+    new = torch.zeros((4, D), dtype=torch.float16, device="cuda")
+    with pytest.raises(tq.TqError) as e:
+        tq.tq_decode_step(kctx, kctx, q, new, new, Kc, Vc, 1, 8, 4, seq, cap, 0.1, out, ws)
+    assert e.value.status == tq.TQ_ERR_UNSUPPORTED
