@@ -52,7 +52,7 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true",
                     help="decode: skip the other configurations' measurements in the same run")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "encode", "scores", "longctx", "keys", "prefill"],
+                    choices=["decode", "encode", "scores", "longctx", "keys", "prefill", "mixed"],
                     help="decode (the headline) or a secondary workload (see bench_workloads.py)")
     ap.add_argument("--dim", type=int, default=3072, help="encode: vector dimension")
     ap.add_argument("--rows", type=int, default=100_000, help="encode: number of vectors")
@@ -390,6 +390,10 @@ def other_configs(args, world, rank, local):
     lc = bw.run_longctx(ns(steps=5), world, rank, local, ROOT, Clocks, {})
     out["longctx_80_layers"] = _summary(lc, ("prefill_encode_mvec_s", "ms_per_layer", "layers"))
     torch.cuda.empty_cache()
+    mx = bw.run_mixed(ns(steps=20, bits=2), world, rank, local, ROOT, Clocks, {})
+    out["decode_2p5bit"] = _summary(mx, ("encode_mvec_s", "encode_roofline")) | {
+        "us_per_call": mx["roofline"]["us_per_call"]}
+    torch.cuda.empty_cache()
     for rot in ("dense", "hadamard"):
         ln = bw.run_encode(ns(steps=5, dim=128, rows=1_000_000, rotation=rot), world, rank, local, ROOT, Clocks, {})
         out[f"bulk_encode_d128_{rot}_1m"] = _summary(ln)
@@ -516,6 +520,35 @@ def cpu_scores_baseline(tq, cs, q, G, S):
             "kind": "oracle", "sample": f"64 queries x {n} keys (fp64 explicit dequantization)"}
 
 
+def cpu_mixed_baseline(tq, rep, b, cap, q):
+    """Oracle decode at b + 1/2 bits (explicit dequantization, fp64) on one KV
+    head x 4096 tokens of the GPU's cache, as decode-attn GB/s of its bytes."""
+    import numpy as np
+
+    from kv_cache_vector_tq_gb300 import synth
+    from oracle import attention as oatt
+    from oracle import codebook as ocb
+    from oracle import quantizer as oq
+    from oracle import rotation as orot
+    K, V = rep
+    n = 4096
+    lo, hi = ocb.build_codebook(D, b)["centroids"], ocb.build_codebook(D, b + 1)["centroids"]
+    Pk = orot.haar_rotation(synth.gaussian_matrix(0, D))
+    Pv = orot.haar_rotation(synth.gaussian_matrix(1, D))
+    ik, iv = tq.tq_unpack_indices(K, 0, n).astype(np.int64), tq.tq_unpack_indices(V, 0, n).astype(np.int64)
+    kn = K.norm[:n].cpu().numpy().astype(np.float64)
+    vn = V.norm[:n].cpu().numpy().astype(np.float64)
+    qs = q[:, :HQ // HKV].float().cpu().numpy().astype(np.float64)
+    t0 = time.perf_counter()
+    Kh = oq.mixed_dequantize(ik, kn, Pk, lo, hi, b, math.sqrt(D)).reshape(1, 1, n, D)
+    Vh = oq.mixed_dequantize(iv, vn, Pv, lo, hi, b, math.sqrt(D)).reshape(1, 1, n, D)
+    oatt.decode_attention(qs, Kh, Vh, 1 / math.sqrt(D))
+    t = time.perf_counter() - t0
+    nbytes = n * 2 * (K.words_per_vec * 4 + 4)
+    return {"value": round(nbytes / t / 1e9, 6), "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "sample": f"1 KV head x {n} tokens, {HQ // HKV} query heads (fp64 explicit dequantization)"}
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, world, rank):
     """The oracle as it stands, timed on the host cores, same metric/config."""
@@ -578,9 +611,9 @@ def main():
     elif args.workload != "decode":
         import bench_workloads as bw
         run = {"encode": bw.run_encode, "scores": bw.run_scores, "longctx": bw.run_longctx,
-               "keys": bw.run_keys, "prefill": bw.run_prefill}[args.workload]
+               "keys": bw.run_keys, "prefill": bw.run_prefill, "mixed": bw.run_mixed}[args.workload]
         line = run(args, world, rank, local, ROOT, Clocks,
-                   {"encode": cpu_encode_baseline, "scores": cpu_scores_baseline})
+                   {"encode": cpu_encode_baseline, "scores": cpu_scores_baseline, "mixed": cpu_mixed_baseline})
     else:
         line = run_tq(args, world, rank, local)
     if line is not None:

@@ -1,4 +1,4 @@
-"""Secondary workloads of bench.py (--workload encode | scores | longctx | keys).
+"""Secondary workloads of bench.py (--workload encode | scores | longctx | keys | prefill | mixed).
 
 Each prints one JSON line in the same shape as the decode headline:
   encode   bulk indexing: b = 4, d = --dim (1536 / 3072), N = --rows fp32 rows
@@ -13,6 +13,10 @@ Each prints one JSON line in the same shape as the decode headline:
            over all layers; metric decode-attn HBM GB/s.
   keys     d = 128, b = 3: encode 4096 fp32 keys (channels 0-3 x20), then score
            one query against them; metric encode Mvec/s (scores in config).
+  mixed    the decode layer of the headline at b + 1/2 bits per coordinate
+           (--bits 1..3, 2.5 bits by default): append with tq_encode, then
+           attend; metric decode-attn HBM GB/s, the encoder at that width on
+           1M fp16 rows in config.
 Inputs of the large workloads are generated on the device (torch's seeded
 generator) with the same distributions as the seeded host recipes the parity
 tests use; the parity tests cover the same kernels on host-generated rows.
@@ -465,4 +469,126 @@ def run_keys(args, world, rank, local, root, clocks_cls, cpu):
                   "traffic": None, "kernel": "encode_kernel + scores_kernel (latency-bound at this size)",
                   "peak_kind": kind},
                  None, 2 * args.steps, clk)
+    return line if rank == 0 else None
+
+
+# ---------------------------------------------------------------- b + 1/2 bits per coordinate
+def run_mixed(args, world, rank, local, root, clocks_cls, cpu):
+    """One decode layer (batch 1, 32 q / 8 kv heads, head_dim 128, seq 16384)
+    with K and V at b + 1/2 bits per coordinate (b = --bits when 1..3, else 2:
+    2.5 bits).  A step appends the new token's K and V with tq_encode and
+    attends with tq_decode_attention (three launches), on each of R replica
+    caches larger than L2 together.  The roofline unit is the attention call;
+    the same line reports the encoder at that width on 1M fp16 rows."""
+    import numpy as np
+    import torch
+
+    import kv_cache_vector_tq_gb300 as tq
+    from kv_cache_vector_tq_gb300 import synth
+    torch.cuda.set_device(local)
+    b = args.bits if args.bits in (1, 2, 3) else 2
+    D, B, HQ, HKV, SEQ = 128, 1, 32, 8, 16384
+    kctx = tq.Context(D, b, tq.TQ_MIXED, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(synth.gaussian_matrix(0, D)))
+    vctx = tq.Context(D, b, tq.TQ_MIXED, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(synth.gaussian_matrix(1, D)))
+    cap = SEQ
+    Kh, Vh = synth.kv_layer(0, 0, B, HKV, SEQ, D)
+    K0 = tq.CodeSet(kctx, B * HKV * cap, tq.TQ_LAYOUT_TOKEN)
+    V0 = tq.CodeSet(vctx, B * HKV * cap, tq.TQ_LAYOUT_PAIR)
+    tq.tq_encode(kctx, torch.from_numpy(np.ascontiguousarray(Kh[:, :, :SEQ - 1].reshape(-1, D))).cuda(), K0, 0,
+                 SEQ - 1, cap)
+    tq.tq_encode(vctx, torch.from_numpy(np.ascontiguousarray(Vh[:, :, :SEQ - 1].reshape(-1, D))).cuda(), V0, 0,
+                 SEQ - 1, cap)
+    vec_bytes = K0.words_per_vec * 4 + 4  # codes + fp32 norm
+    cache_bytes = B * HKV * SEQ * 2 * vec_bytes
+    R = max(2, int(math.ceil(4 * 129 * 1024 * 1024 / cache_bytes)))
+    reps = [(K0, V0)]
+    for _ in range(R - 1):
+        Kr, Vr = tq.CodeSet(kctx, B * HKV * cap, tq.TQ_LAYOUT_TOKEN), tq.CodeSet(vctx, B * HKV * cap, tq.TQ_LAYOUT_PAIR)
+        Kr.codes.copy_(K0.codes), Kr.norm.copy_(K0.norm), Vr.codes.copy_(V0.codes), Vr.norm.copy_(V0.norm)
+        reps.append((Kr, Vr))
+    knew = torch.from_numpy(np.ascontiguousarray(Kh[:, :, SEQ - 1].reshape(-1, D))).cuda()
+    vnew = torch.from_numpy(np.ascontiguousarray(Vh[:, :, SEQ - 1].reshape(-1, D))).cuda()
+    q = torch.from_numpy(synth.queries(0, B * HQ, D).reshape(B, HQ, D)).to(torch.float16).cuda()
+    out = torch.empty((B, HQ, D), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(tq.tq_decode_workspace_size(kctx, B, HQ, HKV, SEQ) // 4 + 64, dtype=torch.float32, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    stream = torch.cuda.Stream()
+
+    def step(r, append=True):
+        K, V = reps[r]
+        if append:
+            tq.tq_encode(kctx, knew, K, SEQ - 1, 1, cap)
+            tq.tq_encode(vctx, vnew, V, SEQ - 1, 1, cap)
+        tq.tq_decode_attention(kctx, vctx, q, K, V, B, HQ, HKV, SEQ, cap, scale, out, ws)
+
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            step(r)
+    torch.cuda.synchronize()
+    g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
+        for r in range(R):
+            step(r)
+    with torch.cuda.graph(g_attn, stream=stream):
+        for r in range(R):
+            step(r, append=False)
+    torch.cuda.synchronize()
+    total_ms, clk = _timed(g_step.replay, args.steps, args.warmup, stream, clocks_cls, local)
+    assert kctx.poll() == tq.TQ_OK and vctx.poll() == tq.TQ_OK
+    attn_bytes = cache_bytes + q.numel() * 2 + out.numel() * 4
+    step_bytes = attn_bytes + 2 * B * HKV * (D * 2 + vec_bytes)  # + the appended rows in, their codes out
+    value = world * args.steps * R * step_bytes / (total_ms * 1e-3) / 1e9
+    reps_attn = max(5, min(200, args.steps))
+    attn_ms, _ = _timed(g_attn.replay, reps_attn, 1, stream, clocks_cls, local)
+    attn_us = attn_ms * 1e3 / (reps_attn * R)
+    hbm, _, kind = _peaks(root)
+    ach = attn_bytes / (attn_us * 1e-6) / 1e9
+    # end to end: q and the new K/V rows from pinned host memory, the output back, per step
+    q_h, kn_h, vn_h = q.cpu().pin_memory(), knew.cpu().pin_memory(), vnew.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 50))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for r in range(R):
+                q.copy_(q_h, non_blocking=True)
+                knew.copy_(kn_h, non_blocking=True)
+                vnew.copy_(vn_h, non_blocking=True)
+                step(r)
+                out_h.copy_(out, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e = {"value": round(world * e2e_steps * R * step_bytes / (e0.elapsed_time(e1) * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": R * (q.numel() + knew.numel() + vnew.numel()) * 2,
+           "d2h_bytes_per_step": R * out.numel() * 4}
+    # the encoder at this width: 1M fp16 rows (2 KV heads' worth of the same recipe, tiled)
+    N = 1 << 20
+    X = torch.from_numpy(np.ascontiguousarray(Kh.reshape(-1, D))).cuda().repeat(N // (HKV * SEQ), 1)
+    cs = tq.CodeSet(kctx, N, tq.TQ_LAYOUT_TOKEN)
+    enc_ms, _ = _timed(lambda: tq.tq_encode(kctx, X, cs), 10, 3, stream, clocks_cls, local)
+    enc_mvec = 10 * N / (enc_ms * 1e-3) / 1e6
+    enc_bpv = D * 2 + vec_bytes
+    assert kctx.poll() == tq.TQ_OK
+    line = _line(args, world, "decode-attn HBM GB/s", round(value, 2), "GB/s", total_ms / args.steps,
+                 f"u{b}/u{b + 1} codes (b + 1/2 bits), f16 operands, f32 accumulate",
+                 "synthetic (seeded N(0,1) fp16 K/V with 4 outlier channels x10)",
+                 {"workload": f"decode attention at {b}.5 bits per coordinate (TurboQuant_mse, coordinates j mod 16 < 8 "
+                              f"at {b + 1} bits), 1 layer, batch 1, 32 q / 8 kv heads, head_dim 128, seq 16384; step = "
+                              f"append 1 token (tq_encode K and V) + attend, on each of {R} replica caches",
+                  "bits": b + 0.5, "replicas": R, "bytes_per_vector": vec_bytes, "bytes_per_step": step_bytes,
+                  "l2": f"inputs larger than L2: {R} distinct caches x {cache_bytes / 1e6:.1f} MB per step",
+                  "encode_mvec_s": round(enc_mvec, 1),
+                  "encode_roofline": {"bound": "hbm", "achieved": round(enc_mvec * 1e6 * enc_bpv / 1e9, 1),
+                                      "peak": hbm, "unit": "GB/s",
+                                      "frac": round(enc_mvec * 1e6 * enc_bpv / 1e9 / hbm, 4),
+                                      "kernel": "encode128_kernel", "bytes_per_vector": enc_bpv,
+                                      "rows": f"{N} fp16 rows"}},
+                 {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                  "traffic": traffic(root, f"decode_mixed_b{b}"), "kernel": "decode_step_kernel (b + 1/2 bits)",
+                  "peak_kind": kind, "us_per_call": round(attn_us, 3), "bytes_per_call": attn_bytes},
+                 e2e, args.steps * R * 3, clk)
+    if rank == 0 and not args.no_cpu_baseline and "mixed" in cpu:
+        line["cpu_baseline"] = cpu["mixed"](tq, reps[0], b, cap, q)
     return line if rank == 0 else None

@@ -677,23 +677,25 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
 #pragma unroll
             for (int w = 0; w < BM; ++w) blk[(even ? 0 : BM) + w] = ow[w];
           } else if (valid) {
-            // the partner is written by another call (or not at all): update this
-            // vector's slot of the chunk's 2·BM block words with masked atomics
-            const int slot = (int)(dv & 1);
-#pragma unroll 1
+            // the partner is written by another call (or not at all): this
+            // vector's fields of the chunk's 2·BM block words by masked atomics
+            // (both slots built at compile-time positions, then picked)
+            const bool odd = (dv & 1) != 0;
+            uint32_t f0[2 * BM], f1[2 * BM], m0[2 * BM], m1[2 * BM];
+#pragma unroll
+            for (int w = 0; w < 2 * BM; ++w) f0[w] = f1[w] = m0[w] = m1[w] = 0u;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const uint32_t code = get_bits<BM>(cw[cc], jj * BM);
+              put_bits<BM>(f0, 2 * jj * BM, code);
+              put_bits<BM>(f1, (2 * jj + 1) * BM, code);
+              put_bits<BM>(m0, 2 * jj * BM, (1u << BM) - 1u);
+              put_bits<BM>(m1, (2 * jj + 1) * BM, (1u << BM) - 1u);
+            }
+#pragma unroll
             for (int w = 0; w < 2 * BM; ++w) {
-              uint32_t m = 0u, bits = 0u;
-#pragma unroll 1
-              for (int bt = 0; bt < 32; ++bt) {
-                const int pos = 32 * w + bt;  // bit of the chunk's block stream
-                const int j = pos / (2 * BM), k = pos % (2 * BM);
-                if (k / BM == slot) {
-                  m |= 1u << bt;
-                  bits |= ((code_at<BM>(cw[cc], j) >> (k % BM)) & 1u) << bt;
-                }
-              }
-              atomicAnd(blk + w, ~m);
-              atomicOr(blk + w, bits);
+              atomicAnd(blk + w, ~(odd ? m1[w] : m0[w]));
+              atomicOr(blk + w, odd ? f1[w] : f0[w]);
             }
           }
         }
@@ -735,26 +737,26 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
           } else if (valid) {
             // the partner is written by another call (or not at all): this
             // vector's fields of the half's 2·HW block words by masked atomics
-            const int slot = (int)(dv & 1);
-#pragma unroll 1
+            // (word by word: only the fields overlapping word w, a compile-time
+            // test once both loops are unrolled; the slot picks the shift)
+            const bool odd = (dv & 1) != 0;
+            auto shift = [](uint32_t x, int sh) -> uint32_t {
+              return sh >= 32 || sh <= -32 ? 0u : (sh >= 0 ? x << sh : x >> (-sh));
+            };
+#pragma unroll
             for (int w = 0; w < 2 * HW; ++w) {
-              uint32_t m = 0u, bits = 0u;
-#pragma unroll 1
+              uint32_t fb = 0u, mb = 0u;
+#pragma unroll
               for (int k = 0; k < 64; ++k) {
-                const int wk = (k & 8) ? BM : BM + 1;
-                const int pos = 2 * mixed_pos(k, BM) + slot * wk - 32 * w;  // relative to word w
-                if (pos >= 32 || pos + wk <= 0) continue;
-                const uint32_t code = get_bits_rt(hw, mixed_pos(k, BM), wk), fm = (1u << wk) - 1u;
-                if (pos >= 0) {
-                  m |= fm << pos;
-                  bits |= code << pos;
-                } else {
-                  m |= fm >> (-pos);
-                  bits |= code >> (-pos);
-                }
+                const int wk = (k & 8) ? BM : BM + 1, pk = mixed_pos(k, BM);
+                const int p0 = 2 * pk - 32 * w;  // the pair field of coordinate k, relative to word w
+                if (p0 >= 32 || p0 + 2 * wk <= 0) continue;
+                const int sh = odd ? p0 + wk : p0;
+                fb |= shift(get_bits_rt(hw, pk, wk), sh);
+                mb |= shift((1u << wk) - 1u, sh);
               }
-              atomicAnd(blk + w, ~m);
-              atomicOr(blk + w, bits);
+              atomicAnd(blk + w, ~mb);
+              atomicOr(blk + w, fb);
             }
           }
         }
