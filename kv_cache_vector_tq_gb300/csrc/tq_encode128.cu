@@ -109,7 +109,6 @@ struct Enc128Params {
   float thr[15];
   float cen[16];
   float thr_hi[15];  // b + 1/2 bits: the (BM+1)-bit codebook's thresholds
-  int sym;  // thresholds symmetric about 0 (thr[H] = 0, thr[H-1-j] = -thr[H+1+j], H = 2^(BM-1) - 1)
   int layout, W, QW, pair_aligned;
   int64_t offset, group_rows, group_stride;
   int* status;
@@ -255,6 +254,38 @@ __device__ __forceinline__ void set_code(uint32_t (&wd)[BM], int col, uint32_t c
     if (sh >= 0 && sh < 32) wd[w] = (wd[w] & ~(m << sh)) | (code << sh);
     if (sh < 0 && sh > -BM) wd[w] = (wd[w] & ~(m >> (-sh))) | (code >> (-sh));
   }
+}
+
+// A flagged coordinate redone exactly, by the whole warp: v = √d·⟨x_row, Π_col⟩/s
+// as a float-float dot product (products split by an FMA, two-sum
+// reduction).  Rare, so kept out of line: its temporaries then do not compete
+// for the epilogue's registers.
+template <bool F16>
+__device__ __noinline__ float exact_coord(const void* x, const float* pi, double sqrt_d, int64_t row, int col,
+                                          float s, int lane) {
+  float4 xv;
+  if constexpr (F16) {
+    const uint2 h = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(x) + row * kDim) + lane);
+    const float2 x0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+    const float2 x1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+    xv = make_float4(x0.x, x0.y, x1.x, x1.y);
+  } else {
+    xv = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x) + row * kDim) + lane);
+  }
+  const float4 pv = __ldg(reinterpret_cast<const float4*>(pi + (int64_t)col * kDim) + lane);
+  float sh = 0.f, sl = 0.f;
+  ff_fma(xv.x, pv.x, sh, sl);
+  ff_fma(xv.y, pv.y, sh, sl);
+  ff_fma(xv.z, pv.z, sh, sl);
+  ff_fma(xv.w, pv.w, sh, sl);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float oh = __shfl_xor_sync(kFull, sh, o), ol = __shfl_xor_sync(kFull, sl, o);
+    const float s2 = sh + oh, bb = s2 - sh;
+    sl = sl + ol + ((sh - (s2 - bb)) + (oh - bb));
+    sh = s2;
+  }
+  return (float)(((double)sh + (double)sl) * (sqrt_d / (double)s));
 }
 
 // The three-pass product of a tensor-memory A operand (hi at a0, lo at a0 + 64
@@ -554,36 +585,37 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
       // a3/a4 per 32-coordinate chunk: bucketize, flag, pack into BM words
       // (chunk c of a row is words [c·BM, c·BM + BM) of its stream), recompute
       // flagged coordinates, store
-      uint32_t cw[2][BM];
+      // Plain MSE runs both chunks through one rolled loop (the second chunk's
+      // accumulator copied into a0), which keeps one copy of the bucketize code
+      // in the instruction cache; Prod needs both chunks' codes afterwards and
+      // b + 1/2 bits packs at chunk-dependent positions, so they unroll.
+      constexpr bool kRoll = !PROD && !MIX;
+      uint32_t cw[kRoll ? 1 : 2][BM];
       uint32_t hw[MIX ? 2 * BM + 1 : 1];  // b + 1/2 bits: the half's codes (mix_pos)
 #pragma unroll
       for (int w = 0; w < (MIX ? 2 * BM + 1 : 1); ++w) hw[w] = 0u;
       float g2 = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      // the accumulator is in registers: hand it back to the MMA
+      auto release_acc = [&]() {
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      };
+      auto do_chunk = [&](const int cc, const uint32_t(&av)[32], uint32_t(&cwc)[BM]) {
         const int c = 2 * half + cc;
-        if (cc == 1) {
-          tmem_wait_ld();
-          // the accumulator is in registers now: hand it back to the MMA
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[ab]);
-        }
         uint32_t m32;
         if constexpr (MIX) {
           if (cc == 0)
-            m32 = p.sym ? mix_chunk_codes<BM, true, 0>(a0, f, p.thr, p.thr_hi, hw)
-                        : mix_chunk_codes<BM, false, 0>(a0, f, p.thr, p.thr_hi, hw);
+            m32 = mix_chunk_codes<BM, true, 0>(a0, f, p.thr, p.thr_hi, hw);
           else
-            m32 = p.sym ? mix_chunk_codes<BM, true, 1>(a1, f, p.thr, p.thr_hi, hw)
-                        : mix_chunk_codes<BM, false, 1>(a1, f, p.thr, p.thr_hi, hw);
+            m32 = mix_chunk_codes<BM, true, 1>(a1, f, p.thr, p.thr_hi, hw);
         } else {
-          m32 = p.sym ? chunk_codes<BM, true, PROD>(cc ? a1 : a0, f, p.thr, cen_s, cw[cc], g2)
-                      : chunk_codes<BM, false, PROD>(cc ? a1 : a0, f, p.thr, cen_s, cw[cc], g2);
+          m32 = chunk_codes<BM, true, PROD>(av, f, p.thr, cen_s, cwc, g2);
         }
         if (!live) {
 #pragma unroll
-          for (int w = 0; w < BM; ++w) cw[cc][w] = 0u;
+          for (int w = 0; w < BM; ++w) cwc[w] = 0u;
 #pragma unroll
           for (int w = 0; w < (MIX ? 2 * BM + 1 : 1); ++w) hw[w] = 0u;
           m32 = 0u;
@@ -600,33 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
             m32 &= m32 - 1u;
           }
           j = __shfl_sync(kFull, j, src);
-          const int col = 32 * c + j;
           const float ssrc = __shfl_sync(kFull, s, src);
-          const int64_t srow = t * kRows + 32 * q + src;
-          float4 xv;
-          if constexpr (F16) {
-            const uint2 h = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(p.x) + srow * kDim) + lane);
-            const float2 x0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
-            const float2 x1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
-            xv = make_float4(x0.x, x0.y, x1.x, x1.y);
-          } else {
-            xv = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + srow * kDim) + lane);
-          }
-          const float4 pv = __ldg(reinterpret_cast<const float4*>(p.pi + (int64_t)col * kDim) + lane);
-          float sh = 0.f, sl = 0.f;
-          ff_fma(xv.x, pv.x, sh, sl);
-          ff_fma(xv.y, pv.y, sh, sl);
-          ff_fma(xv.z, pv.z, sh, sl);
-          ff_fma(xv.w, pv.w, sh, sl);
-#pragma unroll
-          for (int o = 16; o; o >>= 1) {
-            const float oh = __shfl_xor_sync(kFull, sh, o), ol = __shfl_xor_sync(kFull, sl, o);
-            const float s2 = sh + oh, bb = s2 - sh;
-            sl = sl + ol + ((sh - (s2 - bb)) + (oh - bb));
-            sh = s2;
-          }
+          const float vv = exact_coord<F16>(p.x, p.pi, p.sqrt_d, t * kRows + 32 * q + src, 32 * c + j, ssrc, lane);
           if (lane == src) {
-            const float vv = (float)(((double)sh + (double)sl) * (p.sqrt_d / (double)ssrc));
             bool nr;
             if constexpr (MIX) {
               const bool hi = (j & 8) == 0;
@@ -635,11 +643,11 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
             } else {
               const uint32_t code = bucketize<BM>(vv, thr_s, 0.f, nr);
               if constexpr (PROD) {
-                const uint32_t old = code_at<BM>(cw[cc], j);
+                const uint32_t old = code_at<BM>(cwc, j);
                 const float e0 = vv - cen_s[old], e1 = vv - cen_s[code];
                 g2 += e1 * e1 - e0 * e0;
               }
-              set_code<BM>(cw[cc], j, code);
+              set_code<BM>(cwc, j, code);
             }
           }
         }
@@ -649,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
           if (valid) {
             uint32_t* dst = p.codes + dv * p.W + c * BM;
 #pragma unroll
-            for (int w = 0; w < BM; ++w) dst[w] = cw[cc][w];
+            for (int w = 0; w < BM; ++w) dst[w] = cwc[w];
           }
         } else {
           // PAIR: vectors 2k and 2k+1 share a block; coordinate j's two codes
@@ -659,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
           // the odd lane those of 32c+16..32c+31, after one exchange.
           uint32_t part[BM];
 #pragma unroll
-          for (int w = 0; w < BM; ++w) part[w] = __shfl_xor_sync(kFull, cw[cc][w], 1);
+          for (int w = 0; w < BM; ++w) part[w] = __shfl_xor_sync(kFull, cwc[w], 1);
           const int64_t base_row = row - (even ? 0 : 1);
           const bool whole = p.pair_aligned && base_row + 1 < p.N;
           uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)p.W) + 2 * c * BM;
@@ -669,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
             for (int w = 0; w < BM; ++w) ow[w] = 0u;
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
-              const uint32_t own = even ? get_bits<BM>(cw[cc], jj * BM) : get_bits<BM>(cw[cc], (16 + jj) * BM);
+              const uint32_t own = even ? get_bits<BM>(cwc, jj * BM) : get_bits<BM>(cwc, (16 + jj) * BM);
               const uint32_t prt = even ? get_bits<BM>(part, jj * BM) : get_bits<BM>(part, (16 + jj) * BM);
               put_bits<BM>(ow, 2 * jj * BM, even ? own : prt);
               put_bits<BM>(ow, (2 * jj + 1) * BM, even ? prt : own);
@@ -686,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
             for (int w = 0; w < 2 * BM; ++w) f0[w] = f1[w] = m0[w] = m1[w] = 0u;
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
-              const uint32_t code = get_bits<BM>(cw[cc], jj * BM);
+              const uint32_t code = get_bits<BM>(cwc, jj * BM);
               put_bits<BM>(f0, 2 * jj * BM, code);
               put_bits<BM>(f1, (2 * jj + 1) * BM, code);
               put_bits<BM>(m0, 2 * jj * BM, (1u << BM) - 1u);
@@ -699,6 +707,21 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
             }
           }
         }
+            };
+      if constexpr (kRoll) {
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          if (cc == 1) {
+            release_acc();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a0[j] = a1[j];
+          }
+          do_chunk(cc, a0, cw[0]);
+        }
+      } else {
+        do_chunk(0, a0, cw[0]);
+        release_acc();
+        do_chunk(1, a1, cw[kRoll ? 0 : 1]);
       }
       if constexpr (MIX) {
         // the half's 2·BM + 1 words: coordinates 64·half .. 64·half + 63
@@ -868,8 +891,10 @@ cudaError_t launch_mode(const Enc128Params& p, const CUtensorMap& xmap, int bm, 
 }  // namespace
 
 bool enc128_supported(const DevCtx& c) {
+  // symmetric codebooks only (tq_codebook_build makes them): the bucketize
+  // compares |v| with the positive thresholds
   return c.d == kDim && c.enc_tab != nullptr && (c.mode != TQ_PROD || c.enc_tab_m != nullptr) &&
-         c.b_mse >= 1 && c.b_mse <= (c.mode == TQ_MSE ? 4 : 3);
+         c.b_mse >= 1 && c.b_mse <= (c.mode == TQ_MSE ? 4 : 3) && c.sym_thr != 0;
 }
 
 tq_status launch_encode128(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,
@@ -893,15 +918,6 @@ tq_status launch_encode128(const DevCtx& c, const void* x, int x_dtype, int64_t 
   for (int k = 0; k < 16; ++k) p.cen[k] = c.cen[k];
   for (int k = 0; k < 15; ++k) p.thr_hi[k] = c.thr_hi[k];
   const bool mix = c.mode == TQ_MIXED;
-  {
-    auto symmetric = [](const float* thr, int bits) {
-      const int nt = (1 << bits) - 1, h = nt / 2;
-      bool sym = thr[h] == 0.f;
-      for (int j = 0; sym && j < h; ++j) sym = thr[h - 1 - j] == -thr[h + 1 + j];
-      return sym;
-    };
-    p.sym = symmetric(c.thr, c.b_mse) && (!mix || symmetric(c.thr_hi, c.b_mse + 1)) ? 1 : 0;
-  }
   p.layout = out->layout;
   p.W = c.words_per_vec;
   p.QW = c.qjl_words_per_vec;

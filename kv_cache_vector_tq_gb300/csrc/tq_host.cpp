@@ -499,6 +499,20 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   const int KH = mixed ? 2 * K : 0;  // TQ_MIXED: the (b+1)-bit codebook
   for (int k = 0; k < KH; ++k) v.cen_hi[k] = (float)cb[1].centroid[k];
   for (int k = 0; k + 1 < KH; ++k) v.thr_hi[k] = (float)cb[1].threshold[k];
+  {
+    auto symmetric = [](const float* thr, int n) {  // n thresholds, n odd
+      const int h = n / 2;
+      bool sym = thr[h] == 0.f;
+      for (int j = 0; sym && j < h; ++j) sym = thr[h - 1 - j] == -thr[h + 1 + j];
+      return sym;
+    };
+    v.sym_thr = symmetric(v.thr, K - 1) && (!mixed || symmetric(v.thr_hi, KH - 1)) ? 1 : 0;
+  }
+  if (mixed && !v.sym_thr) {  // only the tensor-memory encoder packs b + 1/2 bits
+    delete[] c->h_pi;
+    delete c;
+    return TQ_ERR_UNSUPPORTED;
+  }
 
   // alpha: scale that makes alpha·c_k closest to fp16 values (max relative
   // error); one alpha for both codebooks of TQ_MIXED, whose tables share the

@@ -37,6 +37,7 @@ struct DevCtx {
   float thr[15];         // thresholds, unit-variance units (fp32)
   float cen[16];         // centroids, unit-variance units (fp32)
   float thr_hi[15];      // TQ_MIXED: the (b+1)-bit codebook's thresholds
+  int sym_thr;           // thresholds (both sets for TQ_MIXED) symmetric about 0 in fp32
   float cen_hi[16];      // TQ_MIXED: the (b+1)-bit codebook's centroids
   const uint2* enc_pi;   // encoder B fragments of Π (hi/lo)
   const uint2* enc_m;    // encoder B fragments of S·Πᵀ (hi/lo), Prod only
