@@ -19,7 +19,8 @@ LIB = os.path.join(PKG, "libtq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["tq_host.cpp", "tq_encode.cu", "tq_encode_wht.cu", "tq_encode_umma.cu", "tq_encode128.cu", "tq_scores.cu",
-           "tq_decode.cu", "tq_decode_k12.cu", "tq_decode_k34.cu", "tq_decode_prod.cu", "tq_decode_mixed.cu"]
+           "tq_decode.cu", "tq_decode_k1.cu", "tq_decode_k2.cu", "tq_decode_k3.cu", "tq_decode_k4.cu",
+           "tq_decode_prod.cu", "tq_decode_mixed.cu"]
 
 
 def _nvcc():

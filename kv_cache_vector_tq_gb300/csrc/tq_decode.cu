@@ -82,10 +82,14 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
     e = decode_run_mixed(p, kc.b_mse, G, groups, stream);
   else if (prod)
     e = decode_run_prod(p, kc.b_mse, vc.b_mse, G, groups, stream);
-  else if (kc.b_mse == 1 || kc.b_mse == 2)
-    e = decode_run_k12(p, kc.b_mse, vc.b_mse, G, groups, stream);
-  else if (kc.b_mse == 3 || kc.b_mse == 4)
-    e = decode_run_k34(p, kc.b_mse, vc.b_mse, G, groups, stream);
+  else if (kc.b_mse == 1)
+    e = decode_run_k1(p, vc.b_mse, G, groups, stream);
+  else if (kc.b_mse == 2)
+    e = decode_run_k2(p, vc.b_mse, G, groups, stream);
+  else if (kc.b_mse == 3)
+    e = decode_run_k3(p, vc.b_mse, G, groups, stream);
+  else if (kc.b_mse == 4)
+    e = decode_run_k4(p, vc.b_mse, G, groups, stream);
   else
     return TQ_ERR_UNSUPPORTED;
   return e == cudaSuccess ? TQ_OK : set_cuda_error(e);

@@ -1,0 +1,11 @@
+// Decode kernels instantiated for key codes of 4 bits (every value width and
+// GQA; one translation unit per key width so that they compile in parallel).
+#include "tq_decode_kernel.cuh"
+
+namespace tq {
+
+cudaError_t decode_run_k4(const StepParams& p, int bv, int G, int groups, cudaStream_t st) {
+  return run_step_v<4>(p, bv, G, groups, st);
+}
+
+}  // namespace tq

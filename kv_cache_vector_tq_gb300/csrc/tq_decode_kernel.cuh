@@ -239,7 +239,7 @@ __host__ __device__ inline StepSmem step_smem(int bk, int bv, int G, int W, bool
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int BK, int BV, int G, int W, bool Q, bool MX = false>
+template <int BK, int BV, int G, int W, bool Q, bool MX = false, bool SH = false>
 __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams p) {
   constexpr int NT = (2 * G + 7) / 8;
   constexpr int WK = 4 * BK, WV = 4 * BV;  // words per vector
@@ -292,6 +292,12 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
   const int t_begin = split_begin(split, p.S, p.tiles, append);
   const int t_end = split_begin(split + 1, p.S, p.tiles, append);
   const int ntl = t_end - t_begin;
+  // SH (short loops: at most 8 tiles per warp, as in one decode layer of 16K
+  // tokens): one tile in flight ahead of the one in use, so the first tiles
+  // arrive sooner (12.56 against 12.80 us per call at b = 4).  Otherwise
+  // kStages tiles in flight (a 128K-token layer: 66.7 against 67.7 us).  A
+  // template choice: one loop holding both orders scheduled worse than either.
+  constexpr bool shallow = SH;
   const int64_t gbase = (int64_t)grp * p.cap;  // vector index of token 0 of the group
   const int new_tile = (int)((p.seq - 1) / kTileTok), new_row = (int)((p.seq - 1) % kTileTok);
   const bool owner = append && new_tile >= t_begin && new_tile < t_end;
@@ -624,8 +630,10 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
       qf[s][nt] = qfs[(s * NT + nt) * 32 + lane];
       if constexpr (Q) qsf[s][nt] = reinterpret_cast<const uint2*>(cpart)[(s * NT + nt) * 32 + lane];
     }
+  if constexpr (!shallow) {
 #pragma unroll
-  for (int j = 1; j < kStages; ++j) issue(j);
+    for (int j = 1; j < kStages; ++j) issue(j);
+  }
 
   // ---- 3. stream the tiles
   const uint32_t* mykl = klut + lane;
@@ -654,7 +662,12 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
   const bool pv_in_loop = warp < ntl;
   for (int j = 0; warp + j * W < ntl; ++j) {
     const int tile = t_begin + warp + j * W;
-    cp_async_wait<kStages - 1>();
+    if constexpr (shallow) {  // the next tile into another stage, then this one complete
+      issue(j + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<kStages - 1>();
+    }
     const unsigned char* st = my_stage + (j % kStages) * SB;
     constexpr int KN = MX ? BK + 1 : BK, VN = MX ? BV + 1 : BV;
     uint32_t k0[KN], k1[KN], v0w[VN], v1w[VN];
@@ -716,7 +729,7 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
       }
     }
     // every lane's words are in registers: refill this stage
-    issue(j + kStages);
+    if constexpr (!shallow) issue(j + kStages);
     if (warp + (j + 1) * W >= ntl) issue_pv();  // the warp's last tile: its region is free now
     const int lt0 = tile * kTileTok;
     // K side: S = K̂·Q with two independent MMA chains
@@ -1055,13 +1068,20 @@ static int choose_splits(int tiles, int groups, int W, bool append, int merge_ca
 template <int BK, int BV, int G, bool Q = false, bool MX = false>
 static cudaError_t run_step(const StepParams& p, int groups, cudaStream_t st) {
   constexpr int W = G >= 8 ? 8 : 16;
+  // the short-loop variant for plain MSE caches with up to 4 query heads per KV head
+  constexpr bool kHasShort = !Q && !MX && G <= 4;
   auto kern = decode_step_kernel<BK, BV, G, W, Q, MX>;
-  static PerDeviceValue smem_attr;  // set once per device, before any stream capture
-  const cudaError_t e = smem_attr_once(smem_attr, (const void*)kern, 227 * 1024);
+  auto kern_short = decode_step_kernel<BK, BV, G, W, Q, MX, kHasShort>;
+  static PerDeviceValue smem_attr, smem_attr_short;  // set once per device, before any stream capture
+  cudaError_t e = smem_attr_once(smem_attr, (const void*)kern, 227 * 1024);
+  if (e == cudaSuccess && kHasShort) e = smem_attr_once(smem_attr_short, (const void*)kern_short, 227 * 1024);
   if (e != cudaSuccess) return e;
   const StepSmem L = step_smem(BK, BV, G, W, p.same_lut != 0, Q, MX);
   StepParams pp = p;
   pp.S = choose_splits(p.tiles, groups, W, p.append != 0, L.mw / (G * kPart * 4));
+  // largest share of a CTA in tiles (the owner's is smaller), per warp
+  const int per_warp = ((p.tiles + pp.S - 1) / pp.S + W - 1) / W;
+  if (kHasShort && per_warp <= 8) kern = kern_short;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(groups * pp.S);
   cfg.blockDim = dim3(W * 32);
@@ -1099,8 +1119,10 @@ static cudaError_t run_step_v(const StepParams& p, int bv, int G, int groups, cu
 
 // Launchers of the instantiated kernels, one translation unit per group of
 // key bit widths (they compile in parallel).
-cudaError_t decode_run_k12(const StepParams& p, int bk, int bv, int G, int groups, cudaStream_t st);
-cudaError_t decode_run_k34(const StepParams& p, int bk, int bv, int G, int groups, cudaStream_t st);
+cudaError_t decode_run_k1(const StepParams& p, int bv, int G, int groups, cudaStream_t st);
+cudaError_t decode_run_k2(const StepParams& p, int bv, int G, int groups, cudaStream_t st);
+cudaError_t decode_run_k3(const StepParams& p, int bv, int G, int groups, cudaStream_t st);
+cudaError_t decode_run_k4(const StepParams& p, int bv, int G, int groups, cudaStream_t st);
 // Prod keys ((b−1)-bit codes bk in 1..3), G in {1, 2, 4}
 cudaError_t decode_run_prod(const StepParams& p, int bk, int bv, int G, int groups, cudaStream_t st);
 // K and V at b + 1/2 bits per coordinate (b in 1..3), G in {1, 2, 4, 8}
