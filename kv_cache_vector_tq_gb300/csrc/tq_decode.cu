@@ -73,7 +73,21 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
   p.new_f16 = new_dtype == TQ_F16;
   p.append = knew != nullptr;
   p.out = out;
-  const int groups = B * Hkv;
+  int groups = B * Hkv;
+  p.kv_shift = 0;
+  // 8 query heads per KV head over short caches: as 4-head groups over two
+  // virtual KV heads per cache head (the 8-head kernel needs ~230 registers and
+  // so runs 8 warps per SM; the 4-head one runs 16).  Both halves read the same
+  // cache bytes, the second mostly from L2 while the cache is short: 64 q / 8
+  // kv heads at b = 3, 4096 tokens 12.6 -> 9.8 us, but 16384 tokens 18.5 ->
+  // 20.5 us and 131072 tokens 65.7 -> 100 us (the second reads miss L2).
+  int Gk = G;
+  if (G == 8 && !prod && !mixed && 2 * groups <= num_sms() && seq <= 4096) {
+    Gk = 4;
+    groups *= 2;
+    p.Hkv = 2 * Hkv;
+    p.kv_shift = 1;
+  }
   p.S = 1;
   p.counters = static_cast<int*>(ws);
   p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + ws_counter_bytes(groups));
@@ -83,13 +97,13 @@ tq_status launch_step(const DevCtx& kc, const DevCtx& vc, const void* q, int q_d
   else if (prod)
     e = decode_run_prod(p, kc.b_mse, vc.b_mse, G, groups, stream);
   else if (kc.b_mse == 1)
-    e = decode_run_k1(p, vc.b_mse, G, groups, stream);
+    e = decode_run_k1(p, vc.b_mse, Gk, groups, stream);
   else if (kc.b_mse == 2)
-    e = decode_run_k2(p, vc.b_mse, G, groups, stream);
+    e = decode_run_k2(p, vc.b_mse, Gk, groups, stream);
   else if (kc.b_mse == 3)
-    e = decode_run_k3(p, vc.b_mse, G, groups, stream);
+    e = decode_run_k3(p, vc.b_mse, Gk, groups, stream);
   else if (kc.b_mse == 4)
-    e = decode_run_k4(p, vc.b_mse, G, groups, stream);
+    e = decode_run_k4(p, vc.b_mse, Gk, groups, stream);
   else
     return TQ_ERR_UNSUPPORTED;
   return e == cudaSuccess ? TQ_OK : set_cuda_error(e);

@@ -163,6 +163,7 @@ struct StepParams {
   int append;
   float kthr[15];
   float vthr[15];
+  int kv_shift;  // 1: Hkv counts virtual KV heads, two per cache head (vh >> 1)
 };
 
 // First tile of CTA u of the U CTAs that share a (batch, KV head).  With an
@@ -298,7 +299,9 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
   // kStages tiles in flight (a 128K-token layer: 66.7 against 67.7 us).  A
   // template choice: one loop holding both orders scheduled worse than either.
   constexpr bool shallow = SH;
-  const int64_t gbase = (int64_t)grp * p.cap;  // vector index of token 0 of the group
+  // vector index of token 0 of the group's cache head (virtual heads share one)
+  const int cgrp = b * (p.Hkv >> p.kv_shift) + (kvh >> p.kv_shift);
+  const int64_t gbase = (int64_t)cgrp * p.cap;
   const int new_tile = (int)((p.seq - 1) / kTileTok), new_row = (int)((p.seq - 1) % kTileTok);
   const bool owner = append && new_tile >= t_begin && new_tile < t_end;
   unsigned char* my_stage = stage + warp * L.wreg;
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
   float nv = 0.f;  // owner: element tid of [k_new; v_new]
   if (owner && tid < 256) {
     const void* src = tid >= 128 ? p.vnew : p.knew;
-    const int64_t off = (int64_t)grp * 128 + (tid & 127);
+    const int64_t off = (int64_t)cgrp * 128 + (tid & 127);
     nv = p.new_f16 ? __half2float(static_cast<const __half*>(src)[off]) : static_cast<const float*>(src)[off];
   }
   auto issue = [&](int j) {  // warp-local tile j -> stage j % kStages, one 16-byte slot per lane
