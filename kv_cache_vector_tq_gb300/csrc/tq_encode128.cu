@@ -159,25 +159,78 @@ __device__ __forceinline__ uint32_t bucketize_c(float v, const float (&thr)[15],
   }
 }
 
+// Symmetric bucketize without a per-coordinate near test: code of v from the
+// sign bits of |v| - t over the positive thresholds (a sign bit counts a
+// threshold above |v|, one shift-add each), and every |v - t| (and |v|, for
+// the threshold at 0) folded into dmin, a running minimum over the chunk.
+template <int BM>
+__device__ __forceinline__ uint32_t bucketize_fold(float v, const float (&thr)[15], float& dmin) {
+  constexpr int H = (1 << (BM - 1)) - 1;
+  constexpr uint32_t kAll = (1u << BM) - 1u;  // 2H + 1
+  const float a = fabsf(v);
+  dmin = fminf(dmin, a);
+  uint32_t above = 0u;  // thresholds t > |v|
+#pragma unroll
+  for (int j = 0; j < H; ++j) {
+    const float dj = a - thr[H + 1 + j];
+    dmin = fminf(dmin, fabsf(dj));
+    above += __float_as_uint(dj) >> 31;
+  }
+  // v >= 0: H + 1 + (H - above) = kAll - above; v < 0: H - (H - above) = above
+  // = (kAll - above) ^ kAll
+  return (kAll - above) ^ ((uint32_t)((int32_t)__float_as_uint(v) >> 31) & kAll);
+}
+
+// Near-threshold flags of a chunk (symmetric codebook), bit j for coordinate j.
+template <int BM>
+__device__ __forceinline__ uint32_t near_mask(const uint32_t (&a)[32], float f, const float (&thr)[15]) {
+  uint32_t m32 = 0u;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    bool near;
+    bucketize_c<BM, true>(__uint_as_float(a[j]) * f, thr, kMargin, near);
+    m32 |= (near ? 1u : 0u) << j;
+  }
+  return m32;
+}
+
 // One 32-column chunk of a row's accumulator: its BM code words (coordinate j
 // of the chunk at bits j·BM), the near-threshold flags, and (Prod) the sum of
-// squared residuals in v units.
+// squared residuals in v units.  Symmetric codebooks test the whole chunk for
+// a coordinate near a threshold at once (`flagged`) and leave the flags to
+// the caller, which finds them in the rare chunks that have one.
 template <int BM, bool SYM, bool PROD>
 __device__ __forceinline__ uint32_t chunk_codes(const uint32_t (&a)[32], float f, const float (&thr)[15],
-                                                const float* cen_s, uint32_t (&cw)[BM], float& g2) {
+                                                const float* cen_s, uint32_t (&cw)[BM], float& g2,
+                                                bool& flagged) {
   uint32_t m32 = 0u;
 #pragma unroll
   for (int w = 0; w < BM; ++w) cw[w] = 0u;
+  if constexpr (SYM) {
+    float dmin = INFINITY;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float v = __uint_as_float(a[j]) * f;
-    bool near;
-    const uint32_t code = bucketize_c<BM, SYM>(v, thr, kMargin, near);
-    m32 |= (near ? 1u : 0u) << j;
-    put_bits<BM>(cw, j * BM, code);
-    if constexpr (PROD) {
-      const float rr = v - cen_s[code];
-      g2 = fmaf(rr, rr, g2);
+    for (int j = 0; j < 32; ++j) {
+      const float v = __uint_as_float(a[j]) * f;
+      const uint32_t code = bucketize_fold<BM>(v, thr, dmin);
+      put_bits<BM>(cw, j * BM, code);
+      if constexpr (PROD) {
+        const float rr = v - cen_s[code];
+        g2 = fmaf(rr, rr, g2);
+      }
+    }
+    flagged = dmin < kMargin;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float v = __uint_as_float(a[j]) * f;
+      bool near;
+      const uint32_t code = bucketize_c<BM, false>(v, thr, kMargin, near);
+      m32 |= (near ? 1u : 0u) << j;
+      put_bits<BM>(cw, j * BM, code);
+      if constexpr (PROD) {
+        const float rr = v - cen_s[code];
+        g2 = fmaf(rr, rr, g2);
+      }
     }
   }
   return m32;
@@ -187,23 +240,38 @@ __device__ __forceinline__ uint32_t chunk_codes(const uint32_t (&a)[32], float f
 // bits where k mod 16 < 8 and BM bits elsewhere; its code starts at bit
 // mixed_pos(k, BM) of the half's 2·BM + 1 words (every 16 coordinates span
 // 8·(2·BM + 1) bits, so a half is whole words of the row's stream).
-// One 32-column chunk CC (0 or 1) of a half at b + 1/2 bits: codes into the
-// half's words hw (compile-time positions), near-threshold flags returned.
-template <int BM, bool SYM, int CC>
-__device__ __forceinline__ uint32_t mix_chunk_codes(const uint32_t (&a)[32], float f, const float (&tlo)[15],
-                                                    const float (&thi)[15], uint32_t (&hw)[2 * BM + 1]) {
+// One 32-column chunk CC (0 or 1) of a half at b + 1/2 bits (symmetric
+// codebooks): codes into the half's words hw at compile-time positions; a
+// coordinate near a threshold anywhere in the chunk sets `flagged`.
+template <int BM, int CC>
+__device__ __forceinline__ void mix_chunk_codes(const uint32_t (&a)[32], float f, const float (&tlo)[15],
+                                                const float (&thi)[15], uint32_t (&hw)[2 * BM + 1],
+                                                bool& flagged) {
+  float dmin = INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float v = __uint_as_float(a[j]) * f;
+    if ((j & 8) == 0)
+      put_bits<BM + 1>(hw, mixed_pos(32 * CC + j, BM), bucketize_fold<BM + 1>(v, thi, dmin));
+    else
+      put_bits<BM>(hw, mixed_pos(32 * CC + j, BM), bucketize_fold<BM>(v, tlo, dmin));
+  }
+  flagged = dmin < kMargin;
+}
+
+// Near-threshold flags of a b + 1/2-bit chunk, each coordinate against its own codebook.
+template <int BM>
+__device__ __forceinline__ uint32_t mix_near_mask(const uint32_t (&a)[32], float f, const float (&tlo)[15],
+                                                  const float (&thi)[15]) {
   uint32_t m32 = 0u;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const float v = __uint_as_float(a[j]) * f;
     bool near;
-    if ((j & 8) == 0) {
-      const uint32_t code = bucketize_c<BM + 1, SYM>(v, thi, kMargin, near);
-      put_bits<BM + 1>(hw, mixed_pos(32 * CC + j, BM), code);
-    } else {
-      const uint32_t code = bucketize_c<BM, SYM>(v, tlo, kMargin, near);
-      put_bits<BM>(hw, mixed_pos(32 * CC + j, BM), code);
-    }
+    if ((j & 8) == 0)
+      bucketize_c<BM + 1, true>(v, thi, kMargin, near);
+    else
+      bucketize_c<BM, true>(v, tlo, kMargin, near);
     m32 |= (near ? 1u : 0u) << j;
   }
   return m32;
@@ -596,9 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
 #pragma unroll
       for (int w = 0; w < (MIX ? 2 * BM + 1 : 1); ++w) hw[w] = 0u;
       float g2 = 0.f;
-      // the accumulator is in registers: hand it back to the MMA
+      // hand the accumulator back to the MMA
       auto release_acc = [&]() {
-        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[ab]);
@@ -607,17 +674,34 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
         const int c = 2 * half + cc;
         uint32_t m32;
         if constexpr (MIX) {
+          bool flagged = false;
           if (cc == 0)
-            m32 = mix_chunk_codes<BM, true, 0>(a0, f, p.thr, p.thr_hi, hw);
+            mix_chunk_codes<BM, 0>(a0, f, p.thr, p.thr_hi, hw, flagged);
           else
-            m32 = mix_chunk_codes<BM, true, 1>(a1, f, p.thr, p.thr_hi, hw);
+            mix_chunk_codes<BM, 1>(a1, f, p.thr, p.thr_hi, hw, flagged);
+          m32 = 0u;
+          if (__any_sync(kFull, flagged && live)) {  // rare: the flags, from tensor memory again
+            uint32_t t32[32];
+            tmem_ld32_nw(acc + 64 * half + 32 * cc, t32);
+            tmem_wait_ld();
+            if (flagged) m32 = mix_near_mask<BM>(t32, f, p.thr, p.thr_hi);
+          }
         } else {
           // Prod keys take general thresholds too (keeping that branch also
           // schedules the Prod epilogue better: 2.57 -> 2.95 Gvec/s measured)
+          bool flagged = false;
           if (PROD && !p.sym)
-            m32 = chunk_codes<BM, false, PROD>(av, f, p.thr, cen_s, cwc, g2);
+            m32 = chunk_codes<BM, false, PROD>(av, f, p.thr, cen_s, cwc, g2, flagged);
           else
-            m32 = chunk_codes<BM, true, PROD>(av, f, p.thr, cen_s, cwc, g2);
+            m32 = chunk_codes<BM, true, PROD>(av, f, p.thr, cen_s, cwc, g2, flagged);
+          // a chunk with a coordinate near a threshold (~1e-3 of them): its
+          // values again from tensor memory (not yet handed back), then the flags
+          if (__any_sync(kFull, flagged && live)) {
+            uint32_t t32[32];
+            tmem_ld32_nw(acc + 64 * half + 32 * cc, t32);
+            tmem_wait_ld();
+            if (flagged) m32 = near_mask<BM>(t32, f, p.thr);
+          }
         }
         if (!live) {
 #pragma unroll
@@ -714,11 +798,13 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
           }
         }
             };
+      // the accumulator goes back to the MMA after both chunks (a flagged chunk
+      // reads it again); the kernel is epilogue-bound, so the MMA loses nothing
       if constexpr (kRoll) {
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
           if (cc == 1) {
-            release_acc();
+            tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j) a0[j] = a1[j];
           }
@@ -726,9 +812,10 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
         }
       } else {
         do_chunk(0, a0, cw[0]);
-        release_acc();
+        tmem_wait_ld();
         do_chunk(1, a1, cw[kRoll ? 0 : 1]);
       }
+      release_acc();
       if constexpr (MIX) {
         // the half's 2·BM + 1 words: coordinates 64·half .. 64·half + 63
         constexpr int HW = 2 * BM + 1;
