@@ -373,6 +373,15 @@ def test_decode_gqa_variants(gqa):
     run_decode(3, 3, 1, 4 * gqa, 4, 777, q_dtype=torch.float32)
 
 
+@pytest.mark.parametrize("b_k,b_v,B,Hq,Hkv,seq", [(3, 3, 1, 32, 4, 6007), (4, 4, 1, 64, 8, 5000),
+                                                   (4, 2, 2, 16, 2, 9001)])
+def test_decode_gqa8_long(b_k, b_v, B, Hq, Hkv, seq):
+    """8 query heads per KV head over caches past 4096 tokens (the K/V warp
+    pairs: one warp scores and runs the softmax, its partner sums P·V), table
+    and byte-row lookups, asymmetric bits, ragged last tiles."""
+    run_decode(b_k, b_v, B, Hq, Hkv, seq)
+
+
 def test_decode_asymmetric_bits():
     run_decode(4, 2, 1, 16, 4, 2048)
 
@@ -558,6 +567,7 @@ def test_decode_config4_layer_subset():
 @pytest.mark.parametrize("b,B,Hq,Hkv,seq,rot", [(4, 1, 32, 8, 16384, "dense"), (2, 1, 32, 8, 16383, "dense"),
                                                  (3, 2, 16, 2, 1001, "dense"), (3, 1, 64, 8, 4096, "dense"),
                                                  (4, 1, 8, 8, 17, "dense"), (3, 1, 32, 8, 2047, "hadamard"),
+                                                 (3, 1, 64, 8, 6001, "dense"),
                                                  (4, 1, 32, 8, 16384, "hadamard")])
 def test_decode_step_appends_then_attends(b, B, Hq, Hkv, seq, rot):
     """The step encodes the new token's K and V into position seq-1 (same codes
