@@ -35,6 +35,7 @@ struct WhtParams {
   int W;
   const float* signs;  // σ, d entries of ±1
   float thr[15];
+  int sym;             // thresholds symmetric about 0
   int64_t offset, group_rows, group_stride;
 };
 
@@ -74,6 +75,26 @@ __device__ __forceinline__ void wcp16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void wcp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+// Code of v: #{k : v >= t_k}, branch-free with the thresholds in registers
+// (kernel parameters): the sign bit of each difference counts a threshold
+// above v.  Symmetric codebooks compare |v| with the positive half only.
+template <int BM>
+__device__ __forceinline__ int wht_code(float v, const float (&thr)[15], bool sym) {
+  constexpr int H = (1 << (BM - 1)) - 1;
+  constexpr uint32_t kAll = (1u << BM) - 1u;
+  uint32_t above = 0u;
+  if (sym) {
+    const float a = fabsf(v);
+#pragma unroll
+    for (int j = 0; j < H; ++j) above += __float_as_uint(a - thr[H + 1 + j]) >> 31;
+    // v >= 0 (-0 included, as the search it replaces): kAll - above; v < 0: above
+    return (int)(v >= 0.f ? kAll - above : above);
+  }
+#pragma unroll
+  for (int k = 0; k < 2 * H + 1; ++k) above += __float_as_uint(v - thr[k]) >> 31;
+  return (int)(kAll - above);
+}
+
 template <int N>
 __device__ __forceinline__ void wcp_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
@@ -261,9 +282,7 @@ __global__ void __launch_bounds__(P == 12 ? 384 : 256) encode_wht_kernel(const W
             acc = fmaf(2.f, pa + xb[aa], -z0);
           }
           const float v = acc * inv;  // v = z/s
-          int code = 0;
-#pragma unroll
-          for (int step = 1 << (BM - 1); step > 0; step >>= 1) code += v >= thr_s[code + step - 1] ? step : 0;
+          const int code = wht_code<BM>(v, p.thr, p.sym != 0);
           cbuf[aa * M + tid] = (unsigned char)(s > 0.f ? code : 0);
         }
       }
@@ -287,9 +306,7 @@ __global__ void __launch_bounds__(P == 12 ? 384 : 256) encode_wht_kernel(const W
 #pragma unroll
       for (int k = 0; k < E; ++k) {
         const float v = x[k] * inv;
-        int code = 0;
-#pragma unroll
-        for (int step = 1 << (BM - 1); step > 0; step >>= 1) code += v >= thr_s[code + step - 1] ? step : 0;
+        const int code = wht_code<BM>(v, p.thr, p.sym != 0);
         cw[32 * k + lane] = (unsigned char)(s > 0.f ? code : 0);
       }
       __syncwarp();
@@ -359,6 +376,7 @@ tq_status launch_encode_wht(const DevCtx& c, const void* x, int x_dtype, int64_t
   p.W = c.words_per_vec;
   p.signs = c.signs;
   for (int k = 0; k < 15; ++k) p.thr[k] = c.thr[k];
+  p.sym = c.sym_thr;
   p.offset = offset;
   p.group_rows = group_rows;
   p.group_stride = group_stride;
