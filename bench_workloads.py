@@ -466,7 +466,7 @@ def run_keys(args, world, rank, local, root, clocks_cls, cpu):
                   "keys": N, "l2": "L2 flushed (256 MB write) before every timed call",
                   "us_per_encode_plus_score": round(total_ms / args.steps * 1e3, 2)},
                  {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
-                  "traffic": None, "kernel": "encode_kernel + scores_kernel (latency-bound at this size)",
+                  "traffic": None, "kernel": "encode128_kernel + scores_kernel (latency-bound at this size)",
                   "peak_kind": kind},
                  None, 2 * args.steps, clk)
     return line if rank == 0 else None
