@@ -64,6 +64,10 @@ constexpr int kDim = 128;                    // d = MMA N = K
 constexpr int kBox = kRows * 128;            // one 128-byte column box of the x tile: 16 KB
 constexpr int kTab = 4 * kUmmaPlaneBytes;    // B operand of one 128 x 128 matrix: (hi, lo) x 2 K chunks
 constexpr int kThreads = 14 * 32;
+// Plain MSE: 16 epilogue warps, one 32-column chunk each (22 warps in all);
+// Prod and b + 1/2 bits: 8, a column half each (they need both chunks of a half)
+__host__ __device__ constexpr int epi_warps(bool prod, bool mix) { return (!prod && !mix) ? 16 : 8; }
+__host__ __device__ constexpr int enc_threads(bool prod, bool mix) { return (6 + epi_warps(prod, mix)) * 32; }
 constexpr float kMargin = 8e-6f;             // recomputation band around each threshold (v units)
 
 template <bool F16, bool PROD>
@@ -373,7 +377,7 @@ __device__ __forceinline__ void mma3_ts(uint32_t acc, uint32_t a0, uint32_t btab
 }
 
 template <int BM, bool PROD, bool F16, bool MIX>
-__global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Params p,
+__global__ void __launch_bounds__(enc_threads(PROD, MIX), 1) encode128_kernel(const Enc128Params p,
                                                                  const __grid_constant__ CUtensorMap xmap) {
   using L = Lay<F16, PROD>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -418,9 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
       mbar_init(&a_full[s], 4);
       mbar_init(&a_empty[s], 1);
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 8);
+      mbar_init(&acc_empty[s], epi_warps(PROD, MIX));
       mbar_init(&nb_full[s], 4);
-      mbar_init(&nb_empty[s], 8);
+      mbar_init(&nb_empty[s], epi_warps(PROD, MIX));
       mbar_init(&g2_full[s], 8);
     }
     mbar_init(a2_full, 8);
@@ -624,9 +628,12 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
       }
     }
   } else {
-    // ---------------- epilogue: warps 6-13; warp w serves TMEM lanes 32·(w % 4)..+31
-    // (rows of the tile) and the column half (w - 6) / 4: chunks 2·half, 2·half + 1
-    const int q = warp & 3, r = 32 * q + lane, half = (warp - 6) >> 2;
+    // ---------------- epilogue: warps 6..; warp w serves TMEM lanes 32·(w % 4)..+31
+    // (rows of the tile); plain MSE: chunk (w - 6) / 4 of the four 32-column
+    // chunks; Prod and b + 1/2 bits: the column half (w - 6) / 4, chunks
+    // 2·half and 2·half + 1
+    constexpr int CPW = epi_warps(PROD, MIX) == 16 ? 1 : 2;  // chunks per warp
+    const int q = warp & 3, r = 32 * q + lane, half = (warp - 6) >> 2, c0 = half * CPW;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const bool even = (lane & 1) == 0;
     for (int i = 0; i < nloc; ++i) {
@@ -648,16 +655,15 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
       tc_fence_after();
       const uint32_t acc = tmem + lane_base + L::ColAcc + ab * 128;
       uint32_t a0[32], a1[32];
-      tmem_ld32_nw(acc + 64 * half, a0);
+      tmem_ld32_nw(acc + 32 * c0, a0);
       tmem_wait_ld();
-      tmem_ld32_nw(acc + 64 * half + 32, a1);  // waited for after the first chunk's codes
+      if constexpr (CPW == 2) tmem_ld32_nw(acc + 32 * (c0 + 1), a1);  // waited for after the first chunk's codes
       // a3/a4 per 32-coordinate chunk: bucketize, flag, pack into BM words
       // (chunk c of a row is words [c·BM, c·BM + BM) of its stream), recompute
       // flagged coordinates, store
-      // Plain MSE runs both chunks through one rolled loop (the second chunk's
-      // accumulator copied into a0), which keeps one copy of the bucketize code
-      // in the instruction cache; Prod needs both chunks' codes afterwards and
-      // b + 1/2 bits packs at chunk-dependent positions, so they unroll.
+      // Plain MSE: one chunk per warp (one copy of the bucketize code in the
+      // instruction cache); Prod needs both chunks' codes of its half afterwards
+      // and b + 1/2 bits packs a half at chunk-dependent positions: two per warp.
       constexpr bool kRoll = !PROD && !MIX;
       uint32_t cw[kRoll ? 1 : 2][BM];
       uint32_t hw[MIX ? 2 * BM + 1 : 1];  // b + 1/2 bits: the half's codes (mix_pos)
@@ -671,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
         if (lane == 0) mbar_arrive(&acc_empty[ab]);
       };
       auto do_chunk = [&](const int cc, const uint32_t(&av)[32], uint32_t(&cwc)[BM]) {
-        const int c = 2 * half + cc;
+        const int c = c0 + cc;
         uint32_t m32;
         if constexpr (MIX) {
           bool flagged = false;
@@ -682,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
           m32 = 0u;
           if (__any_sync(kFull, flagged && live)) {  // rare: the flags, from tensor memory again
             uint32_t t32[32];
-            tmem_ld32_nw(acc + 64 * half + 32 * cc, t32);
+            tmem_ld32_nw(acc + 32 * (c0 + cc), t32);
             tmem_wait_ld();
             if (flagged) m32 = mix_near_mask<BM>(t32, f, p.thr, p.thr_hi);
           }
@@ -698,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
           // values again from tensor memory (not yet handed back), then the flags
           if (__any_sync(kFull, flagged && live)) {
             uint32_t t32[32];
-            tmem_ld32_nw(acc + 64 * half + 32 * cc, t32);
+            tmem_ld32_nw(acc + 32 * (c0 + cc), t32);
             tmem_wait_ld();
             if (flagged) m32 = near_mask<BM>(t32, f, p.thr);
           }
@@ -800,16 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
             };
       // the accumulator goes back to the MMA after both chunks (a flagged chunk
       // reads it again); the kernel is epilogue-bound, so the MMA loses nothing
-      if constexpr (kRoll) {
-#pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          if (cc == 1) {
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) a0[j] = a1[j];
-          }
-          do_chunk(cc, a0, cw[0]);
-        }
+      if constexpr (kRoll) {  // one chunk per warp
+        do_chunk(0, a0, cw[0]);
       } else {
         do_chunk(0, a0, cw[0]);
         tmem_wait_ld();
@@ -877,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode128_kernel(const Enc128Para
           }
         }
       }
-      if (valid && half == 0) p.norm[dv] = s;
+      if (valid && c0 == 0) p.norm[dv] = s;
       // a5 (Prod): γ over both halves, residual operand, second product, signs
       if constexpr (PROD) {
         float* g2_s = norm_s + L::AccBufs * kRows;  // [2 tile parities][2 halves][128]
@@ -949,7 +947,7 @@ cudaError_t launch_t(const Enc128Params& p, const CUtensorMap& xmap, cudaStream_
   if (e != cudaSuccess) return e;
   const int64_t tiles = (p.N + kRows - 1) / kRows;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms()));
-  k<<<grid, kThreads, Lay<F16, PROD>::SmemAlloc, st>>>(p, xmap);
+  k<<<grid, enc_threads(PROD, MIX), Lay<F16, PROD>::SmemAlloc, st>>>(p, xmap);
   return cudaGetLastError();
 }
 
