@@ -64,9 +64,9 @@ constexpr int kDim = 128;                    // d = MMA N = K
 constexpr int kBox = kRows * 128;            // one 128-byte column box of the x tile: 16 KB
 constexpr int kTab = 4 * kUmmaPlaneBytes;    // B operand of one 128 x 128 matrix: (hi, lo) x 2 K chunks
 constexpr int kThreads = 14 * 32;
-// Plain MSE: 16 epilogue warps, one 32-column chunk each (22 warps in all);
-// Prod and b + 1/2 bits: 8, a column half each (they need both chunks of a half)
-__host__ __device__ constexpr int epi_warps(bool prod, bool mix) { return (!prod && !mix) ? 16 : 8; }
+// MSE and Prod: 16 epilogue warps, one 32-column chunk each (22 warps in all);
+// b + 1/2 bits: 8, a column half each (a half's codes are whole words)
+__host__ __device__ constexpr int epi_warps(bool prod, bool mix) { return !mix ? 16 : 8; }
 __host__ __device__ constexpr int enc_threads(bool prod, bool mix) { return (6 + epi_warps(prod, mix)) * 32; }
 constexpr float kMargin = 8e-6f;             // recomputation band around each threshold (v units)
 
@@ -87,7 +87,7 @@ struct Lay {
   static constexpr uint32_t TmemCols = Cols <= 256 ? 256 : 512;
   static constexpr int OffX = kTab * (PROD ? 2 : 1);
   static constexpr int OffNorm = OffX + XStages * Stage;
-  static constexpr int OffThr = OffNorm + (AccBufs + 4) * kRows * 4;  // norms, then (Prod) γ² halves
+  static constexpr int OffThr = OffNorm + (AccBufs + 8) * kRows * 4;  // norms, then (Prod) γ² per chunk
   static constexpr int OffCen = OffThr + 16 * 4;
   static constexpr int OffBar = OffCen + 16 * 4;
   static constexpr int NBar = 26;
@@ -425,12 +425,12 @@ __global__ void __launch_bounds__(enc_threads(PROD, MIX), 1) encode128_kernel(co
       mbar_init(&acc_empty[s], epi_warps(PROD, MIX));
       mbar_init(&nb_full[s], 4);
       mbar_init(&nb_empty[s], epi_warps(PROD, MIX));
-      mbar_init(&g2_full[s], 8);
+      mbar_init(&g2_full[s], epi_warps(PROD, MIX));
     }
-    mbar_init(a2_full, 8);
+    mbar_init(a2_full, epi_warps(PROD, MIX));
     mbar_init(a2_empty, 1);
     mbar_init(acc2_full, 1);
-    mbar_init(acc2_empty, 8);
+    mbar_init(acc2_empty, epi_warps(PROD, MIX));
     mbar_init(tab_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(enc_threads(PROD, MIX), 1) encode128_kernel(co
       // instruction cache); Prod needs both chunks' codes of its half afterwards
       // and b + 1/2 bits packs a half at chunk-dependent positions: two per warp.
       constexpr bool kRoll = !PROD && !MIX;
-      uint32_t cw[kRoll ? 1 : 2][BM];
+      uint32_t cw[CPW][BM];
       uint32_t hw[MIX ? 2 * BM + 1 : 1];  // b + 1/2 bits: the half's codes (mix_pos)
 #pragma unroll
       for (int w = 0; w < (MIX ? 2 * BM + 1 : 1); ++w) hw[w] = 0u;
@@ -806,12 +806,12 @@ __global__ void __launch_bounds__(enc_threads(PROD, MIX), 1) encode128_kernel(co
             };
       // the accumulator goes back to the MMA after both chunks (a flagged chunk
       // reads it again); the kernel is epilogue-bound, so the MMA loses nothing
-      if constexpr (kRoll) {  // one chunk per warp
+      if constexpr (CPW == 1) {  // one chunk per warp
         do_chunk(0, a0, cw[0]);
       } else {
         do_chunk(0, a0, cw[0]);
         tmem_wait_ld();
-        do_chunk(1, a1, cw[kRoll ? 0 : 1]);
+        do_chunk(1, a1, cw[CPW - 1]);
       }
       release_acc();
       if constexpr (MIX) {
@@ -876,32 +876,31 @@ __global__ void __launch_bounds__(enc_threads(PROD, MIX), 1) encode128_kernel(co
         }
       }
       if (valid && c0 == 0) p.norm[dv] = s;
-      // a5 (Prod): γ over both halves, residual operand, second product, signs
+      // a5 (Prod): γ over the row's four chunks, this chunk's residual operand,
+      // the second product, this chunk's signs
       if constexpr (PROD) {
-        float* g2_s = norm_s + L::AccBufs * kRows;  // [2 tile parities][2 halves][128]
-        g2_s[((i & 1) * 2 + half) * kRows + r] = g2;
+        float* g2_s = norm_s + L::AccBufs * kRows;  // [2 tile parities][4 chunks][128]
+        g2_s[((i & 1) * 4 + c0) * kRows + r] = g2;
         __syncwarp();
         if (lane == 0) mbar_arrive(&g2_full[i & 1]);
         if (!__all_sync(kFull, bar_wait(&g2_full[i & 1], ((uint32_t)i >> 1) & 1u, abort_flag, p.status, lim))) break;
-        const float g2t = g2_s[((i & 1) * 2) * kRows + r] + g2_s[((i & 1) * 2 + 1) * kRows + r];
+        const float* g2r = g2_s + (i & 1) * 4 * kRows + r;
+        const float g2t = (g2r[0] + g2r[kRows]) + (g2r[2 * kRows] + g2r[3 * kRows]);
         const float gam = live ? sqrtf(fmaxf(g2t, 0.f)) / (float)p.sqrt_d : 0.f;
         const float rsd = live ? pow2_scale_16_32(gam) / (float)p.sqrt_d : 0.f;
         if (!__all_sync(kFull, bar_wait(a2_empty, ((uint32_t)i & 1u) ^ 1u, abort_flag, p.status, lim))) break;
         tc_fence_after();
         const uint32_t a2 = tmem + lane_base + L::ColA2;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * half + cc;
+        {
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const uint32_t* av = cc ? a1 : a0;
-            const float r0 = (__uint_as_float(av[2 * j]) * f - cen_s[get_bits<BM>(cw[cc], 2 * j * BM)]) * rsd;
-            const float r1 = (__uint_as_float(av[2 * j + 1]) * f - cen_s[get_bits<BM>(cw[cc], (2 * j + 1) * BM)]) * rsd;
+            const float r0 = (__uint_as_float(a0[2 * j]) * f - cen_s[get_bits<BM>(cw[0], 2 * j * BM)]) * rsd;
+            const float r1 = (__uint_as_float(a0[2 * j + 1]) * f - cen_s[get_bits<BM>(cw[0], (2 * j + 1) * BM)]) * rsd;
             split2(r0, r1, hi[j], lo[j]);
           }
-          tmem_st16(a2 + 16 * c, hi);
-          tmem_st16(a2 + 64 + 16 * c, lo);
+          tmem_st16(a2 + 16 * c0, hi);
+          tmem_st16(a2 + 64 + 16 * c0, lo);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -909,23 +908,18 @@ __global__ void __launch_bounds__(enc_threads(PROD, MIX), 1) encode128_kernel(co
         if (lane == 0) mbar_arrive(a2_full);
         if (!__all_sync(kFull, bar_wait(acc2_full, (uint32_t)i & 1u, abort_flag, p.status, lim))) break;
         tc_fence_after();
-        uint32_t sg[2];
+        uint32_t pa[32];
+        tmem_ld32_nw(tmem + lane_base + L::ColAcc2 + 32 * c0, pa);
+        tmem_wait_ld();
+        uint32_t bits = 0u;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t pa[32];
-          tmem_ld32_nw(tmem + lane_base + L::ColAcc2 + 32 * (2 * half + cc), pa);
-          tmem_wait_ld();
-          uint32_t bits = 0u;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) bits |= (__uint_as_float(pa[j]) >= 0.f ? 1u : 0u) << j;
-          sg[cc] = live ? bits : 0u;
-        }
+        for (int j = 0; j < 32; ++j) bits |= (__uint_as_float(pa[j]) >= 0.f ? 1u : 0u) << j;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc2_empty);
         if (valid) {
-          *reinterpret_cast<uint2*>(p.qjl + dv * p.QW + 2 * half) = make_uint2(sg[0], sg[1]);
-          if (half == 0) p.rnorm[dv] = gam;
+          p.qjl[dv * p.QW + c0] = live ? bits : 0u;
+          if (c0 == 0) p.rnorm[dv] = gam;
         }
       }
     }
