@@ -29,7 +29,7 @@
 // fp16 hi + lo into tensor memory, and a second three-pass product with
 // (m_scale·S·Πᵀ) gives p = S·r up to a positive factor; bit_j = [p_j >= 0].
 //
-// Warp roles (14 warps):
+// Warp roles (22 warps):
 //   0     producer: the B operand tables once (bulk copy), then per tile one
 //         2-D TMA load per 128-byte column box of the x tile.
 //   1     MMA issuer (one thread).
@@ -37,13 +37,13 @@
 //         s = ‖x‖ from the staged tile (fp32 sums; a row whose sum leaves
 //         (1e-30, 1e36) is summed again scaled by a power of two); fp32 rows:
 //         the split A operand into tensor memory.
-//   6-13  epilogue: thread = row, two warps per TMEM lane quadrant, each for
-//         64 of the 128 columns, taken as two 32-column chunks (a chunk's
-//         codes are BM whole words of the row's stream): v = acc·√d/(s·scales),
+//   6-21  epilogue: thread = row, four warps per TMEM lane quadrant, each for
+//         one 32-column chunk (its codes are BM whole words of the row's
+//         stream; at b + 1/2 bits 2·BM + 1 halfwords): v = acc·√d/(s·scales),
 //         bucketize (a branch-free count over the thresholds, kept as kernel
 //         constants) with a near-threshold flag, pack in registers, recompute
-//         flagged coordinates, store; Prod: γ over both halves, the residual
-//         operand, the second product, sign bits.
+//         flagged coordinates, store; Prod: γ over the four chunks, the
+//         chunk's residual operand, the second product, its sign bits.
 // All waits are bounded (tq_ctx_set_wait_limit); a wait that gives up sets the
 // abort flag, which every role polls, and bit 0 of the status word.
 #include <cuda.h>
@@ -63,11 +63,10 @@ constexpr int kRows = 128;                   // rows per tile = TMEM lanes = MMA
 constexpr int kDim = 128;                    // d = MMA N = K
 constexpr int kBox = kRows * 128;            // one 128-byte column box of the x tile: 16 KB
 constexpr int kTab = 4 * kUmmaPlaneBytes;    // B operand of one 128 x 128 matrix: (hi, lo) x 2 K chunks
-constexpr int kThreads = 14 * 32;
-// MSE and Prod: 16 epilogue warps, one 32-column chunk each (22 warps in all);
-// b + 1/2 bits: 8, a column half each (a half's codes are whole words)
-__host__ __device__ constexpr int epi_warps(bool prod, bool mix) { return !mix ? 16 : 8; }
-__host__ __device__ constexpr int enc_threads(bool prod, bool mix) { return (6 + epi_warps(prod, mix)) * 32; }
+// 16 epilogue warps, one 32-column chunk of a tensor-memory lane quadrant each
+// (22 warps in all)
+constexpr int kEpiWarps = 16;
+constexpr int kEncThreads = (6 + kEpiWarps) * 32;
 constexpr float kMargin = 8e-6f;             // recomputation band around each threshold (v units)
 
 template <bool F16, bool PROD>
@@ -240,25 +239,25 @@ __device__ __forceinline__ uint32_t chunk_codes(const uint32_t (&a)[32], float f
   return m32;
 }
 
-// b + 1/2 bits per coordinate: coordinate k (0..63) of a column half has BM + 1
-// bits where k mod 16 < 8 and BM bits elsewhere; its code starts at bit
-// mixed_pos(k, BM) of the half's 2·BM + 1 words (every 16 coordinates span
-// 8·(2·BM + 1) bits, so a half is whole words of the row's stream).
-// One 32-column chunk CC (0 or 1) of a half at b + 1/2 bits (symmetric
-// codebooks): codes into the half's words hw at compile-time positions; a
-// coordinate near a threshold anywhere in the chunk sets `flagged`.
-template <int BM, int CC>
+// b + 1/2 bits per coordinate: coordinate j (0..31) of a 32-column chunk has
+// BM + 1 bits where j mod 16 < 8 and BM bits elsewhere; its code starts at bit
+// mixed_pos(j, BM) of the chunk's codes (every 16 coordinates span 8·(2·BM + 1)
+// bits, so a chunk is 2·BM + 1 halfwords of the row's stream).
+// One chunk at b + 1/2 bits (symmetric codebooks): codes into hw at
+// compile-time positions; a coordinate near a threshold anywhere in the chunk
+// sets `flagged`.
+template <int BM>
 __device__ __forceinline__ void mix_chunk_codes(const uint32_t (&a)[32], float f, const float (&tlo)[15],
-                                                const float (&thi)[15], uint32_t (&hw)[2 * BM + 1],
+                                                const float (&thi)[15], uint32_t (&hw)[BM + 1],
                                                 bool& flagged) {
   float dmin = INFINITY;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const float v = __uint_as_float(a[j]) * f;
     if ((j & 8) == 0)
-      put_bits<BM + 1>(hw, mixed_pos(32 * CC + j, BM), bucketize_fold<BM + 1>(v, thi, dmin));
+      put_bits<BM + 1>(hw, mixed_pos(j, BM), bucketize_fold<BM + 1>(v, thi, dmin));
     else
-      put_bits<BM>(hw, mixed_pos(32 * CC + j, BM), bucketize_fold<BM>(v, tlo, dmin));
+      put_bits<BM>(hw, mixed_pos(j, BM), bucketize_fold<BM>(v, tlo, dmin));
   }
   flagged = dmin < kMargin;
 }
@@ -377,7 +376,7 @@ __device__ __forceinline__ void mma3_ts(uint32_t acc, uint32_t a0, uint32_t btab
 }
 
 template <int BM, bool PROD, bool F16, bool MIX>
-__global__ void __launch_bounds__(enc_threads(PROD, MIX), 1) encode128_kernel(const Enc128Params p,
+__global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128Params p,
                                                                  const __grid_constant__ CUtensorMap xmap) {
   using L = Lay<F16, PROD>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -422,15 +421,15 @@ __global__ void __launch_bounds__(enc_threads(PROD, MIX), 1) encode128_kernel(co
       mbar_init(&a_full[s], 4);
       mbar_init(&a_empty[s], 1);
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], epi_warps(PROD, MIX));
+      mbar_init(&acc_empty[s], kEpiWarps);
       mbar_init(&nb_full[s], 4);
-      mbar_init(&nb_empty[s], epi_warps(PROD, MIX));
-      mbar_init(&g2_full[s], epi_warps(PROD, MIX));
+      mbar_init(&nb_empty[s], kEpiWarps);
+      mbar_init(&g2_full[s], kEpiWarps);
     }
-    mbar_init(a2_full, epi_warps(PROD, MIX));
+    mbar_init(a2_full, kEpiWarps);
     mbar_init(a2_empty, 1);
     mbar_init(acc2_full, 1);
-    mbar_init(acc2_empty, epi_warps(PROD, MIX));
+    mbar_init(acc2_empty, kEpiWarps);
     mbar_init(tab_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -629,11 +628,8 @@ __global__ void __launch_bounds__(enc_threads(PROD, MIX), 1) encode128_kernel(co
     }
   } else {
     // ---------------- epilogue: warps 6..; warp w serves TMEM lanes 32·(w % 4)..+31
-    // (rows of the tile); plain MSE: chunk (w - 6) / 4 of the four 32-column
-    // chunks; Prod and b + 1/2 bits: the column half (w - 6) / 4, chunks
-    // 2·half and 2·half + 1
-    constexpr int CPW = epi_warps(PROD, MIX) == 16 ? 1 : 2;  // chunks per warp
-    const int q = warp & 3, r = 32 * q + lane, half = (warp - 6) >> 2, c0 = half * CPW;
+    // (rows of the tile) and chunk c0 = (w - 6) / 4 of the four 32-column chunks
+    const int q = warp & 3, r = 32 * q + lane, c0 = (warp - 6) >> 2;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const bool even = (lane & 1) == 0;
     for (int i = 0; i < nloc; ++i) {
@@ -654,224 +650,226 @@ __global__ void __launch_bounds__(enc_threads(PROD, MIX), 1) encode128_kernel(co
       if (!__all_sync(kFull, bar_wait(&acc_full[ab], par, abort_flag, p.status, lim))) break;
       tc_fence_after();
       const uint32_t acc = tmem + lane_base + L::ColAcc + ab * 128;
-      uint32_t a0[32], a1[32];
+      uint32_t a0[32];
       tmem_ld32_nw(acc + 32 * c0, a0);
       tmem_wait_ld();
-      if constexpr (CPW == 2) tmem_ld32_nw(acc + 32 * (c0 + 1), a1);  // waited for after the first chunk's codes
-      // a3/a4 per 32-coordinate chunk: bucketize, flag, pack into BM words
-      // (chunk c of a row is words [c·BM, c·BM + BM) of its stream), recompute
-      // flagged coordinates, store
-      // Plain MSE: one chunk per warp (one copy of the bucketize code in the
-      // instruction cache); Prod needs both chunks' codes of its half afterwards
-      // and b + 1/2 bits packs a half at chunk-dependent positions: two per warp.
-      constexpr bool kRoll = !PROD && !MIX;
-      uint32_t cw[CPW][BM];
-      uint32_t hw[MIX ? 2 * BM + 1 : 1];  // b + 1/2 bits: the half's codes (mix_pos)
+      // a3/a4 on the warp's 32-coordinate chunk c0: bucketize, flag, pack
+      // (MSE and Prod: BM words, words [c0·BM, c0·BM + BM) of the row's
+      // stream; b + 1/2 bits: 2·BM + 1 halfwords from halfword c0·(2·BM + 1)),
+      // recompute flagged coordinates, store
+      constexpr int HW = 2 * BM + 1;  // b + 1/2 bits: halfwords of a chunk
+      uint32_t cw[BM];
+      uint32_t hw[MIX ? BM + 1 : 1];  // b + 1/2 bits: the chunk's codes at mixed_pos
 #pragma unroll
-      for (int w = 0; w < (MIX ? 2 * BM + 1 : 1); ++w) hw[w] = 0u;
+      for (int w = 0; w < (MIX ? BM + 1 : 1); ++w) hw[w] = 0u;
       float g2 = 0.f;
-      // hand the accumulator back to the MMA
-      auto release_acc = [&]() {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[ab]);
-      };
-      auto do_chunk = [&](const int cc, const uint32_t(&av)[32], uint32_t(&cwc)[BM]) {
-        const int c = c0 + cc;
-        uint32_t m32;
-        if constexpr (MIX) {
-          bool flagged = false;
-          if (cc == 0)
-            mix_chunk_codes<BM, 0>(a0, f, p.thr, p.thr_hi, hw, flagged);
-          else
-            mix_chunk_codes<BM, 1>(a1, f, p.thr, p.thr_hi, hw, flagged);
-          m32 = 0u;
-          if (__any_sync(kFull, flagged && live)) {  // rare: the flags, from tensor memory again
-            uint32_t t32[32];
-            tmem_ld32_nw(acc + 32 * (c0 + cc), t32);
-            tmem_wait_ld();
-            if (flagged) m32 = mix_near_mask<BM>(t32, f, p.thr, p.thr_hi);
-          }
-        } else {
-          // Prod keys take general thresholds too (keeping that branch also
-          // schedules the Prod epilogue better: 2.57 -> 2.95 Gvec/s measured)
-          bool flagged = false;
-          if (PROD && !p.sym)
-            m32 = chunk_codes<BM, false, PROD>(av, f, p.thr, cen_s, cwc, g2, flagged);
-          else
-            m32 = chunk_codes<BM, true, PROD>(av, f, p.thr, cen_s, cwc, g2, flagged);
-          // a chunk with a coordinate near a threshold (~1e-3 of them): its
-          // values again from tensor memory (not yet handed back), then the flags
-          if (__any_sync(kFull, flagged && live)) {
-            uint32_t t32[32];
-            tmem_ld32_nw(acc + 32 * (c0 + cc), t32);
-            tmem_wait_ld();
-            if (flagged) m32 = near_mask<BM>(t32, f, p.thr);
-          }
-        }
-        if (!live) {
-#pragma unroll
-          for (int w = 0; w < BM; ++w) cwc[w] = 0u;
-#pragma unroll
-          for (int w = 0; w < (MIX ? 2 * BM + 1 : 1); ++w) hw[w] = 0u;
-          m32 = 0u;
-          g2 = 0.f;
-        }
-        // flagged coordinates: one warp-wide float-float dot product each
-        for (;;) {
-          const uint32_t any = __ballot_sync(kFull, m32 != 0u);
-          if (!any) break;
-          const int src = __ffs(any) - 1;
-          int j = 0;
-          if (lane == src) {
-            j = __ffs(m32) - 1;
-            m32 &= m32 - 1u;
-          }
-          j = __shfl_sync(kFull, j, src);
-          const float ssrc = __shfl_sync(kFull, s, src);
-          const float vv = exact_coord<F16>(p.x, p.pi, p.sqrt_d, t * kRows + 32 * q + src, 32 * c + j, ssrc, lane);
-          if (lane == src) {
-            bool nr;
-            if constexpr (MIX) {
-              const bool hi = (j & 8) == 0;
-              const uint32_t code = hi ? bucketize<BM + 1>(vv, cen_s, 0.f, nr) : bucketize<BM>(vv, thr_s, 0.f, nr);
-              set_bits_rt(hw, mixed_pos(32 * cc + j, BM), hi ? BM + 1 : BM, code);
-            } else {
-              const uint32_t code = bucketize<BM>(vv, thr_s, 0.f, nr);
-              if constexpr (PROD) {
-                const uint32_t old = code_at<BM>(cwc, j);
-                const float e0 = vv - cen_s[old], e1 = vv - cen_s[code];
-                g2 += e1 * e1 - e0 * e0;
-              }
-              set_code<BM>(cwc, j, code);
-            }
-          }
-        }
-        // stores of this chunk's codes (b + 1/2 bits: of both chunks, below)
-        if (MIX) {
-        } else if (p.layout == TQ_LAYOUT_TOKEN) {
-          if (valid) {
-            uint32_t* dst = p.codes + dv * p.W + c * BM;
-#pragma unroll
-            for (int w = 0; w < BM; ++w) dst[w] = cwc[w];
-          }
-        } else {
-          // PAIR: vectors 2k and 2k+1 share a block; coordinate j's two codes
-          // sit side by side at block bits 2j·BM (even vector low).  Rows r and
-          // r+1 of the tile are lanes l and l+1; when the destination pairs them,
-          // the even lane writes the block words of coordinates 32c..32c+15 and
-          // the odd lane those of 32c+16..32c+31, after one exchange.
-          uint32_t part[BM];
-#pragma unroll
-          for (int w = 0; w < BM; ++w) part[w] = __shfl_xor_sync(kFull, cwc[w], 1);
-          const int64_t base_row = row - (even ? 0 : 1);
-          const bool whole = p.pair_aligned && base_row + 1 < p.N;
-          uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)p.W) + 2 * c * BM;
-          if (valid && whole) {
-            uint32_t ow[BM];
-#pragma unroll
-            for (int w = 0; w < BM; ++w) ow[w] = 0u;
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const uint32_t own = even ? get_bits<BM>(cwc, jj * BM) : get_bits<BM>(cwc, (16 + jj) * BM);
-              const uint32_t prt = even ? get_bits<BM>(part, jj * BM) : get_bits<BM>(part, (16 + jj) * BM);
-              put_bits<BM>(ow, 2 * jj * BM, even ? own : prt);
-              put_bits<BM>(ow, (2 * jj + 1) * BM, even ? prt : own);
-            }
-#pragma unroll
-            for (int w = 0; w < BM; ++w) blk[(even ? 0 : BM) + w] = ow[w];
-          } else if (valid) {
-            // the partner is written by another call (or not at all): this
-            // vector's fields of the chunk's 2·BM block words by masked atomics
-            // (both slots built at compile-time positions, then picked)
-            const bool odd = (dv & 1) != 0;
-            uint32_t f0[2 * BM], f1[2 * BM], m0[2 * BM], m1[2 * BM];
-#pragma unroll
-            for (int w = 0; w < 2 * BM; ++w) f0[w] = f1[w] = m0[w] = m1[w] = 0u;
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const uint32_t code = get_bits<BM>(cwc, jj * BM);
-              put_bits<BM>(f0, 2 * jj * BM, code);
-              put_bits<BM>(f1, (2 * jj + 1) * BM, code);
-              put_bits<BM>(m0, 2 * jj * BM, (1u << BM) - 1u);
-              put_bits<BM>(m1, (2 * jj + 1) * BM, (1u << BM) - 1u);
-            }
-#pragma unroll
-            for (int w = 0; w < 2 * BM; ++w) {
-              atomicAnd(blk + w, ~(odd ? m1[w] : m0[w]));
-              atomicOr(blk + w, odd ? f1[w] : f0[w]);
-            }
-          }
-        }
-            };
-      // the accumulator goes back to the MMA after both chunks (a flagged chunk
-      // reads it again); the kernel is epilogue-bound, so the MMA loses nothing
-      if constexpr (CPW == 1) {  // one chunk per warp
-        do_chunk(0, a0, cw[0]);
-      } else {
-        do_chunk(0, a0, cw[0]);
-        tmem_wait_ld();
-        do_chunk(1, a1, cw[CPW - 1]);
-      }
-      release_acc();
+      uint32_t m32;
       if constexpr (MIX) {
-        // the half's 2·BM + 1 words: coordinates 64·half .. 64·half + 63
-        constexpr int HW = 2 * BM + 1;
-        if (p.layout == TQ_LAYOUT_TOKEN) {
-          if (valid) {
-            uint32_t* dst = p.codes + dv * p.W + half * HW;
+        bool flagged = false;
+        mix_chunk_codes<BM>(a0, f, p.thr, p.thr_hi, hw, flagged);
+        m32 = 0u;
+        if (__any_sync(kFull, flagged && live)) {  // rare: the flags, from tensor memory again
+          uint32_t t32[32];
+          tmem_ld32_nw(acc + 32 * c0, t32);
+          tmem_wait_ld();
+          if (flagged) m32 = mix_near_mask<BM>(t32, f, p.thr, p.thr_hi);
+        }
+      } else {
+        // Prod keys take general thresholds too (keeping that branch also
+        // schedules the Prod epilogue better: 2.57 -> 2.95 Gvec/s measured)
+        bool flagged = false;
+        if (PROD && !p.sym)
+          m32 = chunk_codes<BM, false, PROD>(a0, f, p.thr, cen_s, cw, g2, flagged);
+        else
+          m32 = chunk_codes<BM, true, PROD>(a0, f, p.thr, cen_s, cw, g2, flagged);
+        // a chunk with a coordinate near a threshold (~1e-3 of them): its
+        // values again from tensor memory (not yet handed back), then the flags
+        if (__any_sync(kFull, flagged && live)) {
+          uint32_t t32[32];
+          tmem_ld32_nw(acc + 32 * c0, t32);
+          tmem_wait_ld();
+          if (flagged) m32 = near_mask<BM>(t32, f, p.thr);
+        }
+      }
+      // the accumulator goes back to the MMA (the kernel is epilogue-bound,
+      // so the MMA loses nothing by waiting for a flagged chunk's re-read)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      if (!live) {
 #pragma unroll
-            for (int w = 0; w < HW; ++w) dst[w] = hw[w];
+        for (int w = 0; w < BM; ++w) cw[w] = 0u;
+#pragma unroll
+        for (int w = 0; w < (MIX ? BM + 1 : 1); ++w) hw[w] = 0u;
+        m32 = 0u;
+        g2 = 0.f;
+      }
+      // flagged coordinates: one warp-wide float-float dot product each
+      for (;;) {
+        const uint32_t any = __ballot_sync(kFull, m32 != 0u);
+        if (!any) break;
+        const int src = __ffs(any) - 1;
+        int j = 0;
+        if (lane == src) {
+          j = __ffs(m32) - 1;
+          m32 &= m32 - 1u;
+        }
+        j = __shfl_sync(kFull, j, src);
+        const float ssrc = __shfl_sync(kFull, s, src);
+        const float vv = exact_coord<F16>(p.x, p.pi, p.sqrt_d, t * kRows + 32 * q + src, 32 * c0 + j, ssrc, lane);
+        if (lane == src) {
+          bool nr;
+          if constexpr (MIX) {
+            const bool hi = (j & 8) == 0;
+            const uint32_t code = hi ? bucketize<BM + 1>(vv, cen_s, 0.f, nr) : bucketize<BM>(vv, thr_s, 0.f, nr);
+            set_bits_rt(hw, mixed_pos(j, BM), hi ? BM + 1 : BM, code);
+          } else {
+            const uint32_t code = bucketize<BM>(vv, thr_s, 0.f, nr);
+            if constexpr (PROD) {
+              const uint32_t old = code_at<BM>(cw, j);
+              const float e0 = vv - cen_s[old], e1 = vv - cen_s[code];
+              g2 += e1 * e1 - e0 * e0;
+            }
+            set_code<BM>(cw, j, code);
           }
-        } else {
-          // PAIR: coordinate k's field of 2·w_k bits at block bit 2·P_k.  The
-          // half's block words are 2·HW: the even lane of a row pair writes the
-          // first HW (coordinates 0-31 of the half), the odd lane the rest
-          // (32-63, whose fields sit at the same offsets within its words).
-          uint32_t part[HW];
+        }
+      }
+      // stores of the chunk's codes
+      if (MIX && p.layout == TQ_LAYOUT_TOKEN) {
+        if (valid) {
+          uint16_t* dst = reinterpret_cast<uint16_t*>(p.codes + dv * p.W) + c0 * HW;
 #pragma unroll
-          for (int w = 0; w < HW; ++w) part[w] = __shfl_xor_sync(kFull, hw[w], 1);
-          const int64_t base_row = row - (even ? 0 : 1);
-          const bool whole = p.pair_aligned && base_row + 1 < p.N;
-          uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)p.W) + half * 2 * HW;
-          if (valid && whole) {
-            uint32_t ow[HW];
+          for (int k = 0; k < HW; ++k) dst[k] = (uint16_t)(hw[k >> 1] >> (16 * (k & 1)));
+        }
+      } else if (MIX) {
+        // PAIR: coordinate j's field of 2·w_j bits at block bit 2·P_j; the
+        // chunk's block is 2·HW halfwords from halfword 2·c0·HW.  Rows r and
+        // r+1 of the tile are lanes l and l+1; when the destination pairs them,
+        // the even lane writes the fields of coordinates 0-15 (halfwords
+        // [0, HW)), the odd lane those of 16-31 ([HW, 2·HW), the same offsets
+        // within), after one exchange.
+        uint32_t part[BM + 1];
 #pragma unroll
-            for (int w = 0; w < HW; ++w) ow[w] = 0u;
+        for (int w = 0; w <= BM; ++w) part[w] = __shfl_xor_sync(kFull, hw[w], 1);
+        const int64_t base_row = row - (even ? 0 : 1);
+        const bool whole = p.pair_aligned && base_row + 1 < p.N;
+        uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)p.W) + c0 * HW;
+        if (valid && whole) {
+          // the even and odd vectors' codes of this lane's 16 coordinates
+          // (the odd lane's start 8·HW bits into the chunk)
+          constexpr int K = 8 * HW;
+          uint32_t E[BM + 1], O[BM + 1], ev[BM + 1], od[BM + 1], ob[BM + 1];
 #pragma unroll
-            for (int kk = 0; kk < 32; ++kk) {
-              const int wk = (kk & 8) ? BM : BM + 1, pk = mixed_pos(kk, BM);
-              const uint32_t own = even ? get_bits_rt(hw, pk, wk) : get_bits_rt(hw, pk + 16 * HW, wk);
-              const uint32_t prt = even ? get_bits_rt(part, pk, wk) : get_bits_rt(part, pk + 16 * HW, wk);
-              set_bits_rt(ow, 2 * pk, wk, even ? own : prt);
-              set_bits_rt(ow, 2 * pk + wk, wk, even ? prt : own);
+          for (int w = 0; w <= BM; ++w) {
+            E[w] = even ? hw[w] : part[w];
+            O[w] = even ? part[w] : hw[w];
+          }
+#pragma unroll
+          for (int w = 0; w <= BM; ++w) {
+            const int lo = (K + 32 * w) >> 5, sh = (K + 32 * w) & 31;
+            uint32_t se = 0u, so = 0u;
+            if (lo <= BM) {
+              se = E[lo] >> sh;
+              so = O[lo] >> sh;
             }
-#pragma unroll
-            for (int w = 0; w < HW; ++w) blk[(even ? 0 : HW) + w] = ow[w];
-          } else if (valid) {
-            // the partner is written by another call (or not at all): this
-            // vector's fields of the half's 2·HW block words by masked atomics
-            // (word by word: only the fields overlapping word w, a compile-time
-            // test once both loops are unrolled; the slot picks the shift)
-            const bool odd = (dv & 1) != 0;
-            auto shift = [](uint32_t x, int sh) -> uint32_t {
-              return sh >= 32 || sh <= -32 ? 0u : (sh >= 0 ? x << sh : x >> (-sh));
-            };
-#pragma unroll
-            for (int w = 0; w < 2 * HW; ++w) {
-              uint32_t fb = 0u, mb = 0u;
-#pragma unroll
-              for (int k = 0; k < 64; ++k) {
-                const int wk = (k & 8) ? BM : BM + 1, pk = mixed_pos(k, BM);
-                const int p0 = 2 * pk - 32 * w;  // the pair field of coordinate k, relative to word w
-                if (p0 >= 32 || p0 + 2 * wk <= 0) continue;
-                const int sh = odd ? p0 + wk : p0;
-                fb |= shift(get_bits_rt(hw, pk, wk), sh);
-                mb |= shift((1u << wk) - 1u, sh);
-              }
-              atomicAnd(blk + w, ~mb);
-              atomicOr(blk + w, fb);
+            if (sh != 0 && lo + 1 <= BM) {
+              se |= E[lo + 1] << (32 - sh);
+              so |= O[lo + 1] << (32 - sh);
             }
+            ev[w] = even ? E[w] : se;
+            od[w] = even ? O[w] : so;
+            ob[w] = 0u;
+          }
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int pk = mixed_pos(k, BM);
+            if ((k & 8) == 0) {
+              put_bits<BM + 1>(ob, 2 * pk, get_bits<BM + 1>(ev, pk));
+              put_bits<BM + 1>(ob, 2 * pk + BM + 1, get_bits<BM + 1>(od, pk));
+            } else {
+              put_bits<BM>(ob, 2 * pk, get_bits<BM>(ev, pk));
+              put_bits<BM>(ob, 2 * pk + BM, get_bits<BM>(od, pk));
+            }
+          }
+          uint16_t* dst = reinterpret_cast<uint16_t*>(blk) + (even ? 0 : HW);
+#pragma unroll
+          for (int k = 0; k < HW; ++k) dst[k] = (uint16_t)(ob[k >> 1] >> (16 * (k & 1)));
+        } else if (valid) {
+          // the partner is written by another call (or not at all): this
+          // vector's fields of the chunk's HW block words by masked atomics
+          // (word by word: only the fields overlapping word w, a compile-time
+          // test once both loops are unrolled; the slot picks the shift)
+          const bool odd = (dv & 1) != 0;
+          auto shift = [](uint32_t x, int sh) -> uint32_t {
+            return sh >= 32 || sh <= -32 ? 0u : (sh >= 0 ? x << sh : x >> (-sh));
+          };
+#pragma unroll
+          for (int w = 0; w < HW; ++w) {
+            uint32_t fb = 0u, mb = 0u;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int wk = (k & 8) ? BM : BM + 1, pk = mixed_pos(k, BM);
+              const int p0 = 2 * pk - 32 * w;  // the pair field of coordinate k, relative to word w
+              if (p0 >= 32 || p0 + 2 * wk <= 0) continue;
+              const int sh = odd ? p0 + wk : p0;
+              fb |= shift(get_bits_rt(hw, pk, wk), sh);
+              mb |= shift((1u << wk) - 1u, sh);
+            }
+            atomicAnd(blk + w, ~mb);
+            atomicOr(blk + w, fb);
+          }
+        }
+      } else if (p.layout == TQ_LAYOUT_TOKEN) {
+        if (valid) {
+          uint32_t* dst = p.codes + dv * p.W + c0 * BM;
+#pragma unroll
+          for (int w = 0; w < BM; ++w) dst[w] = cw[w];
+        }
+      } else {
+        // PAIR: vectors 2k and 2k+1 share a block; coordinate j's two codes
+        // sit side by side at block bits 2j·BM (even vector low).  Rows r and
+        // r+1 of the tile are lanes l and l+1; when the destination pairs them,
+        // the even lane writes the block words of coordinates 32c..32c+15 and
+        // the odd lane those of 32c+16..32c+31, after one exchange.
+        uint32_t part[BM];
+#pragma unroll
+        for (int w = 0; w < BM; ++w) part[w] = __shfl_xor_sync(kFull, cw[w], 1);
+        const int64_t base_row = row - (even ? 0 : 1);
+        const bool whole = p.pair_aligned && base_row + 1 < p.N;
+        uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)p.W) + 2 * c0 * BM;
+        if (valid && whole) {
+          uint32_t ow[BM];
+#pragma unroll
+          for (int w = 0; w < BM; ++w) ow[w] = 0u;
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const uint32_t own = even ? get_bits<BM>(cw, jj * BM) : get_bits<BM>(cw, (16 + jj) * BM);
+            const uint32_t prt = even ? get_bits<BM>(part, jj * BM) : get_bits<BM>(part, (16 + jj) * BM);
+            put_bits<BM>(ow, 2 * jj * BM, even ? own : prt);
+            put_bits<BM>(ow, (2 * jj + 1) * BM, even ? prt : own);
+          }
+#pragma unroll
+          for (int w = 0; w < BM; ++w) blk[(even ? 0 : BM) + w] = ow[w];
+        } else if (valid) {
+          // the partner is written by another call (or not at all): this
+          // vector's fields of the chunk's 2·BM block words by masked atomics
+          // (both slots built at compile-time positions, then picked)
+          const bool odd = (dv & 1) != 0;
+          uint32_t f0[2 * BM], f1[2 * BM], m0[2 * BM], m1[2 * BM];
+#pragma unroll
+          for (int w = 0; w < 2 * BM; ++w) f0[w] = f1[w] = m0[w] = m1[w] = 0u;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const uint32_t code = get_bits<BM>(cw, jj * BM);
+            put_bits<BM>(f0, 2 * jj * BM, code);
+            put_bits<BM>(f1, (2 * jj + 1) * BM, code);
+            put_bits<BM>(m0, 2 * jj * BM, (1u << BM) - 1u);
+            put_bits<BM>(m1, (2 * jj + 1) * BM, (1u << BM) - 1u);
+          }
+#pragma unroll
+          for (int w = 0; w < 2 * BM; ++w) {
+            atomicAnd(blk + w, ~(odd ? m1[w] : m0[w]));
+            atomicOr(blk + w, odd ? f1[w] : f0[w]);
           }
         }
       }
@@ -895,8 +893,8 @@ __global__ void __launch_bounds__(enc_threads(PROD, MIX), 1) encode128_kernel(co
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float r0 = (__uint_as_float(a0[2 * j]) * f - cen_s[get_bits<BM>(cw[0], 2 * j * BM)]) * rsd;
-            const float r1 = (__uint_as_float(a0[2 * j + 1]) * f - cen_s[get_bits<BM>(cw[0], (2 * j + 1) * BM)]) * rsd;
+            const float r0 = (__uint_as_float(a0[2 * j]) * f - cen_s[get_bits<BM>(cw, 2 * j * BM)]) * rsd;
+            const float r1 = (__uint_as_float(a0[2 * j + 1]) * f - cen_s[get_bits<BM>(cw, (2 * j + 1) * BM)]) * rsd;
             split2(r0, r1, hi[j], lo[j]);
           }
           tmem_st16(a2 + 16 * c0, hi);
@@ -941,7 +939,7 @@ cudaError_t launch_t(const Enc128Params& p, const CUtensorMap& xmap, cudaStream_
   if (e != cudaSuccess) return e;
   const int64_t tiles = (p.N + kRows - 1) / kRows;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)num_sms()));
-  k<<<grid, enc_threads(PROD, MIX), Lay<F16, PROD>::SmemAlloc, st>>>(p, xmap);
+  k<<<grid, kEncThreads, Lay<F16, PROD>::SmemAlloc, st>>>(p, xmap);
   return cudaGetLastError();
 }
 
