@@ -280,6 +280,36 @@ __device__ __forceinline__ uint32_t mix_near_mask(const uint32_t (&a)[32], float
   return m32;
 }
 
+// One 32-column chunk (symmetric codebook) for the PAIR layout: coordinate j's
+// code goes straight to its even-vector slot of the chunk's pair block, bits
+// 2(j mod 16)·BM of lo (j < 16) or hi (j >= 16), so that a row pair's block
+// words are one exchange and an OR away (an odd vector shifts by BM first).
+template <int BM>
+__device__ __forceinline__ void chunk_codes_pair(const uint32_t (&a)[32], float f, const float (&thr)[15],
+                                                 uint32_t (&lo)[BM], uint32_t (&hi)[BM], bool& flagged) {
+#pragma unroll
+  for (int w = 0; w < BM; ++w) lo[w] = hi[w] = 0u;
+  float dmin = INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t code = bucketize_fold<BM>(__uint_as_float(a[j]) * f, thr, dmin);
+    if (j < 16)
+      put_bits<BM>(lo, 2 * j * BM, code);
+    else
+      put_bits<BM>(hi, 2 * (j - 16) * BM, code);
+  }
+  flagged = dmin < kMargin;
+}
+
+// Words x << BM (BM < 32) of a BM-word array, the top field leaving nothing behind
+// (slot 30 of the even vector moves to slot 31).
+template <int BM>
+__device__ __forceinline__ void shift_slot(uint32_t (&x)[BM]) {
+#pragma unroll
+  for (int w = BM - 1; w > 0; --w) x[w] = (x[w] << BM) | (x[w - 1] >> (32 - BM));
+  x[0] <<= BM;
+}
+
 // Bits [pos, pos + width) of a word array (run-time position and width), and their replacement.
 template <int N>
 __device__ __forceinline__ uint32_t get_bits_rt(const uint32_t (&wd)[N], int pos, int width) {
@@ -375,7 +405,7 @@ __device__ __forceinline__ void mma3_ts(uint32_t acc, uint32_t a0, uint32_t btab
     }
 }
 
-template <int BM, bool PROD, bool F16, bool MIX>
+template <int BM, bool PROD, bool F16, bool MIX, bool PAIRL>
 __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128Params p,
                                                                  const __grid_constant__ CUtensorMap xmap) {
   using L = Lay<F16, PROD>;
@@ -660,6 +690,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
       constexpr int HW = 2 * BM + 1;  // b + 1/2 bits: halfwords of a chunk
       uint32_t cw[BM];
       uint32_t hw[MIX ? BM + 1 : 1];  // b + 1/2 bits: the chunk's codes at mixed_pos
+      uint32_t plo[PAIRL ? BM : 1], phi[PAIRL ? BM : 1];  // MSE, PAIR: slots of the pair block
 #pragma unroll
       for (int w = 0; w < (MIX ? BM + 1 : 1); ++w) hw[w] = 0u;
       float g2 = 0.f;
@@ -673,6 +704,16 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
           tmem_ld32_nw(acc + 32 * c0, t32);
           tmem_wait_ld();
           if (flagged) m32 = mix_near_mask<BM>(t32, f, p.thr, p.thr_hi);
+        }
+      } else if constexpr (PAIRL) {
+        bool flagged = false;
+        chunk_codes_pair<BM>(a0, f, p.thr, plo, phi, flagged);
+        m32 = 0u;
+        if (__any_sync(kFull, flagged && live)) {
+          uint32_t t32[32];
+          tmem_ld32_nw(acc + 32 * c0, t32);
+          tmem_wait_ld();
+          if (flagged) m32 = near_mask<BM>(t32, f, p.thr);
         }
       } else {
         // Prod keys take general thresholds too (keeping that branch also
@@ -701,6 +742,8 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
         for (int w = 0; w < BM; ++w) cw[w] = 0u;
 #pragma unroll
         for (int w = 0; w < (MIX ? BM + 1 : 1); ++w) hw[w] = 0u;
+#pragma unroll
+        for (int w = 0; w < (PAIRL ? BM : 1); ++w) plo[w] = phi[w] = 0u;
         m32 = 0u;
         g2 = 0.f;
       }
@@ -723,6 +766,12 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
             const bool hi = (j & 8) == 0;
             const uint32_t code = hi ? bucketize<BM + 1>(vv, cen_s, 0.f, nr) : bucketize<BM>(vv, thr_s, 0.f, nr);
             set_bits_rt(hw, mixed_pos(j, BM), hi ? BM + 1 : BM, code);
+          } else if constexpr (PAIRL) {
+            const uint32_t code = bucketize<BM>(vv, thr_s, 0.f, nr);
+            if (j < 16)
+              set_bits_rt(plo, 2 * j * BM, BM, code);
+            else
+              set_bits_rt(phi, 2 * (j - 16) * BM, BM, code);
           } else {
             const uint32_t code = bucketize<BM>(vv, thr_s, 0.f, nr);
             if constexpr (PROD) {
@@ -735,7 +784,45 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
         }
       }
       // stores of the chunk's codes
-      if (MIX && p.layout == TQ_LAYOUT_TOKEN) {
+      if constexpr (PAIRL) {
+        // PAIR (vectors 2k and 2k+1 share a block; coordinate j's two codes
+        // side by side at block bits 2j·BM, even vector low): the chunk's
+        // block is 2·BM words from word 2·c0·BM; lo holds its first BM words'
+        // fields of this vector, hi the last BM.  When the destination pairs
+        // rows r and r+1 (lanes l and l+1), the even lane writes the first BM
+        // words and the odd lane the rest, after one exchange.
+        const bool odd = (dv & 1) != 0;
+        if (odd) {
+          shift_slot<BM>(plo);
+          shift_slot<BM>(phi);
+        }
+        const int64_t base_row = row - (even ? 0 : 1);
+        const bool whole = p.pair_aligned && base_row + 1 < p.N;
+        uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)p.W) + 2 * c0 * BM;
+        uint32_t ow[BM];
+#pragma unroll
+        for (int w = 0; w < BM; ++w) ow[w] = (even ? plo[w] : phi[w]) | __shfl_xor_sync(kFull, even ? phi[w] : plo[w], 1);
+        if (valid && whole) {
+#pragma unroll
+          for (int w = 0; w < BM; ++w) blk[(even ? 0 : BM) + w] = ow[w];
+        } else if (valid) {
+          // the partner is written by another call (or not at all): this
+          // vector's slots of the 2·BM block words by masked atomics
+          uint32_t m0[BM];
+#pragma unroll
+          for (int w = 0; w < BM; ++w) m0[w] = 0u;
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) put_bits<BM>(m0, 2 * jj * BM, (1u << BM) - 1u);
+          if (odd) shift_slot<BM>(m0);
+#pragma unroll
+          for (int w = 0; w < BM; ++w) {
+            atomicAnd(blk + w, ~m0[w]);
+            atomicOr(blk + w, plo[w]);
+            atomicAnd(blk + BM + w, ~m0[w]);
+            atomicOr(blk + BM + w, phi[w]);
+          }
+        }
+      } else if (MIX && p.layout == TQ_LAYOUT_TOKEN) {
         if (valid) {
           uint16_t* dst = reinterpret_cast<uint16_t*>(p.codes + dv * p.W) + c0 * HW;
 #pragma unroll
@@ -931,9 +1018,9 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
   }
 }
 
-template <int BM, bool PROD, bool F16, bool MIX = false>
+template <int BM, bool PROD, bool F16, bool MIX = false, bool PAIRL = false>
 cudaError_t launch_t(const Enc128Params& p, const CUtensorMap& xmap, cudaStream_t st) {
-  auto k = encode128_kernel<BM, PROD, F16, MIX>;
+  auto k = encode128_kernel<BM, PROD, F16, MIX, PAIRL>;
   static PerDeviceValue attr;  // set once per device, before any stream capture
   const cudaError_t e = smem_attr_once(attr, (const void*)k, Lay<F16, PROD>::SmemAlloc);
   if (e != cudaSuccess) return e;
@@ -959,6 +1046,15 @@ cudaError_t launch_mode(const Enc128Params& p, const CUtensorMap& xmap, int bm, 
       case 1: return launch_t<1, true, F16>(p, xmap, st);
       case 2: return launch_t<2, true, F16>(p, xmap, st);
       case 3: return launch_t<3, true, F16>(p, xmap, st);
+    }
+    return cudaErrorInvalidValue;
+  }
+  if (p.layout == TQ_LAYOUT_PAIR) {  // plain MSE into PAIR caches: its own kernel
+    switch (bm) {
+      case 1: return launch_t<1, false, F16, false, true>(p, xmap, st);
+      case 2: return launch_t<2, false, F16, false, true>(p, xmap, st);
+      case 3: return launch_t<3, false, F16, false, true>(p, xmap, st);
+      case 4: return launch_t<4, false, F16, false, true>(p, xmap, st);
     }
     return cudaErrorInvalidValue;
   }
