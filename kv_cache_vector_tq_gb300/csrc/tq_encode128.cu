@@ -184,6 +184,53 @@ __device__ __forceinline__ uint32_t bucketize_fold(float v, const float (&thr)[1
   return (kAll - above) ^ ((uint32_t)((int32_t)__float_as_uint(v) >> 31) & kAll);
 }
 
+// Positive thresholds of a symmetric BM-bit codebook (one slot at BM = 1).
+template <int BM>
+constexpr int kTB = BM == 1 ? 1 : (1 << (BM - 1)) - 1;
+
+// Symmetric bucketize of an accumulator value x against the positive
+// thresholds tb, already divided by the row's scale (x·scale >= t and x >= tb
+// differ only by roundings far inside the recomputation band): bucketize_fold
+// without the per-coordinate scaling.  (A binary search over tb, with the
+// bracketing thresholds' distances, issued fewer compares but ran slower.)
+template <int BM>
+__device__ __forceinline__ uint32_t bucketize_sc(float x, const float (&tb)[kTB<BM>], float& dmin) {
+  constexpr int H = (1 << (BM - 1)) - 1;
+  constexpr uint32_t kAll = (1u << BM) - 1u;
+  const float a = fabsf(x);
+  dmin = fminf(dmin, a);
+  uint32_t above = 0u;
+#pragma unroll
+  for (int j = 0; j < H; ++j) {
+    const float dj = a - tb[j];
+    dmin = fminf(dmin, fabsf(dj));
+    above += __float_as_uint(dj) >> 31;
+  }
+  return (kAll - above) ^ ((uint32_t)((int32_t)__float_as_uint(x) >> 31) & kAll);
+}
+
+// The row's positive thresholds divided by its scale: tb[j] = t_{H+1+j}·inv.
+template <int BM>
+__device__ __forceinline__ void scaled_thresholds(const float (&thr)[15], float inv, float (&tb)[kTB<BM>]) {
+  constexpr int H = (1 << (BM - 1)) - 1;
+#pragma unroll
+  for (int j = 0; j < kTB<BM>; ++j) tb[j] = BM == 1 ? 0.f : thr[H + 1 + j] * inv;
+}
+
+// One 32-column chunk of plain MSE codes (symmetric codebook) from the raw
+// accumulator: BM code words (coordinate j at bits j·BM), and `flagged` when a
+// coordinate lies within mg (the band in accumulator units) of a threshold.
+template <int BM>
+__device__ __forceinline__ void chunk_codes_s(const uint32_t (&a)[32], const float (&tb)[kTB<BM>], float mg,
+                                              uint32_t (&cw)[BM], bool& flagged) {
+#pragma unroll
+  for (int w = 0; w < BM; ++w) cw[w] = 0u;
+  float dmin = INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) put_bits<BM>(cw, j * BM, bucketize_sc<BM>(__uint_as_float(a[j]), tb, dmin));
+  flagged = dmin < mg;
+}
+
 // Near-threshold flags of a chunk (symmetric codebook), bit j for coordinate j.
 template <int BM>
 __device__ __forceinline__ uint32_t near_mask(const uint32_t (&a)[32], float f, const float (&thr)[15]) {
@@ -247,19 +294,19 @@ __device__ __forceinline__ uint32_t chunk_codes(const uint32_t (&a)[32], float f
 // compile-time positions; a coordinate near a threshold anywhere in the chunk
 // sets `flagged`.
 template <int BM>
-__device__ __forceinline__ void mix_chunk_codes(const uint32_t (&a)[32], float f, const float (&tlo)[15],
-                                                const float (&thi)[15], uint32_t (&hw)[BM + 1],
+__device__ __forceinline__ void mix_chunk_codes(const uint32_t (&a)[32], const float (&tlo)[kTB<BM>],
+                                                const float (&thi)[kTB<BM + 1>], float mg, uint32_t (&hw)[BM + 1],
                                                 bool& flagged) {
   float dmin = INFINITY;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    const float v = __uint_as_float(a[j]) * f;
+    const float x = __uint_as_float(a[j]);
     if ((j & 8) == 0)
-      put_bits<BM + 1>(hw, mixed_pos(j, BM), bucketize_fold<BM + 1>(v, thi, dmin));
+      put_bits<BM + 1>(hw, mixed_pos(j, BM), bucketize_sc<BM + 1>(x, thi, dmin));
     else
-      put_bits<BM>(hw, mixed_pos(j, BM), bucketize_fold<BM>(v, tlo, dmin));
+      put_bits<BM>(hw, mixed_pos(j, BM), bucketize_sc<BM>(x, tlo, dmin));
   }
-  flagged = dmin < kMargin;
+  flagged = dmin < mg;
 }
 
 // Near-threshold flags of a b + 1/2-bit chunk, each coordinate against its own codebook.
@@ -285,20 +332,20 @@ __device__ __forceinline__ uint32_t mix_near_mask(const uint32_t (&a)[32], float
 // 2(j mod 16)·BM of lo (j < 16) or hi (j >= 16), so that a row pair's block
 // words are one exchange and an OR away (an odd vector shifts by BM first).
 template <int BM>
-__device__ __forceinline__ void chunk_codes_pair(const uint32_t (&a)[32], float f, const float (&thr)[15],
+__device__ __forceinline__ void chunk_codes_pair(const uint32_t (&a)[32], const float (&tb)[kTB<BM>], float mg,
                                                  uint32_t (&lo)[BM], uint32_t (&hi)[BM], bool& flagged) {
 #pragma unroll
   for (int w = 0; w < BM; ++w) lo[w] = hi[w] = 0u;
   float dmin = INFINITY;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    const uint32_t code = bucketize_fold<BM>(__uint_as_float(a[j]) * f, thr, dmin);
+    const uint32_t code = bucketize_sc<BM>(__uint_as_float(a[j]), tb, dmin);
     if (j < 16)
       put_bits<BM>(lo, 2 * j * BM, code);
     else
       put_bits<BM>(hi, 2 * (j - 16) * BM, code);
   }
-  flagged = dmin < kMargin;
+  flagged = dmin < mg;
 }
 
 // Words x << BM (BM < 32) of a BM-word array, the top field leaving nothing behind
@@ -676,6 +723,10 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
       // recomputation band, and fp64 arithmetic is slow on this part
       const float f = s > 0.f ? p.sqrt_df / (s * sc * p.pi_scale) : 0.f;
       const bool live = valid && s > 0.f;
+      // plain MSE and b + 1/2 bits compare the accumulator itself with the
+      // thresholds divided by the row's scale 1/f, and the band with kMargin/f
+      const float inv = s * sc * p.pi_scale / p.sqrt_df;
+      const float mg = kMargin * inv;
       const int64_t dv = valid ? dest_row(p, row) : 0;
       if (!__all_sync(kFull, bar_wait(&acc_full[ab], par, abort_flag, p.status, lim))) break;
       tc_fence_after();
@@ -697,7 +748,10 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
       uint32_t m32;
       if constexpr (MIX) {
         bool flagged = false;
-        mix_chunk_codes<BM>(a0, f, p.thr, p.thr_hi, hw, flagged);
+        float tlo[kTB<BM>], thi[kTB<BM + 1>];
+        scaled_thresholds<BM>(p.thr, inv, tlo);
+        scaled_thresholds<BM + 1>(p.thr_hi, inv, thi);
+        mix_chunk_codes<BM>(a0, tlo, thi, mg, hw, flagged);
         m32 = 0u;
         if (__any_sync(kFull, flagged && live)) {  // rare: the flags, from tensor memory again
           uint32_t t32[32];
@@ -707,7 +761,9 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
         }
       } else if constexpr (PAIRL) {
         bool flagged = false;
-        chunk_codes_pair<BM>(a0, f, p.thr, plo, phi, flagged);
+        float tb[kTB<BM>];
+        scaled_thresholds<BM>(p.thr, inv, tb);
+        chunk_codes_pair<BM>(a0, tb, mg, plo, phi, flagged);
         m32 = 0u;
         if (__any_sync(kFull, flagged && live)) {
           uint32_t t32[32];
@@ -719,10 +775,16 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
         // Prod keys take general thresholds too (keeping that branch also
         // schedules the Prod epilogue better: 2.57 -> 2.95 Gvec/s measured)
         bool flagged = false;
-        if (PROD && !p.sym)
+        if constexpr (!PROD) {
+          float tb[kTB<BM>];
+          scaled_thresholds<BM>(p.thr, inv, tb);
+          chunk_codes_s<BM>(a0, tb, mg, cw, flagged);
+          m32 = 0u;
+        } else if (!p.sym) {
           m32 = chunk_codes<BM, false, PROD>(a0, f, p.thr, cen_s, cw, g2, flagged);
-        else
+        } else {
           m32 = chunk_codes<BM, true, PROD>(a0, f, p.thr, cen_s, cw, g2, flagged);
+        }
         // a chunk with a coordinate near a threshold (~1e-3 of them): its
         // values again from tensor memory (not yet handed back), then the flags
         if (__any_sync(kFull, flagged && live)) {
