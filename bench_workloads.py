@@ -92,14 +92,24 @@ def traffic(root, key):
     return None
 
 
-def _timed(fn, steps, warmup, stream, clocks_cls, local, flush=None):
+def _timed(fn, steps, warmup, stream, clocks_cls, local, flush=None, graph=False):
     """W warm-up calls, then K timed calls bracketed by events on `stream`.
-    With `flush`, L2 is flushed between calls and only the calls are timed."""
+    With `flush`, L2 is flushed between calls and only the calls are timed.
+    With `graph`, one call is captured as a CUDA graph after the warm-up and
+    the timed calls replay it (no host launch gaps between calls)."""
     import torch
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             fn()
     torch.cuda.synchronize()
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        fn = g.replay
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
     clocks = clocks_cls(local)
     clocks.start()
     time.sleep(0.2)
@@ -159,7 +169,7 @@ def run_encode(args, world, rank, local, root, clocks_cls, cpu):
     cs = tq.CodeSet(ctx, N, tq.TQ_LAYOUT_TOKEN)
     stream = torch.cuda.Stream()
     total_ms, clk = _timed(lambda: tq.tq_encode(ctx, x, cs, stream=stream), args.steps, args.warmup, stream,
-                           clocks_cls, local)
+                           clocks_cls, local, graph=True)
     assert ctx.poll() == tq.TQ_OK
     sec = total_ms * 1e-3
     mvec = world * args.steps * N / sec / 1e6
@@ -212,7 +222,7 @@ def run_encode(args, world, rank, local, root, clocks_cls, cpu):
                  "synthetic (device-generated N(0,1) fp32 rows, a seeded 1% x50)",
                  {"workload": f"bulk indexing encode, TurboQuant_MSE b=4, d={d}, N={N}, {rot} rotation",
                   "d": d, "rows": N, "bits": bits, "rotation": rot,
-                  "l2": f"inputs larger than L2: {N * d * 4 / 1e9:.2f} GB of rows per step"},
+                  "timing": "CUDA graph of one call, replayed per step", "l2": f"inputs larger than L2: {N * d * 4 / 1e9:.2f} GB of rows per step"},
                  roof, e2e, args.steps * launches, clk)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu["encode"](d, bits, rot, rotm)
@@ -246,7 +256,7 @@ def run_prefill(args, world, rank, local, root, clocks_cls, cpu):
         tq.tq_encode(ctx, kv[0], K, 0, SEQ, SEQ, stream=stream)
         tq.tq_encode(ctx, kv[1], V, 0, SEQ, SEQ, stream=stream)
 
-    total_ms, clk = _timed(prefill, args.steps, args.warmup, stream, clocks_cls, local)
+    total_ms, clk = _timed(prefill, args.steps, args.warmup, stream, clocks_cls, local, graph=True)
     assert ctx.poll() == tq.TQ_OK
     nvec = 2 * HKV * SEQ
     sec = total_ms * 1e-3
@@ -269,7 +279,7 @@ def run_prefill(args, world, rank, local, root, clocks_cls, cpu):
     keys /= keys.norm(dim=1, keepdim=True)
     cs = tq.CodeSet(pctx, NK, tq.TQ_LAYOUT_TOKEN)
     pms, _ = _timed(lambda: tq.tq_encode(pctx, keys, cs, stream=stream), args.steps, args.warmup, stream,
-                    clocks_cls, local)
+                    clocks_cls, local, graph=True)
     assert pctx.poll() == tq.TQ_OK
     psec = pms * 1e-3
     pbpv = 4 * d + 2 * d // 8 + d // 8 + 8       # fp32 row in; 2-bit codes, sign words, s and γ out
@@ -288,7 +298,7 @@ def run_prefill(args, world, rank, local, root, clocks_cls, cpu):
                  "synthetic (device-generated N(0,1) fp16 K/V, channels 0-3 x10; unit-norm Gaussian keys)",
                  {"workload": "prefill encode of one long-context layer: K and V of 8 KV heads x 131072 tokens, "
                               "d=128, TurboQuant_MSE b=3 (K TOKEN, V PAIR layout)",
-                  "vectors": nvec, "l2": f"inputs larger than L2: {nvec * 2 * d / 1e9:.2f} GB of rows per call",
+                  "vectors": nvec, "timing": "CUDA graph of one call, replayed per step", "l2": f"inputs larger than L2: {nvec * 2 * d / 1e9:.2f} GB of rows per call",
                   "prod_encode": prod},
                  roof, None, args.steps * 2, clk)
     return line if rank == 0 else None
@@ -317,7 +327,7 @@ def run_scores(args, world, rank, local, root, clocks_cls, cpu):
     ws = torch.empty(max(tq.tq_scores_workspace_size(ctx, M) // 4, 4), dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
     total_ms, clk = _timed(lambda: tq.tq_scores(ctx, q, cs, out, ws, stream=stream), args.steps, args.warmup,
-                           stream, clocks_cls, local)
+                           stream, clocks_cls, local, graph=True)
     assert ctx.poll() == tq.TQ_OK
     sec = total_ms * 1e-3
     pairs = world * args.steps * M * N / sec
@@ -345,7 +355,7 @@ def run_scores(args, world, rank, local, root, clocks_cls, cpu):
                  "u2 codes + 1-bit QJL, f16 operands, f32 accumulate",
                  "synthetic (device-generated unit-norm Gaussian keys; seeded N(0,1) queries and S)",
                  {"workload": "TurboQuant_Prod b=3 scores, d=128, 1M keys x 64 queries", "keys": N, "queries": M,
-                  "l2": f"inputs larger than L2: {bytes_call / 1e6:.0f} MB moved per call"},
+                  "timing": "CUDA graph of one call, replayed per step", "l2": f"inputs larger than L2: {bytes_call / 1e6:.0f} MB moved per call"},
                  roof, e2e, args.steps, clk)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu["scores"](tq, cs, q, G, S)
