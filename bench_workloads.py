@@ -177,9 +177,10 @@ def run_encode(args, world, rank, local, root, clocks_cls, cpu):
     bytes_per_vec = 4 * d + d * bits // 8 + 4
     if rot == "hadamard" or d == 128:
         # the Hadamard kernel, and the d = 128 tensor-memory kernel on fp32 rows
-        # (three 32.8 KFLOP products per 580 B: the bytes bind first), are HBM-bound
-        kern = "encode_wht_kernel" if rot == "hadamard" else "encode128_kernel"
-        key = f"encode_wht_d{d}_n{N // 1000}k" if rot == "hadamard" else f"encode128_f32_n{N // 1000}k"
+        # (three 32.8 KFLOP products per 580 B: the bytes bind first; it also
+        # serves d = 128 Hadamard contexts, with H·D/√d as its matrix), are HBM-bound
+        kern = "encode128_kernel" if d == 128 else "encode_wht_kernel"
+        key = f"encode128_f32_n{N // 1000}k" if d == 128 else f"encode_wht_d{d}_n{N // 1000}k"
         ach = args.steps * N * bytes_per_vec / sec / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
                 "traffic": traffic(root, key), "kernel": kern, "peak_kind": kind,

@@ -739,7 +739,10 @@ tq_status tq_encode(const tq_ctx* ctx, const void* d_x, int x_dtype, int64_t N,
   if (st != TQ_OK) return st;
   if (N == 0) return TQ_OK;
   if (!d_x || !al16(d_x)) return TQ_ERR_INVALID_ARG;
-  const bool wht = wht_supported(v) && out->layout == TQ_LAYOUT_TOKEN;
+  // d = 128 takes the tensor-memory encoder for every rotation: the product
+  // with the materialized H·D/√d costs it nothing (its epilogue bounds it),
+  // and it ran faster than the butterflies of the fast transform
+  const bool wht = wht_supported(v) && out->layout == TQ_LAYOUT_TOKEN && !enc128_supported(v);
   const bool wide = !wht && v.d > kChunk;
   if (wide && (!umma_supported(v) || out->layout != TQ_LAYOUT_TOKEN)) return TQ_ERR_UNSUPPORTED;
   // every destination index must lie inside the code set

@@ -82,7 +82,8 @@ def check_rows(cs, Pi, Xs, rows, b, all_rows=False):
 @pytest.mark.parametrize("d", [32, 64, 128, 256, 384, 768, 1536, 3072])
 @pytest.mark.parametrize("b", [1, 2, 3, 4])
 def test_hadamard_fast_transform(d, b):
-    """Orders 2^k and 12·2^k with 32 <= 2^k <= 256 run the fast transform."""
+    """Orders 2^k and 12·2^k with 32 <= 2^k <= 256 run the fast transform
+    (d = 128: the tensor-memory encoder with the materialized H·D/√d)."""
     n = 257 if d <= 384 else 96
     ctx, Pi = hadamard_pair(7, d, b)
     X = synth.bulk_rows(7, n, d)
