@@ -630,7 +630,9 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
             }
           }
       } else {
-#pragma unroll
+        // fp32 rows: one box per trip (the prep code shares each SMSP's
+        // instruction cache with the epilogue's)
+#pragma unroll 1
         for (int bx = 0; bx < 4; ++bx)
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -682,7 +684,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
         const uint32_t as = i % L::AStages;
         if (!__all_sync(kFull, bar_wait(&a_empty[as], ((i / L::AStages) & 1u) ^ 1u, abort_flag, p.status, lim))) break;
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int bx = 0; bx < 4; ++bx) {  // 32 coordinates per box
           uint32_t hi[16], lo[16];
 #pragma unroll
@@ -731,9 +733,14 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
       if (!__all_sync(kFull, bar_wait(&acc_full[ab], par, abort_flag, p.status, lim))) break;
       tc_fence_after();
       const uint32_t acc = tmem + lane_base + L::ColAcc + ab * 128;
-      uint32_t a0[32];
-      tmem_ld32_nw(acc + 32 * c0, a0);
-      tmem_wait_ld();
+      // b = 4 plain MSE: eight columns per trip of a rolled loop (the unrolled
+      // 32-column bucketize overflows the instruction cache at 7 thresholds)
+      constexpr bool kGroups = !PROD && !MIX && !PAIRL && BM == 4;
+      uint32_t a0[kGroups ? 1 : 32];
+      if constexpr (!kGroups) {
+        tmem_ld32_nw(acc + 32 * c0, a0);
+        tmem_wait_ld();
+      }
       // a3/a4 on the warp's 32-coordinate chunk c0: bucketize, flag, pack
       // (MSE and Prod: BM words, words [c0·BM, c0·BM + BM) of the row's
       // stream; b + 1/2 bits: 2·BM + 1 halfwords from halfword c0·(2·BM + 1)),
@@ -775,7 +782,26 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
         // Prod keys take general thresholds too (keeping that branch also
         // schedules the Prod epilogue better: 2.57 -> 2.95 Gvec/s measured)
         bool flagged = false;
-        if constexpr (!PROD) {
+        if constexpr (kGroups) {
+          float tb[kTB<BM>];
+          scaled_thresholds<BM>(p.thr, inv, tb);
+          float dmin = INFINITY;
+#pragma unroll
+          for (int w = 0; w < BM; ++w) cw[w] = 0u;
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) {
+            uint32_t a8[8];
+            tmem_ld8_nw(acc + 32 * c0 + 8 * k, a8);
+            tmem_wait_ld();
+            uint32_t wd = 0u;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) wd |= bucketize_sc<BM>(__uint_as_float(a8[jj]), tb, dmin) << (4 * jj);
+#pragma unroll
+            for (int w = 0; w < BM; ++w) cw[w] = w == k ? wd : cw[w];
+          }
+          flagged = dmin < mg;
+          m32 = 0u;
+        } else if constexpr (!PROD) {
           float tb[kTB<BM>];
           scaled_thresholds<BM>(p.thr, inv, tb);
           chunk_codes_s<BM>(a0, tb, mg, cw, flagged);
