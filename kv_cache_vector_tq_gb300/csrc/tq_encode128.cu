@@ -779,8 +779,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
           if (flagged) m32 = near_mask<BM>(t32, f, p.thr);
         }
       } else {
-        // Prod keys take general thresholds too (keeping that branch also
-        // schedules the Prod epilogue better: 2.57 -> 2.95 Gvec/s measured)
         bool flagged = false;
         if constexpr (kGroups) {
           float tb[kTB<BM>];
@@ -806,8 +804,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
           scaled_thresholds<BM>(p.thr, inv, tb);
           chunk_codes_s<BM>(a0, tb, mg, cw, flagged);
           m32 = 0u;
-        } else if (!p.sym) {
-          m32 = chunk_codes<BM, false, PROD>(a0, f, p.thr, cen_s, cw, g2, flagged);
         } else {
           m32 = chunk_codes<BM, true, PROD>(a0, f, p.thr, cen_s, cw, g2, flagged);
         }
@@ -1158,10 +1154,10 @@ cudaError_t launch_mode(const Enc128Params& p, const CUtensorMap& xmap, int bm, 
 }  // namespace
 
 bool enc128_supported(const DevCtx& c) {
-  // MSE and b + 1/2 bits: symmetric codebooks only (tq_codebook_build makes
-  // them; the bucketize compares |v| with the positive thresholds)
+  // symmetric codebooks only (tq_codebook_build makes them; the bucketize
+  // compares |v| with the positive thresholds); others take the general encoder
   return c.d == kDim && c.enc_tab != nullptr && (c.mode != TQ_PROD || c.enc_tab_m != nullptr) &&
-         c.b_mse >= 1 && c.b_mse <= (c.mode == TQ_MSE ? 4 : 3) && (c.sym_thr != 0 || c.mode == TQ_PROD);
+         c.b_mse >= 1 && c.b_mse <= (c.mode == TQ_MSE ? 4 : 3) && c.sym_thr != 0;
 }
 
 tq_status launch_encode128(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,

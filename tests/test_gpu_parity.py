@@ -227,6 +227,53 @@ def test_encode_prod_config3_sample():
     np.testing.assert_allclose(g[rows_ok], e["gamma"][rows_ok], rtol=1e-5, atol=1e-7)
 
 
+def _shifted_codebook(d, bm):
+    """A codebook that is not symmetric about 0: the Lloyd-Max centroids moved
+    by 0.02..0.08, thresholds at the new midpoints (the nearest-centroid rule,
+    "TurboQuant 详解", section "痛点 2")."""
+    cb = tq.tq_codebook_build(d, bm)
+    K = 1 << bm
+    c = np.array([cb.centroid[k] for k in range(K)]) + 0.02 + 0.06 * np.arange(K) / K
+    for k in range(K):
+        cb.centroid[k] = float(c[k])
+    for k in range(K - 1):
+        cb.threshold[k] = float(0.5 * (c[k] + c[k + 1]))
+    return cb, c
+
+
+@pytest.mark.parametrize("mode", [tq.TQ_MSE, tq.TQ_PROD])
+def test_encode_nonsymmetric_codebook(mode):
+    """A caller's codebook without the ± symmetry (d = 128, b = 3): the codes
+    still follow the nearest-centroid rule and (Prod) the QJL stage."""
+    d, b, N = 128, 3, 3000
+    bm = b - 1 if mode == tq.TQ_PROD else b
+    cb, cen = _shifted_codebook(d, bm)
+    S = synth.qjl_matrix(4, d) if mode == tq.TQ_PROD else None
+    G = synth.gaussian_matrix(4, d)
+    ctx = tq.Context(d, b, mode, tq.TQ_ROT_DENSE, tq.tq_rotation_haar(G), S, codebook=cb)
+    Pi = orot.haar_rotation(G)
+    X = synth.unit_rows(4, N, d) if mode == tq.TQ_PROD else synth.gaussian_rows(4, N, d, outlier_cols=4,
+                                                                                  outlier_scale=10.0)
+    cs = gpu_encode(ctx, X)
+    if mode == tq.TQ_MSE:
+        idx_ref, s_ref, v = oq.mse_quantize(X.astype(np.float64), Pi, cen, math.sqrt(d))
+        band = oq.near_threshold(v, cen)
+        idx = tq.tq_unpack_indices(cs, 0, N).astype(np.int64)
+        assert not ((idx != idx_ref) & ~band).any()
+        np.testing.assert_allclose(cs.norm[:N].cpu().numpy(), s_ref, rtol=1e-6)
+    else:
+        e = oq.prod_quantize(X.astype(np.float64), Pi, S, cen, math.sqrt(d))
+        band = oq.near_threshold(e["v"], cen)
+        idx, bits = tq.tq_unpack_indices(cs, 0, N, with_bits=True)
+        assert not ((idx.astype(np.int64) != e["idx"]) & ~band).any()
+        rows_ok = (idx.astype(np.int64) == e["idx"]).all(axis=1)
+        qband = oq.qjl_near_zero(e["p"], e["gamma"], S)
+        assert not ((bits.astype(np.int64) != e["bits"]) & ~qband & rows_ok[:, None]).any()
+        g = cs.rnorm[:N].cpu().numpy().astype(np.float64)
+        np.testing.assert_allclose(g[rows_ok], e["gamma"][rows_ok], rtol=1e-5, atol=1e-7)
+    assert band.mean() <= BAND_FRAC_MAX
+
+
 # ------------------------------------------------------------------ scores
 def _scores_check(ctx, Pi, S, X, Q, b_mse, prod):
     d = X.shape[1]
