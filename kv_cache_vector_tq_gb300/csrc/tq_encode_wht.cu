@@ -325,8 +325,11 @@ bool wht_supported(const DevCtx& c) {
          c.had_m <= 256 && (c.had_p == 1 || c.had_p == 12);
 }
 
+// prime: only the one-time setup (shared-memory limit, CTAs per SM) of both
+// input types, done when the context is created so that no launch, captured
+// into a graph or not, depends on when the first one ran
 template <int BM, int P, int E>
-static cudaError_t launch_wht_t(const WhtParams& p, bool f16, cudaStream_t st) {
+static cudaError_t launch_wht_t(const WhtParams& p, bool f16, cudaStream_t st, bool prime = false) {
   constexpr int NW = P == 12 ? 12 : 8, VPC = P == 12 ? 1 : 8, D = P * 32 * E;
   const int64_t ctas = (p.N + VPC - 1) / VPC;
   const size_t smem = (size_t)(P == 12 ? D : 0) * 4 + 32 * 4 + (size_t)((VPC * D + 15) / 16) * 16 +
@@ -335,10 +338,15 @@ static cudaError_t launch_wht_t(const WhtParams& p, bool f16, cudaStream_t st) {
   // before any stream capture: every CTA of the grid strides over the rows
   // with an equal share, so the grid must fit in one wave
   static PerDeviceValue attr[2], per_sm[2];  // once per device
+  if (prime && !f16) {
+    const cudaError_t e16 = launch_wht_t<BM, P, E>(p, true, st, true);
+    if (e16 != cudaSuccess) return e16;
+  }
   const void* kf = f16 ? (const void*)encode_wht_kernel<BM, P, E, true> : (const void*)encode_wht_kernel<BM, P, E, false>;
   const cudaError_t e = smem_attr_once(attr[f16 ? 1 : 0], kf, 160 * 1024);
   if (e != cudaSuccess) return e;
   const int resident = ctas_per_sm_once(per_sm[f16 ? 1 : 0], kf, NW * 32, smem);
+  if (prime) return cudaSuccess;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * resident));
   if (f16)
     encode_wht_kernel<BM, P, E, true><<<grid, NW * 32, smem, st>>>(p);
@@ -348,19 +356,34 @@ static cudaError_t launch_wht_t(const WhtParams& p, bool f16, cudaStream_t st) {
 }
 
 template <int BM, int P>
-static cudaError_t launch_wht_e(const WhtParams& p, bool f16, cudaStream_t st) {
+static cudaError_t launch_wht_e(const WhtParams& p, bool f16, cudaStream_t st, bool prime) {
   switch (p.m) {
-    case 32: return launch_wht_t<BM, P, 1>(p, f16, st);
-    case 64: return launch_wht_t<BM, P, 2>(p, f16, st);
-    case 128: return launch_wht_t<BM, P, 4>(p, f16, st);
-    case 256: return launch_wht_t<BM, P, 8>(p, f16, st);
+    case 32: return launch_wht_t<BM, P, 1>(p, f16, st, prime);
+    case 64: return launch_wht_t<BM, P, 2>(p, f16, st, prime);
+    case 128: return launch_wht_t<BM, P, 4>(p, f16, st, prime);
+    case 256: return launch_wht_t<BM, P, 8>(p, f16, st, prime);
   }
   return cudaErrorInvalidValue;
 }
 
 template <int BM>
-static cudaError_t launch_wht_b(const WhtParams& p, int P, bool f16, cudaStream_t st) {
-  return P == 12 ? launch_wht_e<BM, 12>(p, f16, st) : launch_wht_e<BM, 1>(p, f16, st);
+static cudaError_t launch_wht_b(const WhtParams& p, int P, bool f16, cudaStream_t st, bool prime = false) {
+  return P == 12 ? launch_wht_e<BM, 12>(p, f16, st, prime) : launch_wht_e<BM, 1>(p, f16, st, prime);
+}
+
+tq_status prime_encode_wht(const DevCtx& c) {
+  if (!wht_supported(c)) return TQ_OK;
+  WhtParams p{};
+  p.m = c.had_m;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (c.b_mse) {
+    case 1: e = launch_wht_b<1>(p, c.had_p, false, nullptr, true); break;
+    case 2: e = launch_wht_b<2>(p, c.had_p, false, nullptr, true); break;
+    case 3: e = launch_wht_b<3>(p, c.had_p, false, nullptr, true); break;
+    case 4: e = launch_wht_b<4>(p, c.had_p, false, nullptr, true); break;
+    default: return TQ_OK;
+  }
+  return e == cudaSuccess ? TQ_OK : set_cuda_error(e);
 }
 
 tq_status launch_encode_wht(const DevCtx& c, const void* x, int x_dtype, int64_t N, const tq_codes* out,

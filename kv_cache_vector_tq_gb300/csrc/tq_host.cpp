@@ -670,6 +670,10 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   v.lut = (const uint32_t*)(base + o_lut);
   v.lut_hi = mixed ? (const uint32_t*)(base + o_lh) : nullptr;
   v.status = (int*)(base + o_st);
+  // the fast transform's one-time launch setup now, outside any stream capture
+  // (its launches then depend on nothing done before them; a failure here
+  // shows again, and is reported, at the first encode)
+  if (d != kChunk) (void)prime_encode_wht(v);
   *out = reinterpret_cast<tq_ctx*>(c);
   return TQ_OK;
 }

@@ -125,5 +125,7 @@ cudaError_t smem_attr_once(PerDeviceValue& flag, const void* func, int bytes);
 // dynamic shared memory, on the current device (cached per device in `cache`;
 // 1 if the runtime cannot tell).
 int ctas_per_sm_once(PerDeviceValue& cache, const void* func, int threads, size_t smem);
+// One-time launch setup of the Hadamard fast transform for a context's shapes.
+tq_status prime_encode_wht(const DevCtx& c);
 
 }  // namespace tq
