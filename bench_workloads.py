@@ -463,7 +463,8 @@ def run_keys(args, world, rank, local, root, clocks_cls, cpu):
         tq.tq_encode(ctx, x, cs, stream=stream)
         tq.tq_scores(ctx, q, cs, out, ws, stream=stream)
 
-    total_ms, clk = _timed(call, args.steps, args.warmup, stream, clocks_cls, local, flush=flush_buf.zero_)
+    total_ms, clk = _timed(call, args.steps, args.warmup, stream, clocks_cls, local, flush=flush_buf.zero_,
+                           graph=True)
     assert ctx.poll() == tq.TQ_OK
     sec = total_ms * 1e-3
     mvec = world * args.steps * N / sec / 1e6
@@ -474,7 +475,8 @@ def run_keys(args, world, rank, local, root, clocks_cls, cpu):
                  "f32 in, u3 codes, f16 hi/lo tensor products, f32 accumulate",
                  "synthetic (seeded N(0,1) fp32 keys, channels 0-3 x20; N(0,1) query)",
                  {"workload": "TurboQuant_MSE b=3, d=128: encode 4096 keys, then score 1 query against them",
-                  "keys": N, "l2": "L2 flushed (256 MB write) before every timed call",
+                  "keys": N, "timing": "CUDA graph of one encode + score, replayed per step",
+                  "l2": "L2 flushed (256 MB write) before every timed call",
                   "us_per_encode_plus_score": round(total_ms / args.steps * 1e3, 2)},
                  {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
                   "traffic": None, "kernel": "encode128_kernel + scores_kernel (latency-bound at this size)",

@@ -356,6 +356,48 @@ def test_scores_key_ranges_and_query_counts(first, N, M, prod):
     assert (np.abs(got - ref) <= bound).all()
 
 
+@pytest.mark.parametrize("b,M,prod,first,N", [
+    (1, 1, False, 0, 4096), (2, 5, False, 3, 777), (3, 1, False, 0, 30001), (3, 8, False, 0, 9000),
+    (4, 2, False, 11, 129), (2, 1, True, 0, 4096), (3, 8, True, 5, 1001), (4, 3, True, 0, 65),
+    (3, 9, False, 0, 300),  # one query past the small path: the tensor-core scorer
+    (3, 1, False, 0, 40000),  # more keys than the small path takes
+])
+def test_scores_small_query_counts(b, M, prod, first, N):
+    """Up to 8 queries over up to ~10^5/(M + 2) keys take the one-launch scorer
+    (each CTA rotates the queries, four threads per key): every bit width, MSE
+    and Prod, key ranges with an offset, ragged key counts, more keys than one
+    pass of its grid; and both sides of its limits."""
+    d = 128
+    mode = tq.TQ_PROD if prod else tq.TQ_MSE
+    ctx, Pi, S = make_pair(31 + b, d, b, mode)
+    total = first + N + 7
+    X = synth.unit_rows(31, total, d) if prod else synth.gaussian_rows(31, total, d, outlier_cols=4,
+                                                                       outlier_scale=20.0)
+    cs = gpu_encode(ctx, X)
+    Q = synth.queries(31, M, d)
+    q = torch.from_numpy(np.ascontiguousarray(Q)).cuda()
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(tq.tq_scores_workspace_size(ctx, M) // 4 + 4, dtype=torch.float32, device="cuda")
+    tq.tq_scores(ctx, q, cs, out, ws, first=first, N=N)
+    torch.cuda.synchronize()
+    assert ctx.poll() == tq.TQ_OK
+    b_mse = b - 1 if prod else b
+    cb = oracle_codebook(d, b_mse)
+    s = cs.norm[first:first + N].cpu().numpy().astype(np.float64)
+    if prod:
+        idx, bits = tq.tq_unpack_indices(cs, first, N, with_bits=True)
+        gam = cs.rnorm[first:first + N].cpu().numpy().astype(np.float64)
+        ref = oatt.prod_scores(Q.astype(np.float64), idx, s, bits, gam, Pi, S, cb["centroids"], math.sqrt(d))
+    else:
+        idx = tq.tq_unpack_indices(cs, first, N)
+        ref = oatt.mse_scores(Q.astype(np.float64), idx, s, Pi, cb["centroids"], math.sqrt(d))
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    Xs = X[first:first + N].astype(np.float64)
+    bound = 1e-4 * np.linalg.norm(Q, axis=1)[:, None] * np.linalg.norm(Xs, axis=1)[None, :]
+    assert (np.abs(got - ref) <= bound).all(), f"max err/bound {np.max(np.abs(got - ref) / bound)}"
+
+
 def test_scores_prod_config3_sample():
     ctx, Pi, S = make_pair(0, 128, 3, tq.TQ_PROD)
     X = synth.unit_rows(0, 8192, 128)
