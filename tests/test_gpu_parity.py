@@ -176,6 +176,33 @@ def test_encode_fp16_kv_token_and_pair_layouts(b):
             np.testing.assert_array_equal(words[ok], oq.pack_codes(inter[ok], b))
 
 
+@pytest.mark.parametrize("b", [1, 2, 3, 4])
+@pytest.mark.parametrize("f16", [False, True])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_encode_pair_layout_widths_and_offsets(b, f16, offset):
+    """PAIR layout at every width, fp32 and fp16 rows: an odd row count (the
+    last pair block half written) at an even offset (row pairs fill whole
+    blocks) and at an odd one (every row shares its block with a row written by
+    no one: masked writes).  Slots this call does not own keep what was there
+    (the code set starts as all ones)."""
+    d, N = 128, 301
+    ctx, Pi, _ = make_pair(40 + b, d, b)
+    X = synth.gaussian_rows(40 + b, N, d, outlier_cols=4, outlier_scale=10.0)
+    if f16:
+        X = X.astype(np.float16)
+    cs = tq.CodeSet(ctx, N + offset + 1, tq.TQ_LAYOUT_PAIR)
+    cs.codes.fill_(-1)
+    tq.tq_encode(ctx, torch.from_numpy(np.ascontiguousarray(X)).cuda(), cs, offset=offset)
+    torch.cuda.synchronize()
+    assert ctx.poll() == tq.TQ_OK
+    check_mse_encode(ctx, Pi, X.astype(np.float32), b, cs, first=offset)
+    full = (1 << b) - 1
+    untouched = [0] if offset else []
+    untouched += [N + offset]
+    for v in untouched:
+        assert (tq.tq_unpack_indices(cs, v, 1) == full).all()
+
+
 def test_encode_append_mapping_pair_layout():
     """Cache append: one token per (batch, head) block at position t (odd and
     even), written next to tokens encoded earlier into the same pair blocks."""
