@@ -16,8 +16,11 @@ each.  Timed steps replay a CUDA graph of one benchmark step.
 
 value    = algorithmic decode bytes / s (codes + norms of K and V for all cached
            tokens, query, output, and the appended token) over the timed steps.
-e2e      = the same metric with the step inputs (query, new K/V token) copied
-           from pinned host memory and the output copied back every decode step.
+e2e      = the same metric with the step inputs (query, new K/V token: one
+           pinned host block, one copy) copied from pinned host memory and the
+           output copied back every decode step; the replicas alternate between
+           two streams with their own buffers, so one replica's copies overlap
+           another's decode.
 roofline = one decode-attention call alone (the same kernel without the
            append: query rotation, tiles and merge in one launch) against the
            measured HBM copy peak; traffic = its DRAM bytes per launch from the
@@ -183,10 +186,17 @@ def build_replicas(tq, synth, bits, R):
         Kr.codes.copy_(K0.codes), Kr.norm.copy_(K0.norm)
         Vr.codes.copy_(V0.codes), Vr.norm.copy_(V0.norm)
         reps.append((Kr, Vr))
-    knew = torch.from_numpy(np.ascontiguousarray(Kh[:, :, SEQ - 1].reshape(-1, D))).cuda()
-    vnew = torch.from_numpy(np.ascontiguousarray(Vh[:, :, SEQ - 1].reshape(-1, D))).cuda()
-    q = torch.from_numpy(synth.queries(0, B * HQ, D).reshape(B, HQ, D)).to(torch.float16).cuda()
-    return ctx, reps, cap, knew, vnew, q
+    # the step's inputs (query, new K, new V; fp16) as views of one buffer, so
+    # that an end-to-end step moves them from the host in one copy
+    nq, nk = B * HQ * D, B * HKV * D
+    inputs = torch.empty(nq + 2 * nk, dtype=torch.float16, device="cuda")
+    q = inputs[:nq].view(B, HQ, D)
+    knew = inputs[nq:nq + nk].view(-1, D)
+    vnew = inputs[nq + nk:].view(-1, D)
+    q.copy_(torch.from_numpy(synth.queries(0, B * HQ, D).reshape(B, HQ, D)).to(torch.float16))
+    knew.copy_(torch.from_numpy(np.ascontiguousarray(Kh[:, :, SEQ - 1].reshape(-1, D))))
+    vnew.copy_(torch.from_numpy(np.ascontiguousarray(Vh[:, :, SEQ - 1].reshape(-1, D))))
+    return ctx, reps, cap, knew, vnew, q, inputs
 
 
 def run_tq(args, world, rank, local):
@@ -202,18 +212,19 @@ def run_tq(args, world, rank, local):
     step_bytes, attn_bytes = decode_bytes(bits)
     cache_bytes = B * HKV * SEQ * 2 * (D * bits // 8 + 4)
     R = max(2, int(math.ceil(4 * L2_BYTES / cache_bytes)))
-    ctx, reps, cap, knew, vnew, q = build_replicas(tq, synth, bits, R)
+    ctx, reps, cap, knew, vnew, q, inputs = build_replicas(tq, synth, bits, R)
     scale = 1.0 / math.sqrt(D)
     ws = torch.zeros(tq.tq_decode_workspace_size(ctx, B, HQ, HKV, SEQ) // 4 + 64, dtype=torch.float32, device="cuda")
     out = torch.empty((B, HQ, D), dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
 
-    def decode_step(r, with_append=True):
+    def decode_step(r, with_append=True, bufs=None):
         K, V = reps[r]
+        qq, kk, vv, oo, ww = bufs or (q, knew, vnew, out, ws)
         if with_append:  # one launch: encode the new token's K/V into slot SEQ-1, then attend
-            tq.tq_decode_step(ctx, ctx, q, knew, vnew, K, V, B, HQ, HKV, SEQ, cap, scale, out, ws)
+            tq.tq_decode_step(ctx, ctx, qq, kk, vv, K, V, B, HQ, HKV, SEQ, cap, scale, oo, ww)
         else:
-            tq.tq_decode_attention(ctx, ctx, q, K, V, B, HQ, HKV, SEQ, cap, scale, out, ws)
+            tq.tq_decode_attention(ctx, ctx, qq, K, V, B, HQ, HKV, SEQ, cap, scale, oo, ww)
 
     # eager warm-up (sets kernel attributes outside capture), then graphs
     with torch.cuda.stream(stream):
@@ -228,11 +239,19 @@ def run_tq(args, world, rank, local):
     with torch.cuda.graph(g_attn, stream=stream):
         for r in range(R):
             decode_step(r, with_append=False)
+    # end to end: replicas alternate between two streams, each with its own
+    # input block, output and workspace, so one replica's copies overlap
+    # another's decode (the replicas are independent caches)
+    inputs2 = torch.empty_like(inputs)
+    nq, nk = q.numel(), knew.numel()
+    sets = [(q, knew, vnew, out, ws, inputs),
+            (inputs2[:nq].view_as(q), inputs2[nq:nq + nk].view_as(knew), inputs2[nq + nk:].view_as(vnew),
+             torch.empty_like(out), torch.zeros_like(ws), inputs2)]
     g_one = []
     for r in range(R):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            decode_step(r)
+            decode_step(r, bufs=sets[r % 2][:5])
         g_one.append(g)
     torch.cuda.synchronize()
     assert ctx.poll() == tq.TQ_OK
@@ -276,22 +295,25 @@ def run_tq(args, world, rank, local):
     achieved = attn_bytes / (attn_us * 1e-6) / 1e9
 
     # ---------------- end to end through the C ABI with host buffers
-    q_h = torch.empty_like(q, device="cpu").pin_memory()
-    q_h.copy_(q.cpu())
-    kn_h = knew.cpu().pin_memory()
-    vn_h = vnew.cpu().pin_memory()
-    out_h = torch.empty((B, HQ, D), dtype=torch.float32).pin_memory()
+    in_h = inputs.cpu().pin_memory()  # q, k_new, v_new of a step, one pinned block
+    out_h = [torch.empty((B, HQ, D), dtype=torch.float32).pin_memory() for _ in range(2)]
+    streams = [stream, torch.cuda.Stream()]
     e2e_steps = max(3, min(args.steps, 100))
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(e2e_steps):
-            for r in range(R):
-                q.copy_(q_h, non_blocking=True)
-                knew.copy_(kn_h, non_blocking=True)
-                vnew.copy_(vn_h, non_blocking=True)
+    streams[1].wait_event(e0)
+    for _ in range(e2e_steps):
+        for r in range(R):
+            st_r, bs = streams[r % 2], sets[r % 2]
+            with torch.cuda.stream(st_r):
+                bs[5].copy_(in_h, non_blocking=True)
                 g_one[r].replay()
-                out_h.copy_(out, non_blocking=True)
+                out_h[r % 2].copy_(bs[3], non_blocking=True)
+    done1 = torch.cuda.Event()
+    done1.record(streams[1])
+    stream.wait_event(done1)
+    with torch.cuda.stream(stream):
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
