@@ -299,8 +299,10 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
   // kStages tiles in flight (a 128K-token layer: 66.7 against 67.7 us).  A
   // template choice: one loop holding both orders scheduled worse than either.
   constexpr bool shallow = SH;
-  // vector index of token 0 of the group's cache head (virtual heads share one)
-  const int cgrp = b * (p.Hkv >> p.kv_shift) + (kvh >> p.kv_shift);
+  // vector index of token 0 of the group's cache head (virtual heads, plain
+  // MSE caches only, share one; the others keep grp, which the register-bound
+  // 3.5-bit kernel needs: 16.5 against 18.3 us per call with the shift)
+  const int cgrp = (MX || Q) ? grp : b * (p.Hkv >> p.kv_shift) + (kvh >> p.kv_shift);
   const int64_t gbase = (int64_t)cgrp * p.cap;
   const int new_tile = (int)((p.seq - 1) / kTileTok), new_row = (int)((p.seq - 1) % kTileTok);
   const bool owner = append && new_tile >= t_begin && new_tile < t_end;
