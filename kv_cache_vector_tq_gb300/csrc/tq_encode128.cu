@@ -309,6 +309,23 @@ __device__ __forceinline__ void mix_chunk_codes(const uint32_t (&a)[32], const f
   flagged = dmin < mg;
 }
 
+// Half (16 coordinates) of a b + 1/2-bit chunk: codes at mixed_pos(j, BM) of
+// a 64-bit group (8·(2·BM + 1) bits), distances folded into dmin.
+template <int BM>
+__device__ __forceinline__ uint64_t mix_half_codes(const uint32_t (&a)[16], const float (&tlo)[kTB<BM>],
+                                                   const float (&thi)[kTB<BM + 1>], float& dmin) {
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float x = __uint_as_float(a[j]);
+    if ((j & 8) == 0)
+      put_bits<BM + 1>(w, mixed_pos(j, BM), bucketize_sc<BM + 1>(x, thi, dmin));
+    else
+      put_bits<BM>(w, mixed_pos(j, BM), bucketize_sc<BM>(x, tlo, dmin));
+  }
+  return (uint64_t)w[0] | ((uint64_t)w[1] << 32);
+}
+
 // Near-threshold flags of a b + 1/2-bit chunk, each coordinate against its own codebook.
 template <int BM>
 __device__ __forceinline__ uint32_t mix_near_mask(const uint32_t (&a)[32], float f, const float (&tlo)[15],
@@ -736,8 +753,9 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
       // b = 4 plain MSE: eight columns per trip of a rolled loop (the unrolled
       // 32-column bucketize overflows the instruction cache at 7 thresholds)
       constexpr bool kGroups = !PROD && !MIX && !PAIRL && BM == 4;
-      uint32_t a0[kGroups ? 1 : 32];
-      if constexpr (!kGroups) {
+      constexpr bool kMixHalves = MIX && BM == 3;  // 3.5 bits: two rolled halves of 16 columns
+      uint32_t a0[(kGroups || kMixHalves) ? 1 : 32];
+      if constexpr (!kGroups && !kMixHalves) {
         tmem_ld32_nw(acc + 32 * c0, a0);
         tmem_wait_ld();
       }
@@ -753,7 +771,42 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
       for (int w = 0; w < (MIX ? BM + 1 : 1); ++w) hw[w] = 0u;
       float g2 = 0.f;
       uint32_t m32;
-      if constexpr (MIX) {
+      if constexpr (kMixHalves) {
+        bool flagged = false;
+        float tlo[kTB<BM>], thi[kTB<BM + 1>];
+        scaled_thresholds<BM>(p.thr, inv, tlo);
+        scaled_thresholds<BM + 1>(p.thr_hi, inv, thi);
+        float dmin = INFINITY;
+        constexpr int HB = 8 * (2 * BM + 1);  // bits of a half
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+          uint32_t a16[16];
+          tmem_ld16_nw(acc + 32 * c0 + 16 * g, a16);
+          tmem_wait_ld();
+          const uint64_t cv = mix_half_codes<BM>(a16, tlo, thi, dmin);
+          if (g == 0) {
+            hw[0] |= (uint32_t)cv;
+            hw[1] |= (uint32_t)(cv >> 32);
+          } else {  // bits HB .. 2·HB of the chunk
+#pragma unroll
+            for (int w = 0; w <= BM; ++w) {
+              const int lo = 32 * w - HB;  // bit of cv at the start of word w
+              uint32_t x = 0u;
+              if (lo >= 0 && lo < 64) x = (uint32_t)(cv >> lo);
+              if (lo < 0 && lo > -32) x = (uint32_t)(cv << (-lo));
+              hw[w] |= x;
+            }
+          }
+        }
+        flagged = dmin < mg;
+        m32 = 0u;
+        if (__any_sync(kFull, flagged && live)) {  // rare: the flags, from tensor memory again
+          uint32_t t32[32];
+          tmem_ld32_nw(acc + 32 * c0, t32);
+          tmem_wait_ld();
+          if (flagged) m32 = mix_near_mask<BM>(t32, f, p.thr, p.thr_hi);
+        }
+      } else if constexpr (MIX) {
         bool flagged = false;
         float tlo[kTB<BM>], thi[kTB<BM + 1>];
         scaled_thresholds<BM>(p.thr, inv, tlo);
