@@ -309,6 +309,24 @@ __device__ __forceinline__ void mix_chunk_codes(const uint32_t (&a)[32], const f
   flagged = dmin < mg;
 }
 
+// 2·BM + 1 halfwords h (the low ones of words w[0..BM]) to halfword address
+// dst: word stores where the start is word-aligned, else one halfword first
+// (fewer partial-sector writes than one store per halfword).
+template <int BM>
+__device__ __forceinline__ void store_halfwords(uint16_t* dst, const uint32_t (&w)[BM + 1]) {
+  if ((reinterpret_cast<uintptr_t>(dst) & 3u) == 0u) {
+    uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
+#pragma unroll
+    for (int k = 0; k < BM; ++k) d32[k] = w[k];
+    dst[2 * BM] = (uint16_t)w[BM];
+  } else {
+    dst[0] = (uint16_t)w[0];
+    uint32_t* d32 = reinterpret_cast<uint32_t*>(dst + 1);
+#pragma unroll
+    for (int k = 0; k < BM; ++k) d32[k] = __funnelshift_r(w[k], w[k + 1], 16);
+  }
+}
+
 // Half (16 coordinates) of a b + 1/2-bit chunk: codes at mixed_pos(j, BM) of
 // a 64-bit group (8·(2·BM + 1) bits), distances folded into dmin.
 template <int BM>
@@ -959,88 +977,87 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
             atomicOr(blk + BM + w, phi[w]);
           }
         }
-      } else if (MIX && p.layout == TQ_LAYOUT_TOKEN) {
-        if (valid) {
-          uint16_t* dst = reinterpret_cast<uint16_t*>(p.codes + dv * p.W) + c0 * HW;
-#pragma unroll
-          for (int k = 0; k < HW; ++k) dst[k] = (uint16_t)(hw[k >> 1] >> (16 * (k & 1)));
-        }
-      } else if (MIX) {
-        // PAIR: coordinate j's field of 2·w_j bits at block bit 2·P_j; the
-        // chunk's block is 2·HW halfwords from halfword 2·c0·HW.  Rows r and
-        // r+1 of the tile are lanes l and l+1; when the destination pairs them,
-        // the even lane writes the fields of coordinates 0-15 (halfwords
-        // [0, HW)), the odd lane those of 16-31 ([HW, 2·HW), the same offsets
-        // within), after one exchange.
-        uint32_t part[BM + 1];
-#pragma unroll
-        for (int w = 0; w <= BM; ++w) part[w] = __shfl_xor_sync(kFull, hw[w], 1);
-        const int64_t base_row = row - (even ? 0 : 1);
-        const bool whole = p.pair_aligned && base_row + 1 < p.N;
-        uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)p.W) + c0 * HW;
-        if (valid && whole) {
-          // the even and odd vectors' codes of this lane's 16 coordinates
-          // (the odd lane's start 8·HW bits into the chunk)
-          constexpr int K = 8 * HW;
-          uint32_t E[BM + 1], O[BM + 1], ev[BM + 1], od[BM + 1], ob[BM + 1];
-#pragma unroll
-          for (int w = 0; w <= BM; ++w) {
-            E[w] = even ? hw[w] : part[w];
-            O[w] = even ? part[w] : hw[w];
+      } else if constexpr (MIX) {
+        if (p.layout == TQ_LAYOUT_TOKEN) {
+          if (valid) {
+            store_halfwords<BM>(reinterpret_cast<uint16_t*>(p.codes + dv * p.W) + c0 * HW, hw);
           }
+        } else {
+          // PAIR: coordinate j's field of 2·w_j bits at block bit 2·P_j; the
+          // chunk's block is 2·HW halfwords from halfword 2·c0·HW.  Rows r and
+          // r+1 of the tile are lanes l and l+1; when the destination pairs them,
+          // the even lane writes the fields of coordinates 0-15 (halfwords
+          // [0, HW)), the odd lane those of 16-31 ([HW, 2·HW), the same offsets
+          // within), after one exchange.
+          uint32_t part[BM + 1];
 #pragma unroll
-          for (int w = 0; w <= BM; ++w) {
-            const int lo = (K + 32 * w) >> 5, sh = (K + 32 * w) & 31;
-            uint32_t se = 0u, so = 0u;
-            if (lo <= BM) {
-              se = E[lo] >> sh;
-              so = O[lo] >> sh;
+          for (int w = 0; w <= BM; ++w) part[w] = __shfl_xor_sync(kFull, hw[w], 1);
+          const int64_t base_row = row - (even ? 0 : 1);
+          const bool whole = p.pair_aligned && base_row + 1 < p.N;
+          uint32_t* blk = p.codes + (dv >> 1) * (2 * (int64_t)p.W) + c0 * HW;
+          if (valid && whole) {
+            // the even and odd vectors' codes of this lane's 16 coordinates
+            // (the odd lane's start 8·HW bits into the chunk)
+            constexpr int K = 8 * HW;
+            uint32_t E[BM + 1], O[BM + 1], ev[BM + 1], od[BM + 1], ob[BM + 1];
+#pragma unroll
+            for (int w = 0; w <= BM; ++w) {
+              E[w] = even ? hw[w] : part[w];
+              O[w] = even ? part[w] : hw[w];
             }
-            if (sh != 0 && lo + 1 <= BM) {
-              se |= E[lo + 1] << (32 - sh);
-              so |= O[lo + 1] << (32 - sh);
+#pragma unroll
+            for (int w = 0; w <= BM; ++w) {
+              const int lo = (K + 32 * w) >> 5, sh = (K + 32 * w) & 31;
+              uint32_t se = 0u, so = 0u;
+              if (lo <= BM) {
+                se = E[lo] >> sh;
+                so = O[lo] >> sh;
+              }
+              if (sh != 0 && lo + 1 <= BM) {
+                se |= E[lo + 1] << (32 - sh);
+                so |= O[lo + 1] << (32 - sh);
+              }
+              ev[w] = even ? E[w] : se;
+              od[w] = even ? O[w] : so;
+              ob[w] = 0u;
             }
-            ev[w] = even ? E[w] : se;
-            od[w] = even ? O[w] : so;
-            ob[w] = 0u;
-          }
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int pk = mixed_pos(k, BM);
-            if ((k & 8) == 0) {
-              put_bits<BM + 1>(ob, 2 * pk, get_bits<BM + 1>(ev, pk));
-              put_bits<BM + 1>(ob, 2 * pk + BM + 1, get_bits<BM + 1>(od, pk));
-            } else {
-              put_bits<BM>(ob, 2 * pk, get_bits<BM>(ev, pk));
-              put_bits<BM>(ob, 2 * pk + BM, get_bits<BM>(od, pk));
+            for (int k = 0; k < 16; ++k) {
+              const int pk = mixed_pos(k, BM);
+              if ((k & 8) == 0) {
+                put_bits<BM + 1>(ob, 2 * pk, get_bits<BM + 1>(ev, pk));
+                put_bits<BM + 1>(ob, 2 * pk + BM + 1, get_bits<BM + 1>(od, pk));
+              } else {
+                put_bits<BM>(ob, 2 * pk, get_bits<BM>(ev, pk));
+                put_bits<BM>(ob, 2 * pk + BM, get_bits<BM>(od, pk));
+              }
             }
-          }
-          uint16_t* dst = reinterpret_cast<uint16_t*>(blk) + (even ? 0 : HW);
+            uint16_t* dst = reinterpret_cast<uint16_t*>(blk) + (even ? 0 : HW);
+            store_halfwords<BM>(dst, ob);
+          } else if (valid) {
+            // the partner is written by another call (or not at all): this
+            // vector's fields of the chunk's HW block words by masked atomics
+            // (word by word: only the fields overlapping word w, a compile-time
+            // test once both loops are unrolled; the slot picks the shift)
+            const bool odd = (dv & 1) != 0;
+            auto shift = [](uint32_t x, int sh) -> uint32_t {
+              return sh >= 32 || sh <= -32 ? 0u : (sh >= 0 ? x << sh : x >> (-sh));
+            };
 #pragma unroll
-          for (int k = 0; k < HW; ++k) dst[k] = (uint16_t)(ob[k >> 1] >> (16 * (k & 1)));
-        } else if (valid) {
-          // the partner is written by another call (or not at all): this
-          // vector's fields of the chunk's HW block words by masked atomics
-          // (word by word: only the fields overlapping word w, a compile-time
-          // test once both loops are unrolled; the slot picks the shift)
-          const bool odd = (dv & 1) != 0;
-          auto shift = [](uint32_t x, int sh) -> uint32_t {
-            return sh >= 32 || sh <= -32 ? 0u : (sh >= 0 ? x << sh : x >> (-sh));
-          };
+            for (int w = 0; w < HW; ++w) {
+              uint32_t fb = 0u, mb = 0u;
 #pragma unroll
-          for (int w = 0; w < HW; ++w) {
-            uint32_t fb = 0u, mb = 0u;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const int wk = (k & 8) ? BM : BM + 1, pk = mixed_pos(k, BM);
-              const int p0 = 2 * pk - 32 * w;  // the pair field of coordinate k, relative to word w
-              if (p0 >= 32 || p0 + 2 * wk <= 0) continue;
-              const int sh = odd ? p0 + wk : p0;
-              fb |= shift(get_bits_rt(hw, pk, wk), sh);
-              mb |= shift((1u << wk) - 1u, sh);
+              for (int k = 0; k < 32; ++k) {
+                const int wk = (k & 8) ? BM : BM + 1, pk = mixed_pos(k, BM);
+                const int p0 = 2 * pk - 32 * w;  // the pair field of coordinate k, relative to word w
+                if (p0 >= 32 || p0 + 2 * wk <= 0) continue;
+                const int sh = odd ? p0 + wk : p0;
+                fb |= shift(get_bits_rt(hw, pk, wk), sh);
+                mb |= shift((1u << wk) - 1u, sh);
+              }
+              atomicAnd(blk + w, ~mb);
+              atomicOr(blk + w, fb);
             }
-            atomicAnd(blk + w, ~mb);
-            atomicOr(blk + w, fb);
           }
         }
       } else if (p.layout == TQ_LAYOUT_TOKEN) {
