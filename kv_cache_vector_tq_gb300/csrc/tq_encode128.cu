@@ -309,21 +309,59 @@ __device__ __forceinline__ void mix_chunk_codes(const uint32_t (&a)[32], const f
   flagged = dmin < mg;
 }
 
+// BM consecutive words to dst (4-byte aligned) in the widest aligned vector
+// stores: one lane's codes of a chunk are contiguous, and every store
+// instruction of a warp touches a sector per lane, so fewer, wider stores
+// write fewer partial sectors.
+template <int BM>
+__device__ __forceinline__ void store_words(uint32_t* dst, const uint32_t (&w)[BM]) {
+  const uint32_t al = (uint32_t)reinterpret_cast<uintptr_t>(dst) & 15u;
+  if constexpr (BM == 1) {
+    dst[0] = w[0];
+  } else if constexpr (BM == 2) {
+    if ((al & 7u) == 0u) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    } else {
+      dst[0] = w[0];
+      dst[1] = w[1];
+    }
+  } else if constexpr (BM == 3) {
+    if ((al & 7u) == 0u) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+      dst[2] = w[2];
+    } else {
+      dst[0] = w[0];
+      *reinterpret_cast<uint2*>(dst + 1) = make_uint2(w[1], w[2]);
+    }
+  } else {
+    if (al == 0u) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if ((al & 7u) == 0u) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+      *reinterpret_cast<uint2*>(dst + 2) = make_uint2(w[2], w[3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dst[k] = w[k];
+    }
+  }
+}
+
 // 2·BM + 1 halfwords h (the low ones of words w[0..BM]) to halfword address
 // dst: word stores where the start is word-aligned, else one halfword first
 // (fewer partial-sector writes than one store per halfword).
 template <int BM>
 __device__ __forceinline__ void store_halfwords(uint16_t* dst, const uint32_t (&w)[BM + 1]) {
+  uint32_t v[BM];
   if ((reinterpret_cast<uintptr_t>(dst) & 3u) == 0u) {
-    uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
 #pragma unroll
-    for (int k = 0; k < BM; ++k) d32[k] = w[k];
+    for (int k = 0; k < BM; ++k) v[k] = w[k];
+    store_words<BM>(reinterpret_cast<uint32_t*>(dst), v);
     dst[2 * BM] = (uint16_t)w[BM];
   } else {
     dst[0] = (uint16_t)w[0];
-    uint32_t* d32 = reinterpret_cast<uint32_t*>(dst + 1);
 #pragma unroll
-    for (int k = 0; k < BM; ++k) d32[k] = __funnelshift_r(w[k], w[k + 1], 16);
+    for (int k = 0; k < BM; ++k) v[k] = __funnelshift_r(w[k], w[k + 1], 16);
+    store_words<BM>(reinterpret_cast<uint32_t*>(dst + 1), v);
   }
 }
 
@@ -958,8 +996,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
 #pragma unroll
         for (int w = 0; w < BM; ++w) ow[w] = (even ? plo[w] : phi[w]) | __shfl_xor_sync(kFull, even ? phi[w] : plo[w], 1);
         if (valid && whole) {
-#pragma unroll
-          for (int w = 0; w < BM; ++w) blk[(even ? 0 : BM) + w] = ow[w];
+          store_words<BM>(blk + (even ? 0 : BM), ow);
         } else if (valid) {
           // the partner is written by another call (or not at all): this
           // vector's slots of the 2·BM block words by masked atomics
@@ -1063,8 +1100,12 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
       } else if (p.layout == TQ_LAYOUT_TOKEN) {
         if (valid) {
           uint32_t* dst = p.codes + dv * p.W + c0 * BM;
+          if constexpr (BM == 3) {  // three word stores measured faster here than 8 + 4 bytes
 #pragma unroll
-          for (int w = 0; w < BM; ++w) dst[w] = cw[w];
+            for (int w = 0; w < BM; ++w) dst[w] = cw[w];
+          } else {
+            store_words<BM>(dst, cw);
+          }
         }
       } else {
         // PAIR: vectors 2k and 2k+1 share a block; coordinate j's two codes
@@ -1089,8 +1130,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
             put_bits<BM>(ow, 2 * jj * BM, even ? own : prt);
             put_bits<BM>(ow, (2 * jj + 1) * BM, even ? prt : own);
           }
-#pragma unroll
-          for (int w = 0; w < BM; ++w) blk[(even ? 0 : BM) + w] = ow[w];
+          store_words<BM>(blk + (even ? 0 : BM), ow);
         } else if (valid) {
           // the partner is written by another call (or not at all): this
           // vector's fields of the chunk's 2·BM block words by masked atomics
