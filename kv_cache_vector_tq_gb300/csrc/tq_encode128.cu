@@ -1170,16 +1170,20 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
         if (!__all_sync(kFull, bar_wait(a2_empty, ((uint32_t)i & 1u) ^ 1u, abort_flag, p.status, lim))) break;
         tc_fence_after();
         const uint32_t a2 = tmem + lane_base + L::ColA2;
-        {
-          uint32_t hi[16], lo[16];
+        // two halves of 16 columns (8 packed words each), so that the
+        // temporaries of the split stay within the register budget
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int j = 8 * hf + jj;
             const float r0 = (__uint_as_float(a0[2 * j]) * f - cen_s[get_bits<BM>(cw, 2 * j * BM)]) * rsd;
             const float r1 = (__uint_as_float(a0[2 * j + 1]) * f - cen_s[get_bits<BM>(cw, (2 * j + 1) * BM)]) * rsd;
-            split2(r0, r1, hi[j], lo[j]);
+            split2(r0, r1, hi[jj], lo[jj]);
           }
-          tmem_st16(a2 + 16 * c0, hi);
-          tmem_st16(a2 + 64 + 16 * c0, lo);
+          tmem_st8(a2 + 16 * c0 + 8 * hf, hi);
+          tmem_st8(a2 + 64 + 16 * c0 + 8 * hf, lo);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -1187,12 +1191,15 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
         if (lane == 0) mbar_arrive(a2_full);
         if (!__all_sync(kFull, bar_wait(acc2_full, (uint32_t)i & 1u, abort_flag, p.status, lim))) break;
         tc_fence_after();
-        uint32_t pa[32];
-        tmem_ld32_nw(tmem + lane_base + L::ColAcc2 + 32 * c0, pa);
-        tmem_wait_ld();
         uint32_t bits = 0u;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) bits |= (__uint_as_float(pa[j]) >= 0.f ? 1u : 0u) << j;
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pa[16];
+          tmem_ld16_nw(tmem + lane_base + L::ColAcc2 + 32 * c0 + 16 * hf, pa);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) bits |= (__uint_as_float(pa[j]) >= 0.f ? 1u : 0u) << (16 * hf + j);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc2_empty);
