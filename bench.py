@@ -20,7 +20,8 @@ e2e      = the same metric with the step inputs (query, new K/V token: one
            pinned host block, one copy) copied from pinned host memory and the
            output copied back every decode step; the replicas alternate between
            two streams with their own buffers, so one replica's copies overlap
-           another's decode.
+           another's decode, and a benchmark step (copies included) replays as
+           one CUDA graph.
 roofline = one decode-attention call alone (the same kernel without the
            append: query rotation, tiles and merge in one launch) against the
            measured HBM copy peak; traffic = its DRAM bytes per launch from the
@@ -247,12 +248,26 @@ def run_tq(args, world, rank, local):
     sets = [(q, knew, vnew, out, ws, inputs),
             (inputs2[:nq].view_as(q), inputs2[nq:nq + nk].view_as(knew), inputs2[nq + nk:].view_as(vnew),
              torch.empty_like(out), torch.zeros_like(ws), inputs2)]
-    g_one = []
-    for r in range(R):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            decode_step(r, bufs=sets[r % 2][:5])
-        g_one.append(g)
+    in_h = inputs.cpu().pin_memory()  # q, k_new, v_new of a step, one pinned block
+    out_h = [torch.empty((B, HQ, D), dtype=torch.float32).pin_memory() for _ in range(2)]
+    side = torch.cuda.Stream()
+    # one benchmark step end to end, as one graph: per replica the copy of its
+    # inputs from pinned host memory, the decode step and the copy of its
+    # output back, the replicas alternating between two streams
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        side.wait_event(fork)
+        for r in range(R):
+            st_r, bs = (stream, side)[r % 2], sets[r % 2]
+            with torch.cuda.stream(st_r):
+                bs[5].copy_(in_h, non_blocking=True)
+                decode_step(r, bufs=bs[:5])
+                out_h[r % 2].copy_(bs[3], non_blocking=True)
+        join = torch.cuda.Event()
+        join.record(side)
+        stream.wait_event(join)
     torch.cuda.synchronize()
     assert ctx.poll() == tq.TQ_OK
 
@@ -295,25 +310,14 @@ def run_tq(args, world, rank, local):
     achieved = attn_bytes / (attn_us * 1e-6) / 1e9
 
     # ---------------- end to end through the C ABI with host buffers
-    in_h = inputs.cpu().pin_memory()  # q, k_new, v_new of a step, one pinned block
-    out_h = [torch.empty((B, HQ, D), dtype=torch.float32).pin_memory() for _ in range(2)]
-    streams = [stream, torch.cuda.Stream()]
     e2e_steps = max(3, min(args.steps, 100))
+    with torch.cuda.stream(stream):
+        g_e2e.replay()  # untimed
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         e0.record(stream)
-    streams[1].wait_event(e0)
-    for _ in range(e2e_steps):
-        for r in range(R):
-            st_r, bs = streams[r % 2], sets[r % 2]
-            with torch.cuda.stream(st_r):
-                bs[5].copy_(in_h, non_blocking=True)
-                g_one[r].replay()
-                out_h[r % 2].copy_(bs[3], non_blocking=True)
-    done1 = torch.cuda.Event()
-    done1.record(streams[1])
-    stream.wait_event(done1)
-    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            g_e2e.replay()
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
