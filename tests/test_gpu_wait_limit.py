@@ -64,7 +64,9 @@ def test_encoder_wait_limit_zero_times_out_then_recovers(d, b, mode, f16):
 
 @pytest.mark.parametrize("mode", [tq.TQ_MSE, tq.TQ_PROD])
 def test_scorer_wait_limit_zero_times_out_then_recovers(mode):
-    d, b, n, M = 128, 3, 1000, 5
+    # 9 queries: past the one-launch scorer for up to 8 (it has no pipeline
+    # waits), so the tensor-core scorer with its bounded waits runs
+    d, b, n, M = 128, 3, 1000, 9
     ctx, clean = _pair(32, d, b, mode)
     keys = torch.from_numpy(synth.unit_rows(32, n, d)).cuda()
     cs = tq.CodeSet(clean, n)
