@@ -437,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_umma_kernel(const UmmaPara
     // ---------------- producer
     uint32_t i = 0;
     bool ok = true;
+    const uint64_t pol_b = l2_policy_evict_last();
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       const int64_t row0 = t / nob * kTM;
       const int ob = (int)(t % nob);
@@ -451,11 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1) encode_umma_kernel(const UmmaPara
           // rows past N read as zeros and still count toward the box's bytes
           mbar_arrive_expect_tx(&x_full[s], (uint32_t)XL::Stage);
           mbar_arrive_expect_tx(&b_full[s], (uint32_t)kBStage);
+          // the Π tiles are read by every CTA again and again: keep them in L2
+          // (a row tile is read once per output block by CTAs that run about
+          // together, so the rows take the default policy: marked evict-first
+          // they were fetched from DRAM again for every block)
 #pragma unroll
           for (int bx = 0; bx < XL::Boxes; ++bx)
             tma_load_2d(sX + s * XL::Stage + bx * (kTM * 128), &xmap, kc * kKC + bx * XL::BoxCols, (int)row0,
                         &x_full[s]);
-          bulk_g2s(sB + s * kBStage, p.btab + ((int64_t)ob * nkc + kc) * kBStage, kBStage, &b_full[s]);
+          bulk_g2s_hint(sB + s * kBStage, p.btab + ((int64_t)ob * nkc + kc) * kBStage, kBStage, &b_full[s], pol_b);
         }
         __syncwarp();
       }
