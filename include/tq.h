@@ -114,7 +114,7 @@ tq_status tq_rotation_haar(int d, const double* h_G, double* h_Pi);
  *           j of Π·u takes b + 1 bits where j mod 16 < 8 and b bits elsewhere,
  *           each half with the Lloyd-Max codebook of its own width (which half
  *           is immaterial: the coordinates of Π·u are exchangeable); b = 1..3
- *           (1.5, 2.5 or 3.5 bits), d = 128, TQ_ROT_DENSE only.
+ *           (1.5, 2.5 or 3.5 bits), d = 128 (either rotation).
  * rot_kind  TQ_ROT_DENSE: h_rot is Π, d×d row-major fp64 (e.g. from
  *           tq_rotation_haar).  TQ_ROT_HADAMARD: h_rot is the sign vector σ
  *           (d entries ±1) and Π = H·diag(σ)/√d, H the Sylvester Hadamard

@@ -441,7 +441,7 @@ tq_status tq_ctx_create(int d, int b, int mode, int rot_kind, const double* h_ro
   const bool mixed = mode == TQ_MIXED;
   if (mixed && (cb[1].d != d || cb[1].b != b + 1)) return TQ_ERR_INVALID_ARG;
   // b + 1/2 bits: the tensor-memory encoder, the scorer and decode at d = 128
-  if (mixed && (d != kChunk || rot_kind != TQ_ROT_DENSE)) return TQ_ERR_UNSUPPORTED;
+  if (mixed && d != kChunk) return TQ_ERR_UNSUPPORTED;  // the d = 128 encoder, scorer and decode
   if (mode == TQ_PROD && !h_S) return TQ_ERR_INVALID_ARG;
   if (mode == TQ_PROD && d > kChunk) return TQ_ERR_UNSUPPORTED;
   int hm = 0;

@@ -103,6 +103,22 @@ def test_hadamard_fast_transform_fp16_rows():
     check(cs, Pi, X.astype(np.float32), 3)
 
 
+@pytest.mark.parametrize("b", [2, 3, 4])
+@pytest.mark.parametrize("f16", [False, True])
+def test_hadamard_d128_pair_layout(b, f16):
+    """d = 128 Hadamard contexts into PAIR caches (the tensor-memory encoder's
+    slot-placed kernel with H·D/√d as its matrix), an odd row count."""
+    ctx, Pi = hadamard_pair(9, 128, b)
+    X = synth.gaussian_rows(9, 333, 128, outlier_cols=4, outlier_scale=10.0)
+    if f16:
+        X = X.astype(np.float16)
+    cs = tq.CodeSet(ctx, X.shape[0], tq.TQ_LAYOUT_PAIR)
+    tq.tq_encode(ctx, torch.from_numpy(np.ascontiguousarray(X)).cuda(), cs)
+    torch.cuda.synchronize()
+    assert ctx.poll() == tq.TQ_OK
+    check(cs, Pi, X.astype(np.float32), b)
+
+
 @pytest.mark.parametrize("d", [256, 3072])
 def test_hadamard_extreme_magnitudes(d):
     """Rows scaled by 1e-20, 1e-25 and 1e22 and rows with a single non-zero

@@ -56,6 +56,42 @@ def oracle_codes(X, Pi, b):
     return idx, s, band
 
 
+@pytest.mark.parametrize("b", [1, 3])
+def test_mixed_encode_hadamard(b):
+    """b + 1/2 bits with the randomized Hadamard rotation (d = 128: the
+    tensor-memory encoder with H·D/√d), fp16 rows, both layouts."""
+    sg = synth.hadamard_signs(5, D)
+    ctx = tq.Context(D, b, tq.TQ_MIXED, tq.TQ_ROT_HADAMARD, sg)
+    Pi = orot.hadamard_rotation(D, sg)
+    K, V = synth.kv_layer(5, 0, 1, 2, 500, D)
+    for arr, layout in ((K, tq.TQ_LAYOUT_TOKEN), (V, tq.TQ_LAYOUT_PAIR)):
+        X = arr.reshape(-1, D)
+        cs = tq.CodeSet(ctx, X.shape[0], layout)
+        tq.tq_encode(ctx, torch.from_numpy(np.ascontiguousarray(X)).cuda(), cs)
+        torch.cuda.synchronize()
+        assert ctx.poll() == tq.TQ_OK
+        idx, s, band = oracle_codes(X.astype(np.float32), Pi, b)
+        got = tq.tq_unpack_indices(cs).astype(np.int64)
+        assert not ((got != idx) & ~band).any()
+        np.testing.assert_allclose(cs.norm[:X.shape[0]].cpu().numpy().astype(np.float64), s, rtol=1e-6, atol=0)
+    # scores over the TOKEN keys against the oracle's dequantization
+    Q = synth.queries(5, 3, D)
+    out = torch.empty((3, X.shape[0]), dtype=torch.float32, device="cuda")
+    Kc = tq.CodeSet(ctx, X.shape[0], tq.TQ_LAYOUT_TOKEN)
+    Kx = K.reshape(-1, D)
+    tq.tq_encode(ctx, torch.from_numpy(np.ascontiguousarray(Kx)).cuda(), Kc)
+    ws = torch.empty(tq.tq_scores_workspace_size(ctx, 3) // 4 + 4, dtype=torch.float32, device="cuda")
+    tq.tq_scores(ctx, torch.from_numpy(np.ascontiguousarray(Q)).cuda(), Kc, out, ws)
+    torch.cuda.synchronize()
+    assert ctx.poll() == tq.TQ_OK
+    lo, hi = codebooks(b)
+    idx = tq.tq_unpack_indices(Kc).astype(np.int64)
+    Xh = oq.mixed_dequantize(idx, Kc.norm[:Kx.shape[0]].cpu().numpy().astype(np.float64), Pi, lo, hi, b, math.sqrt(D))
+    ref = Q.astype(np.float64) @ Xh.T
+    bound = 1e-4 * np.linalg.norm(Q, axis=1)[:, None] * np.linalg.norm(Kx.astype(np.float64), axis=1)[None, :]
+    assert (np.abs(out.cpu().numpy().astype(np.float64) - ref) <= bound).all()
+
+
 def words_of(cs, n_words):
     return cs.codes.view(torch.int32).cpu().numpy().view(np.uint32)[:n_words]
 
