@@ -202,13 +202,19 @@ def test_mixed_scores(b, N, M):
     assert (np.abs(got - ref) <= bound).all(), f"max err/bound {np.max(np.abs(got - ref) / bound)}"
 
 
-def run_decode_mixed(b, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float16):
+def hadamard_mixed_pair(seed, b):
+    sg = synth.hadamard_signs(seed, D)
+    return tq.Context(D, b, tq.TQ_MIXED, tq.TQ_ROT_HADAMARD, sg), orot.hadamard_rotation(D, sg)
+
+
+def run_decode_mixed(b, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float16, hadamard=False):
     """Decode attention over b + 1/2-bit K (TOKEN) and V (PAIR) caches, each with
-    its own Haar rotation, against fp64 attention over the oracle's
-    dequantization of the GPU's own codes (2e-3·‖out‖ per head)."""
+    its own Haar (or randomized Hadamard) rotation, against fp64 attention over
+    the oracle's dequantization of the GPU's own codes (2e-3·‖out‖ per head)."""
     cap = cap or (seq + 15) // 16 * 16
-    kctx, Pk = mixed_pair(seed, b)
-    vctx, Pv = mixed_pair(seed + 1000, b)
+    make = hadamard_mixed_pair if hadamard else mixed_pair
+    kctx, Pk = make(seed, b)
+    vctx, Pv = make(seed + 1000, b)
     Kh, Vh = synth.kv_layer(seed, 0, B, Hkv, seq, D)
     Kc = tq.CodeSet(kctx, B * Hkv * cap, tq.TQ_LAYOUT_TOKEN)
     Vc = tq.CodeSet(vctx, B * Hkv * cap, tq.TQ_LAYOUT_PAIR)
@@ -237,6 +243,13 @@ def run_decode_mixed(b, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float16
     rel = np.linalg.norm(got - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
     assert rel.max() <= 2e-3, f"max per-head relative error {rel.max()}"
     return rel.max()
+
+
+@pytest.mark.parametrize("b", [2, 3])
+def test_mixed_decode_hadamard(b):
+    """b + 1/2-bit caches with randomized Hadamard rotations: GQA 4, a ragged
+    sequence."""
+    run_decode_mixed(b, 1, 16, 4, 3001, seed=8, hadamard=True)
 
 
 @pytest.mark.parametrize("b", [1, 2, 3])
