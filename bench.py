@@ -375,8 +375,8 @@ def _summary(sub_line, keep=()):
     r = sub_line.get("roofline") or {}
     out = {"workload": sub_line["config"]["workload"], "metric": sub_line["metric"], "value": sub_line["value"],
            "unit": sub_line["unit"], "ms_per_step": sub_line["ms_per_step"], "steps": sub_line["steps"],
-           "roofline": {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac", "kernel", "peak_kind")
-                        if k in r},
+           "roofline": {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic", "kernel",
+                                          "peak_kind") if k in r},
            "clocks": sub_line.get("clocks")}
     for k in keep:
         if k in sub_line["config"]:
