@@ -112,7 +112,6 @@ struct Enc128Params {
   float thr[15];
   float cen[16];
   float thr_hi[15];  // b + 1/2 bits: the (BM+1)-bit codebook's thresholds
-  int sym;           // thresholds symmetric about 0 (Prod keys also take general ones)
   int layout, W, QW, pair_aligned;
   int64_t offset, group_rows, group_stride;
   int* status;
@@ -129,37 +128,25 @@ __device__ __forceinline__ int64_t dest_row(const Enc128Params& p, int64_t r) {
 // Branch-free bucketize against thresholds held as kernel constants (every
 // index is known at compile time, so no shared-memory loads and no dependent
 // chain): code = #{k : v >= t_k}, near = v lies within m of some threshold.
-// Symmetric codebooks (the ones tq_codebook_build makes) compare |v| with the
-// H = 2^(BM-1) - 1 positive thresholds only; a value exactly equal to a
-// negative threshold then counts as below it, which differs from the
-// definition only at exact ties, all inside the band that parity excuses.
-template <int BM, bool SYM>
+// The codebooks this kernel serves are symmetric (the ones tq_codebook_build
+// makes), so |v| is compared with the H = 2^(BM-1) - 1 positive thresholds
+// only; a value exactly equal to a negative threshold then counts as below
+// it, which differs from the definition only at exact ties, all inside the
+// band that parity excuses.
+template <int BM>
 __device__ __forceinline__ uint32_t bucketize_c(float v, const float (&thr)[15], float m, bool& near) {
   constexpr int H = (1 << (BM - 1)) - 1;
-  if constexpr (SYM) {
-    const float a = fabsf(v);
-    float dmin = a;
-    int n = 0;
+  const float a = fabsf(v);
+  float dmin = a;
+  int n = 0;
 #pragma unroll
-    for (int j = 0; j < H; ++j) {
-      const float dj = a - thr[H + 1 + j];
-      dmin = fminf(dmin, fabsf(dj));
-      n += dj >= 0.f ? 1 : 0;
-    }
-    near = dmin < m;
-    return v >= 0.f ? (uint32_t)(H + 1 + n) : (uint32_t)(H - n);
-  } else {
-    float dmin = INFINITY;
-    int n = 0;
-#pragma unroll
-    for (int k = 0; k < 2 * H + 1; ++k) {
-      const float dk = v - thr[k];
-      dmin = fminf(dmin, fabsf(dk));
-      n += dk >= 0.f ? 1 : 0;
-    }
-    near = dmin < m;
-    return (uint32_t)n;
+  for (int j = 0; j < H; ++j) {
+    const float dj = a - thr[H + 1 + j];
+    dmin = fminf(dmin, fabsf(dj));
+    n += dj >= 0.f ? 1 : 0;
   }
+  near = dmin < m;
+  return v >= 0.f ? (uint32_t)(H + 1 + n) : (uint32_t)(H - n);
 }
 
 // Symmetric bucketize without a per-coordinate near test: code of v from the
@@ -238,52 +225,32 @@ __device__ __forceinline__ uint32_t near_mask(const uint32_t (&a)[32], float f, 
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     bool near;
-    bucketize_c<BM, true>(__uint_as_float(a[j]) * f, thr, kMargin, near);
+    bucketize_c<BM>(__uint_as_float(a[j]) * f, thr, kMargin, near);
     m32 |= (near ? 1u : 0u) << j;
   }
   return m32;
 }
 
-// One 32-column chunk of a row's accumulator: its BM code words (coordinate j
-// of the chunk at bits j·BM), the near-threshold flags, and (Prod) the sum of
-// squared residuals in v units.  Symmetric codebooks test the whole chunk for
-// a coordinate near a threshold at once (`flagged`) and leave the flags to
-// the caller, which finds them in the rare chunks that have one.
-template <int BM, bool SYM, bool PROD>
-__device__ __forceinline__ uint32_t chunk_codes(const uint32_t (&a)[32], float f, const float (&thr)[15],
-                                                const float* cen_s, uint32_t (&cw)[BM], float& g2,
-                                                bool& flagged) {
-  uint32_t m32 = 0u;
+// One 32-column chunk of the Prod encoder's (b-1)-bit MSE stage: its BM code
+// words (coordinate j at bits j·BM), the sum of squared residuals in v units
+// (for γ), and `flagged` when a coordinate of the chunk lies near a threshold
+// (the caller finds which in the rare chunks that have one).
+template <int BM>
+__device__ __forceinline__ void prod_chunk_codes(const uint32_t (&a)[32], float f, const float (&thr)[15],
+                                                 const float* cen_s, uint32_t (&cw)[BM], float& g2,
+                                                 bool& flagged) {
 #pragma unroll
   for (int w = 0; w < BM; ++w) cw[w] = 0u;
-  if constexpr (SYM) {
-    float dmin = INFINITY;
+  float dmin = INFINITY;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float v = __uint_as_float(a[j]) * f;
-      const uint32_t code = bucketize_fold<BM>(v, thr, dmin);
-      put_bits<BM>(cw, j * BM, code);
-      if constexpr (PROD) {
-        const float rr = v - cen_s[code];
-        g2 = fmaf(rr, rr, g2);
-      }
-    }
-    flagged = dmin < kMargin;
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float v = __uint_as_float(a[j]) * f;
-      bool near;
-      const uint32_t code = bucketize_c<BM, false>(v, thr, kMargin, near);
-      m32 |= (near ? 1u : 0u) << j;
-      put_bits<BM>(cw, j * BM, code);
-      if constexpr (PROD) {
-        const float rr = v - cen_s[code];
-        g2 = fmaf(rr, rr, g2);
-      }
-    }
+  for (int j = 0; j < 32; ++j) {
+    const float v = __uint_as_float(a[j]) * f;
+    const uint32_t code = bucketize_fold<BM>(v, thr, dmin);
+    put_bits<BM>(cw, j * BM, code);
+    const float rr = v - cen_s[code];
+    g2 = fmaf(rr, rr, g2);
   }
-  return m32;
+  flagged = dmin < kMargin;
 }
 
 // b + 1/2 bits per coordinate: coordinate j (0..31) of a 32-column chunk has
@@ -392,9 +359,9 @@ __device__ __forceinline__ uint32_t mix_near_mask(const uint32_t (&a)[32], float
     const float v = __uint_as_float(a[j]) * f;
     bool near;
     if ((j & 8) == 0)
-      bucketize_c<BM + 1, true>(v, thi, kMargin, near);
+      bucketize_c<BM + 1>(v, thi, kMargin, near);
     else
-      bucketize_c<BM, true>(v, tlo, kMargin, near);
+      bucketize_c<BM>(v, tlo, kMargin, near);
     m32 |= (near ? 1u : 0u) << j;
   }
   return m32;
@@ -914,7 +881,8 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode128_kernel(const Enc128P
           chunk_codes_s<BM>(a0, tb, mg, cw, flagged);
           m32 = 0u;
         } else {
-          m32 = chunk_codes<BM, true, PROD>(a0, f, p.thr, cen_s, cw, g2, flagged);
+          prod_chunk_codes<BM>(a0, f, p.thr, cen_s, cw, g2, flagged);
+          m32 = 0u;
         }
         // a chunk with a coordinate near a threshold (~1e-3 of them): its
         // values again from tensor memory (not yet handed back), then the flags
@@ -1298,7 +1266,6 @@ tq_status launch_encode128(const DevCtx& c, const void* x, int x_dtype, int64_t 
   for (int k = 0; k < 16; ++k) p.cen[k] = c.cen[k];
   for (int k = 0; k < 15; ++k) p.thr_hi[k] = c.thr_hi[k];
   const bool mix = c.mode == TQ_MIXED;
-  p.sym = c.sym_thr;
   p.layout = out->layout;
   p.W = c.words_per_vec;
   p.QW = c.qjl_words_per_vec;
