@@ -422,12 +422,26 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
         // BK + 1 words from the word holding the lane's first bit (bit
         // 16·(2·BK + 1)·t of a K row, ·g of a V pair block)
         const int ko = (t * (2 * BK + 1)) >> 1, vo = (g * (2 * BK + 1)) >> 1;
+        if constexpr (BK == 2) {
+          // 2.5 bits: four words from the even (8-byte aligned) word at or
+          // below the first, in two 8-byte copies (rows of 10 words, pair
+          // blocks of 20: every lane's four words stay inside its row/block)
+          const int ke = ko & ~1, ve = vo & ~1;
 #pragma unroll
-        for (int w = 0; w <= BK; ++w) {
-          cp_async4(st + 0 * kFieldBytes + lane * 16 + 4 * w, p.kcodes + (vb + g) * WX + ko + w);
-          cp_async4(st + 1 * kFieldBytes + lane * 16 + 4 * w, p.kcodes + (vb + g + 8) * WX + ko + w);
-          cp_async4(st + 2 * kFieldBytes + lane * 16 + 4 * w, p.vcodes + (vb + 2 * t) * WX + vo + w);
-          cp_async4(st + 3 * kFieldBytes + lane * 16 + 4 * w, p.vcodes + (vb + 2 * t + 8) * WX + vo + w);
+          for (int w = 0; w < 2; ++w) {
+            cp_async8(st + 0 * kFieldBytes + lane * 16 + 8 * w, p.kcodes + (vb + g) * WX + ke + 2 * w);
+            cp_async8(st + 1 * kFieldBytes + lane * 16 + 8 * w, p.kcodes + (vb + g + 8) * WX + ke + 2 * w);
+            cp_async8(st + 2 * kFieldBytes + lane * 16 + 8 * w, p.vcodes + (vb + 2 * t) * WX + ve + 2 * w);
+            cp_async8(st + 3 * kFieldBytes + lane * 16 + 8 * w, p.vcodes + (vb + 2 * t + 8) * WX + ve + 2 * w);
+          }
+        } else {
+#pragma unroll
+          for (int w = 0; w <= BK; ++w) {
+            cp_async4(st + 0 * kFieldBytes + lane * 16 + 4 * w, p.kcodes + (vb + g) * WX + ko + w);
+            cp_async4(st + 1 * kFieldBytes + lane * 16 + 4 * w, p.kcodes + (vb + g + 8) * WX + ko + w);
+            cp_async4(st + 2 * kFieldBytes + lane * 16 + 4 * w, p.vcodes + (vb + 2 * t) * WX + vo + w);
+            cp_async4(st + 3 * kFieldBytes + lane * 16 + 4 * w, p.vcodes + (vb + 2 * t + 8) * WX + vo + w);
+          }
         }
       } else {
         copy_words<BK>(st + 0 * kFieldBytes + lane * 16, p.kcodes + (vb + g) * WK + t * BK);
@@ -676,10 +690,26 @@ __global__ void __launch_bounds__(W * 32, 1) decode_step_kernel(const StepParams
     const unsigned char* st = my_stage + (j % kStages) * SB;
     constexpr int KN = MX ? BK + 1 : BK, VN = MX ? BV + 1 : BV;
     uint32_t k0[KN], k1[KN], v0w[VN], v1w[VN];
-    read_words<KN>(k0, st + 0 * kFieldBytes + lane * 16);
-    read_words<KN>(k1, st + 1 * kFieldBytes + lane * 16);
-    read_words<VN>(v0w, st + 2 * kFieldBytes + lane * 16);
-    read_words<VN>(v1w, st + 3 * kFieldBytes + lane * 16);
+    if constexpr (MX && BK == 2) {  // drop the leading word where the first one was odd
+      uint32_t a[4], b2[4], c[4], d[4];
+      read_words<4>(a, st + 0 * kFieldBytes + lane * 16);
+      read_words<4>(b2, st + 1 * kFieldBytes + lane * 16);
+      read_words<4>(c, st + 2 * kFieldBytes + lane * 16);
+      read_words<4>(d, st + 3 * kFieldBytes + lane * 16);
+      const bool kodd = ((t * 5) >> 1) & 1, vodd = ((g * 5) >> 1) & 1;
+#pragma unroll
+      for (int w = 0; w < 3; ++w) {
+        k0[w] = kodd ? a[w + 1] : a[w];
+        k1[w] = kodd ? b2[w + 1] : b2[w];
+        v0w[w] = vodd ? c[w + 1] : c[w];
+        v1w[w] = vodd ? d[w + 1] : d[w];
+      }
+    } else {
+      read_words<KN>(k0, st + 0 * kFieldBytes + lane * 16);
+      read_words<KN>(k1, st + 1 * kFieldBytes + lane * 16);
+      read_words<VN>(v0w, st + 2 * kFieldBytes + lane * 16);
+      read_words<VN>(v1w, st + 3 * kFieldBytes + lane * 16);
+    }
     if constexpr (MX) {  // bring the lane's first bit to bit 0 (odd t for K, odd g for V)
       const uint32_t ks = (uint32_t)(t & 1) * 16u, vs = (uint32_t)(g & 1) * 16u;
 #pragma unroll
