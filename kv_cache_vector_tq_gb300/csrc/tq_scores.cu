@@ -233,10 +233,14 @@ __global__ void __launch_bounds__(kThreads, 1) scores_kernel(const ScoreParams p
 #pragma unroll
         for (int k8 = 0; k8 < 16; ++k8) {
           const uint32_t byte = (sb[k8 >> 2] >> (8 * (k8 & 3))) & 0xFFu;
+          // bit i of the byte at i and at i + 15: shifted left by 15 - 2e, bit
+          // 2e lands on 15 and bit 2e + 1 on 31, the sign bits of the word's
+          // two fp16 halves
+          const uint32_t sp = byte | (byte << 15);
           uint32_t v[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)  // −1 in both halves; bit 1 flips its half to +1
-            v[e] = 0xBC00BC00u ^ (((byte >> (2 * e)) & 1u) << 15) ^ (((byte >> (2 * e + 1)) & 1u) << 31);
+            v[e] = ((sp << (15 - 2 * e)) & 0x80008000u) ^ 0xBC00BC00u;
           *reinterpret_cast<uint4*>(A + core_off(r, 128 + 8 * k8)) = make_uint4(v[0], v[1], v[2], v[3]);
         }
       }
