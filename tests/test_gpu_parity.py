@@ -506,21 +506,27 @@ def test_decode_asymmetric_bits():
 def test_decode_hadamard_rotation(b):
     """Decode attention over K/V caches encoded with the randomized Hadamard
     rotation Π = H·diag(σ)/√d ("TurboQuant 和 RotorQuant 的真相", chapter 7,
-    WHT vs random rotation): keys by the fast-transform encoder, values (PAIR
-    layout) by the dense encoder with the same Π; the oracle rotates with its
+    WHT vs random rotation): keys (TOKEN) and values (PAIR) by the d = 128
+    tensor-memory encoder with the materialized Π; the oracle rotates with its
     own Hadamard matrix."""
     run_decode(b, b, 1, 32, 8, 3001, seed=5, rot="hadamard")
 
 
-def run_decode_prod(b_k, b_v, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float16):
+def test_decode_hadamard_gqa8_long():
+    """8 query heads per KV head over a Hadamard-rotated cache longer than
+    4096 tokens (the 8-head kernel)."""
+    run_decode(3, 3, 1, 64, 8, 8191, seed=6, rot="hadamard")
+
+
+def run_decode_prod(b_k, b_v, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.float16, rot="dense"):
     """Decode attention with TurboQuant_Prod keys ((b_k - 1)-bit MSE codes plus
     QJL sign bits and γ) and TurboQuant_MSE values, against attention over the
     explicitly dequantized Prod keys x̂ = s·(Πᵀŷ + γ·√(π/2)/d·Sᵀ·sign) built
     from the GPU's own codes."""
     d = 128
     cap = cap or (seq + 15) // 16 * 16
-    kctx, Pi_k, S = make_pair(seed, d, b_k, tq.TQ_PROD)
-    vctx, Pi_v, _ = make_pair(seed + 100, d, b_v)
+    kctx, Pi_k, S = make_pair(seed, d, b_k, tq.TQ_PROD, rot=rot)
+    vctx, Pi_v, _ = make_pair(seed + 100, d, b_v, rot=rot)
     Kh, Vh = synth.kv_layer(seed, 0, B, Hkv, seq, d)
     Kc = tq.CodeSet(kctx, B * Hkv * cap, tq.TQ_LAYOUT_TOKEN)
     Vc = tq.CodeSet(vctx, B * Hkv * cap, tq.TQ_LAYOUT_PAIR)
@@ -569,6 +575,12 @@ def run_decode_prod(b_k, b_v, B, Hq, Hkv, seq, cap=None, seed=0, q_dtype=torch.f
 ])
 def test_decode_prod_keys(b_k, b_v, B, Hq, Hkv, seq):
     run_decode_prod(b_k, b_v, B, Hq, Hkv, seq)
+
+
+def test_decode_prod_keys_hadamard():
+    """Prod keys and MSE values with randomized Hadamard rotations (the Prod
+    stage's S·Πᵀ built from the materialized H·D/√d)."""
+    run_decode_prod(3, 3, 1, 16, 4, 2001, seed=12, rot="hadamard")
 
 
 def test_decode_prod_keys_rejected_where_unsupported():
