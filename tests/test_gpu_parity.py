@@ -425,6 +425,18 @@ def test_scores_small_query_counts(b, M, prod, first, N):
     assert (np.abs(got - ref) <= bound).all(), f"max err/bound {np.max(np.abs(got - ref) / bound)}"
 
 
+@pytest.mark.parametrize("prod", [False, True])
+@pytest.mark.parametrize("M", [3, 70])
+def test_scores_hadamard(prod, M):
+    """Scores over keys encoded with the randomized Hadamard rotation, through
+    the one-launch scorer (3 queries) and the tensor-core scorer (70)."""
+    d, b = 128, 3
+    ctx, Pi, S = make_pair(44, d, b, tq.TQ_PROD if prod else tq.TQ_MSE, rot="hadamard")
+    X = synth.unit_rows(44, 999, d) if prod else synth.gaussian_rows(44, 999, d, outlier_cols=4, outlier_scale=20.0)
+    Q = synth.queries(44, M, d)
+    _scores_check(ctx, Pi, S, X, Q, b - 1 if prod else b, prod)
+
+
 def test_scores_prod_config3_sample():
     ctx, Pi, S = make_pair(0, 128, 3, tq.TQ_PROD)
     X = synth.unit_rows(0, 8192, 128)
