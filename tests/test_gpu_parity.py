@@ -157,6 +157,24 @@ def test_encode_extreme_magnitudes():
     check_mse_encode(ctx, Pi, X, 3, cs)
 
 
+def test_encode_fp16_extreme_rows():
+    """fp16 rows at the ends of the fp16 range, which the tensor cores take
+    unscaled: full of 65504, of subnormals (6e-8), a single subnormal, a zero
+    row, and mixed magnitudes."""
+    d, b = 128, 3
+    ctx, Pi, _ = make_pair(45, d, b)
+    X = synth.gaussian_rows(45, 40, d).astype(np.float16)
+    X[0] = np.float16(65504.0) * np.sign(X[0] + np.float16(1e-3))
+    X[1] = np.float16(6e-8) * np.sign(X[1] + np.float16(1e-3))
+    X[2] = 0.0
+    X[2, 17] = np.float16(6e-8)
+    X[3] = 0.0
+    X[4, :64] = np.float16(65504.0)
+    X[4, 64:] = np.float16(1e-4)
+    cs = gpu_encode(ctx, X)
+    check_mse_encode(ctx, Pi, X.astype(np.float32), b, cs)
+
+
 @pytest.mark.parametrize("b", [2, 3, 4])
 def test_encode_fp16_kv_token_and_pair_layouts(b):
     """fp16 K/V with 4 outlier channels x10 (the KV workloads), both layouts."""
