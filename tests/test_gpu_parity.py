@@ -246,12 +246,18 @@ def test_encode_append_mapping_pair_layout():
         np.testing.assert_allclose(cs.norm[blk * cap: blk * cap + 40].cpu().numpy(), s_ref[blk * 40:(blk + 1) * 40], rtol=1e-6)
 
 
-def test_encode_prod_config3_sample():
-    """TurboQuant_Prod b=3 (2-bit MSE + 1-bit QJL), unit-norm Gaussian keys."""
-    d, b, N = 128, 3, 20000
+@pytest.mark.parametrize("b,f16", [(3, False), (3, True), (2, True), (4, False)])
+def test_encode_prod_config3_sample(b, f16):
+    """TurboQuant_Prod (b - 1-bit MSE + 1-bit QJL), unit-norm Gaussian keys, fp32
+    and fp16 rows (the fp16 instance reads the rows straight from the TMA tile)."""
+    d, N = 128, 20000
     ctx, Pi, S = make_pair(0, d, b, tq.TQ_PROD)
     X = synth.unit_rows(0, N, d)
-    cs = gpu_encode(ctx, X)
+    if f16:
+        X = X.astype(np.float16).astype(np.float32)
+        cs = gpu_encode(ctx, X.astype(np.float16))
+    else:
+        cs = gpu_encode(ctx, X)
     cb = oracle_codebook(d, b - 1)
     e = oq.prod_quantize(X.astype(np.float64), Pi, S, cb["centroids"], math.sqrt(d))
     band = oq.near_threshold(e["v"], cb["centroids"])
