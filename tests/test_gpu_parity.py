@@ -528,14 +528,21 @@ def test_decode_gqa_variants(gqa):
 @pytest.mark.parametrize("b_k,b_v,B,Hq,Hkv,seq", [(3, 3, 1, 32, 4, 6007), (4, 4, 1, 64, 8, 5000),
                                                    (4, 2, 2, 16, 2, 9001)])
 def test_decode_gqa8_long(b_k, b_v, B, Hq, Hkv, seq):
-    """8 query heads per KV head over caches past 4096 tokens (the K/V warp
-    pairs: one warp scores and runs the softmax, its partner sums P·V), table
-    and byte-row lookups, asymmetric bits, ragged last tiles."""
+    """8 query heads per KV head over caches past 4096 tokens (the 8-head
+    kernel, 8 warps per SM), table and byte-row lookups, asymmetric bits,
+    ragged last tiles."""
     run_decode(b_k, b_v, B, Hq, Hkv, seq)
 
 
 def test_decode_asymmetric_bits():
     run_decode(4, 2, 1, 16, 4, 2048)
+
+
+@pytest.mark.parametrize("b_k,b_v,Hq,Hkv,seq", [(1, 1, 32, 8, 4099), (1, 3, 16, 4, 2001), (3, 1, 64, 8, 5003)])
+def test_decode_one_bit(b_k, b_v, Hq, Hkv, seq):
+    """1-bit keys and/or values (sign codes, centroids ±√(2/π)): GQA 4 and 8,
+    asymmetric widths, ragged lengths."""
+    run_decode(b_k, b_v, 1, Hq, Hkv, seq)
 
 
 @pytest.mark.parametrize("b", [2, 3, 4])
